@@ -1,0 +1,187 @@
+/*
+ * zeta.h -- C ABI of the ZETA hot path on one GB300 (sm_103a).
+ *
+ * Method: "ZETA: Leveraging Z-order Curves for Efficient Top-k Attention"
+ * (arXiv 2501.14577).  Queries and keys live in a low-dimensional space
+ * (d_K = 3 by default), are quantised and bit-interleaved into one-dimensional
+ * Z-order (Morton) codes, keys are sorted for every chunk-aligned causal prefix,
+ * each query takes the k keys around its insertion rank in that order, and the
+ * selected keys plus the query's own-chunk causal keys are combined with the
+ * Adaptive Cauchy-softmax into a weighted sum of values.
+ *
+ * Conventions shared by every call
+ *   - Every tensor is a contiguous row-major device array with the batch and
+ *     head dimensions leading: [B, H, N, ...].  One (b, h) pair is a "slice";
+ *     slices are independent except that the gamma gradient sums over b.
+ *   - The caller owns and allocates every buffer, workspaces included (sizes
+ *     come from the *_bytes / *_entries queries).  The library never allocates,
+ *     never synchronises the stream and keeps no global state.
+ *   - Work is enqueued on the given stream (0 = legacy default stream).  A
+ *     returned ZETA_OK means the arguments were valid and the launches were
+ *     enqueued; device-side findings are written to *dev_status when a status
+ *     word is given (read it after synchronising).
+ *   - Arguments are checked before anything is launched.  An empty problem
+ *     (B*H*N == 0) is valid and launches nothing.
+ *   - Code width: codes are uint32 when d_K*bits <= 32, else uint64.
+ *   - Limits: 1 <= d_K <= 8, 1 <= bits <= 24, d_K*bits <= 64, C >= 1, C | N,
+ *     1 <= k <= C, 1 <= d_V <= 256, N < 2^31; zeta_sort_chunks also needs
+ *     N / C <= 1024.
+ */
+#ifndef ZETA_H
+#define ZETA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZETA_OK = 0,
+    ZETA_ERR_INVALID_ARG = 1,     /* null pointer, bad size, C not dividing N, ...  */
+    ZETA_ERR_UNSUPPORTED = 2,     /* valid request outside the implemented limits   */
+    ZETA_ERR_WORKSPACE = 3,       /* workspace missing or smaller than required      */
+    ZETA_ERR_CUDA = 4,            /* a launch failed (cudaGetLastError was not 0)    */
+    ZETA_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device wait gave up (status word)     */
+    ZETA_ERR_BOUNDS = 6           /* an index outside its legal range (status word)  */
+} zeta_status_t;
+
+typedef enum { ZETA_F32 = 0, ZETA_BF16 = 1 } zeta_dtype_t;
+
+/* Problem statement: B batch, H heads, N tokens, d_K query/key width, d_V value
+ * width, k window length, C chunk length, bits grid bits per coordinate,
+ * v_dtype element type of v / out / dout / dv, flags reserved (pass 0).
+ * These are the quantities the pages use to state the method: the 12-bit grid
+ * and d_K = 3 (OpenReview reply A2 "Clarification of Binary Expansion and
+ * Precision"), the chunk count and d_K = d_Q = 3 (reply A2 "Details about
+ * experiments"), k and the trainable gamma (reply A2 "Discussion on its
+ * robustness"). */
+typedef struct {
+    int32_t B, H, N, d_K, d_V, k, C, bits;
+    int32_t v_dtype;
+    uint32_t flags;
+} zeta_problem_t;
+
+/* Bytes per Z-order code (4 or 8); 0 when the problem is invalid. */
+size_t zeta_code_bytes(const zeta_problem_t *p);
+
+/* Entries T of the prefix table of one slice: C * n * (n - 1) / 2 with
+ * n = N / C.  Prefix c (c = 1..n-1) occupies entries [C*c*(c-1)/2, +c*C).
+ * Returns -1 when the problem is invalid. */
+int64_t zeta_prefix_entries(const zeta_problem_t *p);
+
+/* Workspace bytes needed by zeta_sort_chunks / zeta_attend_bwd (0 if invalid). */
+size_t zeta_sort_workspace_bytes(const zeta_problem_t *p);
+size_t zeta_bwd_workspace_bytes(const zeta_problem_t *p);
+
+/* Human-readable name of a status code (static storage). */
+const char *zeta_status_string(zeta_status_t s);
+
+/*
+ * zeta_encode -- Z-order code of every token.
+ * Passage: OpenReview reply A2 "Clarification of Binary Expansion and
+ * Precision" (normalise each coordinate to [0, 1], discretise to a grid of
+ * 2^bits cells, interleave the bits of the d_K cell indices), and the reply on
+ * dimension-ordering asymmetry (coordinate order K^1, K^2, K^3).
+ * Reading: the normalisation is the fixed map [-1, 1) -> [0, 1); in float32,
+ * t = (x + 1) * 2^(bits-1), u = min(max(floor(t), 0), 2^bits - 1) (NaN -> 0);
+ * bit j of coordinate d goes to code bit j*d_K + (d_K - 1 - d).
+ *   x      in : float  [B, H, N, d_K]
+ *   codes  out: uint32 or uint64 (see zeta_code_bytes) [B, H, N]
+ * Errors: ZETA_ERR_INVALID_ARG on null pointers or invalid sizes.
+ */
+zeta_status_t zeta_encode(const zeta_problem_t *p, const float *x, void *codes,
+                          cudaStream_t stream);
+
+/*
+ * zeta_sort_chunks -- sorted key order of every chunk-aligned causal prefix.
+ * Passage: OpenReview reply A3 "Chunking ... & Where efficiency is coming from"
+ * (radix sort of the Z-order codes) and the atlas.scime.ai summary, "Approach"
+ * (sort and chunk keys so every query searches its past in parallel).
+ * Prefix c holds the keys of chunks 0..c-1 ordered by (code, token index).
+ *   key_codes     in : codes of the keys [B, H, N]
+ *   prefix_codes  out: same code type [B, H, T]      (T = zeta_prefix_entries)
+ *   prefix_idx    out: int32 token indices [B, H, T]
+ *   workspace     scratch of at least zeta_sort_workspace_bytes, 256-B aligned
+ * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED (N / C > 1024),
+ *         ZETA_ERR_WORKSPACE (missing or too small).
+ */
+zeta_status_t zeta_sort_chunks(const zeta_problem_t *p, const void *key_codes,
+                               void *prefix_codes, int32_t *prefix_idx,
+                               void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * zeta_select_topk -- the k keys around each query's insertion rank.
+ * Passage: OpenReview reply A3 (binary search of the insertion position) and
+ * reply A2 "Clarification" (the window centred at the insertion position).
+ * For query i in chunk c >= 1, with M = c*C: r = number of prefix-c keys whose
+ * code is <= the query's code; start = min(max(r - ceil(k/2), 0), M - k); the
+ * row is prefix_idx[prefix c][start .. start + k).  Chunk-0 rows are all -1.
+ *   q_codes       in : codes of the queries [B, H, N]
+ *   prefix_codes  in : from zeta_sort_chunks
+ *   prefix_idx    in : from zeta_sort_chunks
+ *   idx           out: int32 [B, H, N, k]
+ * Errors: ZETA_ERR_INVALID_ARG.
+ */
+zeta_status_t zeta_select_topk(const zeta_problem_t *p, const void *q_codes,
+                               const void *prefix_codes, const int32_t *prefix_idx,
+                               int32_t *idx, cudaStream_t stream);
+
+/*
+ * zeta_attend_fwd -- Adaptive Cauchy-softmax over the selected keys.
+ * Passage: OpenReview reply A2 "Discussion on its robustness" (trainable gamma,
+ * Cauchy softmax), reply A3 "Justification for Euclidean Distance Claim", and
+ * the atlas.scime.ai summary, "Approach".
+ * The attended set of query i in chunk c is its window (non-negative entries
+ * of idx row i) plus every key j of its own chunk with cC <= j <= i.  With
+ * w_ij = 1 / (1 + |q_i - k_j|^2 / gamma_h^2) and s_i = sum_j w_ij:
+ * out_i = sum_j w_ij v_j / s_i, rowsum_i = s_i.
+ *   q, k    in : float [B, H, N, d_K]
+ *   v       in : v_dtype [B, H, N, d_V]  (16-B aligned)
+ *   gamma   in : float [H]
+ *   idx     in : int32 [B, H, N, k]; entries must be -1 or in [0, cC)
+ *   out     out: v_dtype [B, H, N, d_V]  (16-B aligned)
+ *   rowsum  out: float [B, H, N]
+ *   dev_status  optional int32 device word; an idx entry outside its range is
+ *               skipped and ZETA_ERR_BOUNDS is recorded there.
+ * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED.
+ */
+zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, const float *k,
+                              const void *v, const float *gamma, const int32_t *idx,
+                              void *out, float *rowsum, int32_t *dev_status,
+                              cudaStream_t stream);
+
+/*
+ * zeta_attend_bwd -- gradients through the Cauchy weights, selection fixed.
+ * Passage: the forward/backward timings of the OpenReview replies A3/A4 (the
+ * method is trained end to end) and the forward definition above.
+ * With a_ij = w_ij / s_i, g_ij = dO_i . v_j and gbar_i = dO_i . out_i:
+ *   dL/dw_ij = (g_ij - gbar_i) / s_i
+ *   dq_i     = sum_j dL/dw_ij * (-2 w_ij^2 / gamma^2) (q_i - k_j)
+ *   dk_j     = sum_i dL/dw_ij * ( 2 w_ij^2 / gamma^2) (q_i - k_j)
+ *   dv_j     = sum_i a_ij dO_i
+ *   dgamma_h = sum_{b,i,j} dL/dw_ij * 2 w_ij (1 - w_ij) / gamma_h
+ *   out, rowsum  in : the forward's outputs
+ *   dout         in : v_dtype [B, H, N, d_V]
+ *   dq, dk       out: float [B, H, N, d_K]
+ *   dv           out: v_dtype [B, H, N, d_V]
+ *   dgamma       out: float [H]
+ *   workspace    scratch of at least zeta_bwd_workspace_bytes, 256-B aligned
+ * Every output is overwritten.  Reductions run in a fixed order, so results
+ * are bit-reproducible run to run.
+ * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED, ZETA_ERR_WORKSPACE.
+ */
+zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, const float *k,
+                              const void *v, const float *gamma, const int32_t *idx,
+                              const void *out, const float *rowsum, const void *dout,
+                              float *dq, float *dk, void *dv, float *dgamma,
+                              void *workspace, size_t ws_bytes, int32_t *dev_status,
+                              cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZETA_H */

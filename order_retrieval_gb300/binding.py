@@ -1,0 +1,232 @@
+"""Thin ctypes binding of libzeta.so with the same names as the C ABI.
+
+Each function only marshals arguments: it checks the torch tensors' dtype,
+shape, device and contiguity, then passes raw device pointers and the current
+CUDA stream to the library.  Every step of the path runs in the library's CUDA
+kernels; there is no fallback of any kind, and a missing library or a failed
+build raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+ZETA_F32 = 0
+ZETA_BF16 = 1
+
+STATUS = {
+    0: "ZETA_OK", 1: "ZETA_ERR_INVALID_ARG", 2: "ZETA_ERR_UNSUPPORTED", 3: "ZETA_ERR_WORKSPACE",
+    4: "ZETA_ERR_CUDA", 5: "ZETA_ERR_DEVICE_TIMEOUT", 6: "ZETA_ERR_BOUNDS",
+}
+
+HEADER = os.path.join(_build.ROOT, "include", "zeta.h")
+
+
+class ZetaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+class zeta_problem_t(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("d_K", ctypes.c_int32), ("d_V", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("C", ctypes.c_int32), ("bits", ctypes.c_int32), ("v_dtype", ctypes.c_int32),
+                ("flags", ctypes.c_uint32)]
+
+
+def problem(B, H, N, d_K, d_V, k, C, bits, v_dtype="bf16", flags=0) -> zeta_problem_t:
+    vd = {"f32": ZETA_F32, "bf16": ZETA_BF16, ZETA_F32: ZETA_F32, ZETA_BF16: ZETA_BF16}[v_dtype]
+    return zeta_problem_t(B, H, N, d_K, d_V, k, C, bits, vd, flags)
+
+
+def problem_of(w) -> zeta_problem_t:
+    """Problem struct of a workloads.Workload."""
+    return problem(w.B, w.H, w.N, w.d_K, w.d_V, w.k, w.C, w.bits, w.v_dtype)
+
+
+_lib = None
+
+
+def lib(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libzeta.so (building it in-tree first if needed)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"ZETA CUDA library not found at {path}")
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    PP = ctypes.POINTER(zeta_problem_t)
+    S = ctypes.c_int
+    L.zeta_code_bytes.argtypes = [PP]
+    L.zeta_code_bytes.restype = ctypes.c_size_t
+    L.zeta_prefix_entries.argtypes = [PP]
+    L.zeta_prefix_entries.restype = ctypes.c_int64
+    L.zeta_sort_workspace_bytes.argtypes = [PP]
+    L.zeta_sort_workspace_bytes.restype = ctypes.c_size_t
+    L.zeta_bwd_workspace_bytes.argtypes = [PP]
+    L.zeta_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.zeta_status_string.argtypes = [S]
+    L.zeta_status_string.restype = ctypes.c_char_p
+    L.zeta_encode.argtypes = [PP, P, P, P]
+    L.zeta_encode.restype = S
+    L.zeta_sort_chunks.argtypes = [PP, P, P, P, P, ctypes.c_size_t, P]
+    L.zeta_sort_chunks.restype = S
+    L.zeta_select_topk.argtypes = [PP, P, P, P, P, P]
+    L.zeta_select_topk.restype = S
+    L.zeta_attend_fwd.argtypes = [PP, P, P, P, P, P, P, P, P, P]
+    L.zeta_attend_fwd.restype = S
+    L.zeta_attend_bwd.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+    L.zeta_attend_bwd.restype = S
+    _lib = L
+    return L
+
+
+def header_functions() -> list:
+    """Names of the functions declared in include/zeta.h."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(zeta_[a-z_0-9]+)\s*\(", text)))
+
+
+# ------------------------------------------------------------- marshalling ---
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("ZETA tensors must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("ZETA tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, code):
+    if code != 0:
+        raise ZetaError(fn, code)
+
+
+def _expect(t, name, dtype, numel):
+    if t is None:
+        return
+    if t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+
+
+def code_dtype(p: zeta_problem_t):
+    return torch.int64 if p.d_K * p.bits > 32 else torch.int32
+
+
+def v_torch_dtype(p: zeta_problem_t):
+    return torch.bfloat16 if p.v_dtype == ZETA_BF16 else torch.float32
+
+
+def zeta_code_bytes(p: zeta_problem_t) -> int:
+    return lib().zeta_code_bytes(ctypes.byref(p))
+
+
+def zeta_prefix_entries(p: zeta_problem_t) -> int:
+    return lib().zeta_prefix_entries(ctypes.byref(p))
+
+
+def zeta_sort_workspace_bytes(p: zeta_problem_t) -> int:
+    return lib().zeta_sort_workspace_bytes(ctypes.byref(p))
+
+
+def zeta_bwd_workspace_bytes(p: zeta_problem_t) -> int:
+    return lib().zeta_bwd_workspace_bytes(ctypes.byref(p))
+
+
+def zeta_status_string(code: int) -> str:
+    return lib().zeta_status_string(code).decode()
+
+
+def zeta_encode(p, x, codes, stream=None):
+    S = p.B * p.H * p.N
+    _expect(x, "x", torch.float32, S * p.d_K)
+    _expect(codes, "codes", code_dtype(p), S)
+    _check("zeta_encode", lib().zeta_encode(ctypes.byref(p), _ptr(x), _ptr(codes), _stream(stream)))
+
+
+def zeta_sort_chunks(p, key_codes, prefix_codes, prefix_idx, workspace, stream=None):
+    S = p.B * p.H
+    T = zeta_prefix_entries(p)
+    _expect(key_codes, "key_codes", code_dtype(p), S * p.N)
+    _expect(prefix_codes, "prefix_codes", code_dtype(p), S * T)
+    _expect(prefix_idx, "prefix_idx", torch.int32, S * T)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("zeta_sort_chunks",
+           lib().zeta_sort_chunks(ctypes.byref(p), _ptr(key_codes), _ptr(prefix_codes),
+                                  _ptr(prefix_idx), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def zeta_select_topk(p, q_codes, prefix_codes, prefix_idx, idx, stream=None):
+    S = p.B * p.H
+    _expect(q_codes, "q_codes", code_dtype(p), S * p.N)
+    _expect(idx, "idx", torch.int32, S * p.N * p.k)
+    _check("zeta_select_topk",
+           lib().zeta_select_topk(ctypes.byref(p), _ptr(q_codes), _ptr(prefix_codes),
+                                  _ptr(prefix_idx), _ptr(idx), _stream(stream)))
+
+
+def zeta_attend_fwd(p, q, k, v, gamma, idx, out, rowsum, dev_status=None, stream=None):
+    S = p.B * p.H * p.N
+    vt = v_torch_dtype(p)
+    _expect(q, "q", torch.float32, S * p.d_K)
+    _expect(k, "k", torch.float32, S * p.d_K)
+    _expect(v, "v", vt, S * p.d_V)
+    _expect(gamma, "gamma", torch.float32, p.H)
+    _expect(idx, "idx", torch.int32, S * p.k)
+    _expect(out, "out", vt, S * p.d_V)
+    _expect(rowsum, "rowsum", torch.float32, S)
+    _expect(dev_status, "dev_status", torch.int32, 1)
+    _check("zeta_attend_fwd",
+           lib().zeta_attend_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                                 _ptr(idx), _ptr(out), _ptr(rowsum), _ptr(dev_status),
+                                 _stream(stream)))
+
+
+def zeta_attend_bwd(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv, dgamma, workspace,
+                    dev_status=None, stream=None):
+    S = p.B * p.H * p.N
+    vt = v_torch_dtype(p)
+    _expect(q, "q", torch.float32, S * p.d_K)
+    _expect(k, "k", torch.float32, S * p.d_K)
+    _expect(v, "v", vt, S * p.d_V)
+    _expect(gamma, "gamma", torch.float32, p.H)
+    _expect(idx, "idx", torch.int32, S * p.k)
+    _expect(out, "out", vt, S * p.d_V)
+    _expect(rowsum, "rowsum", torch.float32, S)
+    _expect(dout, "dout", vt, S * p.d_V)
+    _expect(dq, "dq", torch.float32, S * p.d_K)
+    _expect(dk, "dk", torch.float32, S * p.d_K)
+    _expect(dv, "dv", vt, S * p.d_V)
+    _expect(dgamma, "dgamma", torch.float32, p.H)
+    _expect(dev_status, "dev_status", torch.int32, 1)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("zeta_attend_bwd",
+           lib().zeta_attend_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                                 _ptr(idx), _ptr(out), _ptr(rowsum), _ptr(dout), _ptr(dq),
+                                 _ptr(dk), _ptr(dv), _ptr(dgamma), _ptr(workspace), ws_bytes,
+                                 _ptr(dev_status), _stream(stream)))

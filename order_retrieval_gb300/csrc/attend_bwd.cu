@@ -1,0 +1,319 @@
+// attend_bwd.cu -- gradients of the Cauchy-softmax attention, selection fixed.
+//
+// The pages time a forward+backward pass (OpenReview discussion of "ZETA:
+// Leveraging Z-order Curves for Efficient Top-k Attention", replies A3/A4 on
+// time and memory; atlas.scime.ai summary, "Measured effects", the sequence
+// length 65536 forward + backward row), so the method is trained end to end.
+// The window is not differentiated: idx is an input.
+//
+// With a_ij = w_ij / s_i, g_ij = dO_i . v_j, gbar_i = dO_i . out_i:
+//   dL/dw_ij = (g_ij - gbar_i) / s_i,   dw/d(d^2) = -w^2 / gamma^2,
+//   dw/dgamma = 2 w (1 - w) / gamma.
+// Query side (one warp per query): gbar_i, dq_i and the query's share of
+// dgamma.  Key side (one warp per key): dv_j and dk_j, reducing over the
+// queries that selected j.  Those are found through a transpose of idx built
+// by a stable radix sort of (key, query) pairs, so every key reads its
+// queries in ascending order and all sums run in a fixed order: the results
+// are bit-reproducible, with no floating-point atomics.  dgamma is summed per
+// head in double in a fixed order.
+#include "common.cuh"
+
+namespace zeta {
+namespace {
+
+__device__ __forceinline__ float dist2b(const float *a, const float *b, int dK) {
+    float d2 = 0.f;
+#pragma unroll
+    for (int d = 0; d < kMaxDK; ++d) {
+        if (d < dK) {
+            const float e = a[d] - b[d];
+            d2 = __fmaf_rn(e, e, d2);
+        }
+    }
+    return d2;
+}
+
+template <typename V>
+__device__ __forceinline__ float dot_row(const float *__restrict__ sm, const V *__restrict__ row,
+                                         int dV) {
+    float g = 0.f;
+    for (int e = 0; e < dV; ++e) g = __fmaf_rn(sm[e], VT<V>::ld(row + e), g);
+    return g;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+// ---------------------------------------------------------- query side ---
+
+template <typename V, int VPL>
+__global__ void __launch_bounds__(256)
+bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
+                  const V *__restrict__ v, const float *__restrict__ gamma,
+                  const int32_t *__restrict__ idx, const V *__restrict__ out,
+                  const float *__restrict__ rowsum, const V *__restrict__ dout,
+                  float *__restrict__ dq, float *__restrict__ gbar_out,
+                  float *__restrict__ dg_part, int32_t *status, int64_t S, int N, int H, int dK,
+                  int dV, int k, int C) {
+    __shared__ float sdo[8][kMaxDV];
+    const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    if (gw >= S * N) return;
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int64_t seg = gw / N;
+    const int i = (int)(gw % N);
+    const int64_t row = seg * N + i;
+    const float g = gamma[seg % H];
+    const float inv_g2 = __frcp_rn(g * g);
+    const float inv_g = __frcp_rn(g);
+    float qi[kMaxDK];
+#pragma unroll
+    for (int d = 0; d < kMaxDK; ++d) qi[d] = d < dK ? q[row * dK + d] : 0.f;
+    float gb = 0.f;
+    for (int e = lane; e < dV; e += 32) {
+        const float x = VT<V>::ld(dout + row * dV + e);
+        sdo[wib][e] = x;
+        gb = __fmaf_rn(x, VT<V>::ld(out + row * dV + e), gb);
+    }
+    gb = warp_sum(gb);
+    __syncwarp();
+    const float inv_s = __frcp_rn(rowsum[row]);
+    const float *kb = kx + seg * N * dK;
+    const V *vb = v + seg * N * dV;
+    const int cC = (i / C) * C;
+    float dqa[kMaxDK];
+#pragma unroll
+    for (int d = 0; d < kMaxDK; ++d) dqa[d] = 0.f;
+    float dgp = 0.f;
+    auto visit = [&](int j) {
+        const float *kj = kb + (int64_t)j * dK;
+        const float w = cauchy_w(dist2b(qi, kj, dK), inv_g2);
+        const float gij = dot_row<V>(sdo[wib], vb + (int64_t)j * dV, dV);
+        const float dldw = (gij - gb) * inv_s;
+        const float coef = dldw * (-2.f * w * w * inv_g2);
+#pragma unroll
+        for (int d = 0; d < kMaxDK; ++d)
+            if (d < dK) dqa[d] = __fmaf_rn(coef, qi[d] - kj[d], dqa[d]);
+        dgp = __fmaf_rn(dldw, 2.f * w * (1.f - w) * inv_g, dgp);
+    };
+    const int32_t *irow = idx + row * (int64_t)k;
+    for (int t = lane; t < k; t += 32) {
+        int j = irow[t];
+        if (j == -1) continue;
+        if (j < 0 || j >= cC) { set_status(status, ZETA_ERR_BOUNDS); continue; }
+        visit(j);
+    }
+    for (int j = cC + lane; j <= i; j += 32) visit(j);
+#pragma unroll
+    for (int d = 0; d < kMaxDK; ++d) dqa[d] = warp_sum(dqa[d]);
+    dgp = warp_sum(dgp);
+    if (lane == 0) {
+        for (int d = 0; d < dK; ++d) dq[row * dK + d] = dqa[d];
+        gbar_out[row] = gb;
+        dg_part[row] = dgp;
+    }
+}
+
+// ------------------------------------------------------------ key side ---
+
+// off[seg][j] = first position of key j in the sorted (key, query) list.
+__global__ void csr_offsets(const uint32_t *__restrict__ skeys, const uint32_t *__restrict__ seglen,
+                            int64_t stride, int N, uint32_t *__restrict__ off) {
+    const int64_t seg = blockIdx.y;
+    const int64_t L = seglen[seg];
+    const uint32_t *K = skeys + seg * stride;
+    uint32_t *o = off + seg * (int64_t)(N + 1);
+    for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p <= L;
+         p += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t hiK = p < L ? (int64_t)K[p] : (int64_t)N;
+        const int64_t loK = p > 0 ? (int64_t)K[p - 1] : -1;
+        for (int64_t j = loK + 1; j <= hiK; ++j) o[j] = (uint32_t)p;
+    }
+}
+
+template <typename V, int VPL>
+__global__ void __launch_bounds__(256)
+bwd_key_generic(const float *__restrict__ q, const float *__restrict__ kx,
+                const V *__restrict__ v, const float *__restrict__ gamma,
+                const float *__restrict__ rowsum, const V *__restrict__ dout,
+                const float *__restrict__ gbar, const uint32_t *__restrict__ csr_q,
+                const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
+                V *__restrict__ dv, int64_t S, int N, int H, int dK, int dV, int C) {
+    __shared__ float sv[8][kMaxDV];
+    const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    if (gw >= S * N) return;
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int64_t seg = gw / N;
+    const int j = (int)(gw % N);
+    const int64_t row = seg * N + j;
+    const float g = gamma[seg % H];
+    const float inv_g2 = __frcp_rn(g * g);
+    float kj[kMaxDK];
+#pragma unroll
+    for (int d = 0; d < kMaxDK; ++d) kj[d] = d < dK ? kx[row * dK + d] : 0.f;
+    for (int e = lane; e < dV; e += 32) sv[wib][e] = VT<V>::ld(v + row * dV + e);
+    __syncwarp();
+    const float *qb = q + seg * N * dK;
+    const V *dob = dout + seg * N * dV;
+    const float *rs = rowsum + seg * N;
+    const float *gbb = gbar + seg * N;
+    float acc[VPL];
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
+    float dka[kMaxDK];
+#pragma unroll
+    for (int d = 0; d < kMaxDK; ++d) dka[d] = 0.f;
+    // Lane handles query i (i < 0: none); then the warp adds a_ij dO_i rows.
+    auto step = [&](int i) {
+        float a = 0.f;
+        if (i >= 0) {
+            const float *qi = qb + (int64_t)i * dK;
+            const float w = cauchy_w(dist2b(qi, kj, dK), inv_g2);
+            const float inv_s = __frcp_rn(rs[i]);
+            a = w * inv_s;
+            const float gij = dot_row<V>(sv[wib], dob + (int64_t)i * dV, dV);
+            const float dldw = (gij - gbb[i]) * inv_s;
+            const float coef = dldw * (2.f * w * w * inv_g2);
+#pragma unroll
+            for (int d = 0; d < kMaxDK; ++d)
+                if (d < dK) dka[d] = __fmaf_rn(coef, qi[d] - kj[d], dka[d]);
+        }
+        for (int u = 0; u < 32; ++u) {
+            const float au = __shfl_sync(kFull, a, u);
+            const int iu = __shfl_sync(kFull, i, u);
+            if (iu < 0) continue;
+            const V *drow = dob + (int64_t)iu * dV;
+#pragma unroll
+            for (int e = 0; e < VPL; ++e) {
+                const int col = lane + 32 * e;
+                if (col < dV) acc[e] = __fmaf_rn(au, VT<V>::ld(drow + col), acc[e]);
+            }
+        }
+    };
+    const uint32_t *o = off + seg * (int64_t)(N + 1);
+    const int64_t b0 = o[j], b1 = o[j + 1];
+    const uint32_t *lst = csr_q + seg * csr_stride;
+    for (int64_t p0 = b0; p0 < b1; p0 += 32) {
+        const int64_t p = p0 + lane;
+        step(p < b1 ? (int)lst[p] : -1);
+    }
+    const int cend = (j / C + 1) * C;
+    for (int i0 = j; i0 < cend; i0 += 32) step(i0 + lane < cend ? i0 + lane : -1);
+#pragma unroll
+    for (int d = 0; d < kMaxDK; ++d) dka[d] = warp_sum(dka[d]);
+    if (lane == 0)
+        for (int d = 0; d < dK; ++d) dk[row * dK + d] = dka[d];
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) {
+        const int col = lane + 32 * e;
+        if (col < dV) VT<V>::st(dv + row * dV + col, acc[e]);
+    }
+}
+
+// dgamma[h] = sum over b and i of the per-query partials, in double, fixed order.
+__global__ void __launch_bounds__(256)
+dgamma_reduce(const float *__restrict__ part, int B, int H, int N, float *__restrict__ dgamma) {
+    __shared__ double red[256];
+    const int h = blockIdx.x;
+    double s = 0.0;
+    const int64_t total = (int64_t)B * N;
+    for (int64_t t = threadIdx.x; t < total; t += 256) {
+        const int64_t b = t / N, i = t % N;
+        s += (double)part[(b * H + h) * N + i];
+    }
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) dgamma[h] = (float)red[0];
+}
+
+struct BwdWs {
+    float *gbar;
+    float *dgp;
+    RadixWs rw;
+    uint32_t *off;
+};
+
+BwdWs carve_bwd(const Prob &p, void *base, size_t *bytes) {
+    Carver cv(base);
+    BwdWs w;
+    const int64_t rows = p.S * p.N;
+    const int64_t L = p.N * (int64_t)p.k;
+    w.gbar = cv.take<float>(rows);
+    w.dgp = cv.take<float>(rows);
+    w.rw.keys[0] = cv.take<uint32_t>(p.S * L);
+    w.rw.keys[1] = cv.take<uint32_t>(p.S * L);
+    w.rw.vals[0] = cv.take<uint32_t>(p.S * L);
+    w.rw.vals[1] = cv.take<uint32_t>(p.S * L);
+    w.rw.hist = cv.take<uint32_t>(p.S * 256 * radix_tiles(L));
+    w.rw.seglen = cv.take<uint32_t>(p.S);
+    w.off = cv.take<uint32_t>(p.S * (p.N + 1));
+    if (bytes) *bytes = cv.bytes();
+    return w;
+}
+
+template <typename V, int VPL>
+cudaError_t bwd_generic(const Prob &p, const float *q, const float *k, const void *v,
+                        const float *gamma, const int32_t *idx, const void *out,
+                        const float *rowsum, const void *dout, float *dq, float *dk, void *dv,
+                        float *dgamma, void *ws, int32_t *status, cudaStream_t st) {
+    BwdWs w = carve_bwd(p, ws, nullptr);
+    const int64_t warps = p.S * p.N;
+    const unsigned blocks = (unsigned)((warps + 7) / 8);
+    bwd_query_generic<V, VPL><<<blocks, 256, 0, st>>>(
+        q, k, static_cast<const V *>(v), gamma, idx, static_cast<const V *>(out), rowsum,
+        static_cast<const V *>(dout), dq, w.gbar, w.dgp, status, p.S, p.N, p.H, p.dK, p.dV, p.k,
+        p.C);
+    int ob = 0;
+    cudaError_t e = radix_sort_idx(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st);
+    if (e != cudaSuccess) return e;
+    const int64_t L = p.N * (int64_t)p.k;
+    csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(
+        static_cast<const uint32_t *>(w.rw.keys[ob]), w.rw.seglen, L, p.N, w.off);
+    bwd_key_generic<V, VPL><<<blocks, 256, 0, st>>>(
+        q, k, static_cast<const V *>(v), gamma, rowsum, static_cast<const V *>(dout), w.gbar,
+        w.rw.vals[ob], w.off, L, dk, static_cast<V *>(dv), p.S, p.N, p.H, p.dK, p.dV, p.C);
+    dgamma_reduce<<<(unsigned)p.H, 256, 0, st>>>(w.dgp, p.B, p.H, p.N, dgamma);
+    return cudaGetLastError();
+}
+
+template <typename V>
+cudaError_t bwd_dispatch(const Prob &p, const float *q, const float *k, const void *v,
+                         const float *gamma, const int32_t *idx, const void *out,
+                         const float *rowsum, const void *dout, float *dq, float *dk, void *dv,
+                         float *dgamma, void *ws, int32_t *status, cudaStream_t st) {
+#define ZETA_BWD(VPL) \
+    return bwd_generic<V, VPL>(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv, dgamma, ws, \
+                               status, st)
+    if (p.dV <= 32) ZETA_BWD(1);
+    if (p.dV <= 64) ZETA_BWD(2);
+    if (p.dV <= 128) ZETA_BWD(4);
+    ZETA_BWD(8);
+#undef ZETA_BWD
+}
+
+}  // namespace
+
+size_t bwd_ws_bytes(const Prob &p) {
+    size_t b = 0;
+    carve_bwd(p, nullptr, &b);
+    return b;
+}
+
+cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, const void *v,
+                              const float *gamma, const int32_t *idx, const void *out,
+                              const float *rowsum, const void *dout, float *dq, float *dk,
+                              void *dv, float *dgamma, void *ws, int32_t *status,
+                              cudaStream_t st) {
+    if (p.vdt == ZETA_BF16)
+        return bwd_dispatch<__nv_bfloat16>(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv,
+                                           dgamma, ws, status, st);
+    return bwd_dispatch<float>(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv, dgamma, ws,
+                               status, st);
+}
+
+}  // namespace zeta

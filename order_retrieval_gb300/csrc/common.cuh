@@ -1,0 +1,122 @@
+// common.cuh -- shared device helpers and the internal launcher interface of
+// the ZETA library.  Nothing here is exported; the C ABI is include/zeta.h.
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/zeta.h"
+
+#define ZETA_API extern "C" __attribute__((visibility("default")))
+
+namespace zeta {
+
+constexpr int kMaxDK = 8;
+constexpr int kMaxDV = 256;
+constexpr int kMaxChunks = 1024;
+constexpr unsigned kFull = 0xffffffffu;
+
+// Validated view of a problem, with derived sizes in 64-bit.
+struct Prob {
+    int B, H, N, dK, dV, k, C, bits;
+    int vdt;
+    int64_t S;        // slices B*H
+    int64_t n;        // chunks N / C
+    int64_t T;        // prefix entries per slice
+    int code64;       // 1 when d_K*bits > 32
+};
+
+// Record the first device-side error in an optional status word.
+__device__ __forceinline__ void set_status(int32_t *st, int code) {
+    if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+template <typename T> struct VT;
+template <> struct VT<float> {
+    static __device__ __forceinline__ float ld(const float *p) { return *p; }
+    static __device__ __forceinline__ void st(float *p, float x) { *p = x; }
+};
+template <> struct VT<__nv_bfloat16> {
+    static __device__ __forceinline__ float ld(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+    static __device__ __forceinline__ void st(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+};
+
+// Cauchy weight 1 / (1 + d2 * inv_g2) in float32 with a correctly rounded
+// reciprocal.
+__device__ __forceinline__ float cauchy_w(float d2, float inv_g2) {
+    return __frcp_rn(__fmaf_rn(d2, inv_g2, 1.0f));
+}
+
+// ----------------------------------------------------------- launchers ---
+// Each returns cudaGetLastError() after enqueueing on `st`.
+
+cudaError_t launch_encode(const Prob &p, const float *x, void *codes, cudaStream_t st);
+
+size_t sort_ws_bytes(const Prob &p);
+cudaError_t launch_sort_chunks(const Prob &p, const void *key_codes, void *prefix_codes,
+                               int32_t *prefix_idx, void *ws, cudaStream_t st);
+
+cudaError_t launch_select(const Prob &p, const void *q_codes, const void *prefix_codes,
+                          const int32_t *prefix_idx, int32_t *idx, cudaStream_t st);
+
+cudaError_t launch_attend_fwd(const Prob &p, const float *q, const float *k, const void *v,
+                              const float *gamma, const int32_t *idx, void *out, float *rowsum,
+                              int32_t *status, cudaStream_t st);
+
+size_t bwd_ws_bytes(const Prob &p);
+cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, const void *v,
+                              const float *gamma, const int32_t *idx, const void *out,
+                              const float *rowsum, const void *dout, float *dq, float *dk,
+                              void *dv, float *dgamma, void *ws, int32_t *status,
+                              cudaStream_t st);
+
+// Segmented stable LSD radix sort of (key, value) pairs, 8-bit digits.
+// Slices of `len` items each, laid out `stride` apart.
+struct RadixWs {
+    void *keys[2];          // ping-pong key buffers, S * stride keys each
+    uint32_t *vals[2];      // ping-pong value buffers
+    uint32_t *hist;         // S * 256 * tiles
+    uint32_t *seglen;       // S, valid items per slice (filtered sources)
+};
+
+constexpr int kRadixThreads = 256;
+constexpr int kRadixItems = 8;
+constexpr int kRadixTile = kRadixThreads * kRadixItems;
+
+inline int64_t radix_tiles(int64_t len) { return (len + kRadixTile - 1) / kRadixTile; }
+
+// Sort codes (values = position in slice).  Result lands in keys[out_buf].
+template <typename K>
+cudaError_t radix_sort_codes(const K *codes, int64_t S, int64_t N, int key_bits, RadixWs &ws,
+                             int *out_buf, cudaStream_t st);
+
+// Sort the valid entries of an int32 index array [S][N*k] by index value,
+// values = entry / k (the query i).  Entries equal to -1 are dropped; other
+// entries outside [0, chunk start of i) are dropped and flagged in `status`.
+// Per-slice counts land in ws.seglen.
+cudaError_t radix_sort_idx(const int32_t *idx, int64_t S, int64_t N, int k, int C, RadixWs &ws,
+                           int *out_buf, int32_t *status, cudaStream_t st);
+
+// Carve aligned sub-buffers out of a workspace.
+struct Carver {
+    char *base;
+    size_t off = 0;
+    explicit Carver(void *b) : base(static_cast<char *>(b)) {}
+    template <typename T> T *take(size_t count) {
+        off = (off + 255) & ~size_t(255);
+        T *r = reinterpret_cast<T *>(base ? base + off : nullptr);
+        off += count * sizeof(T);
+        return r;
+    }
+    size_t bytes() const { return (off + 255) & ~size_t(255); }
+};
+
+}  // namespace zeta

@@ -1,0 +1,98 @@
+// encode.cu -- quantise and bit-interleave every token into a Z-order code.
+//
+// Passage: OpenReview discussion of "ZETA: Leveraging Z-order Curves for
+// Efficient Top-k Attention", reply A2 "Clarification of Binary Expansion and
+// Precision": each coordinate is normalised to [0, 1], discretised onto a grid
+// of 2^bits cells and the cell indices' bits are interleaved into one integer.
+// Coordinate 0 is the most significant bit of every level (the K^1, K^2, K^3
+// order of the reply on dimension-ordering asymmetry).
+//
+// One thread per token.  The work is a few integer operations per 4*d_K bytes
+// read, so the kernel runs at copy speed; bit spreading for d_K = 2 and 3 uses
+// the usual shift-and-mask ("magic number") dilation, other widths a bit loop.
+#include "common.cuh"
+
+namespace zeta {
+namespace {
+
+// Grid cell of one coordinate.  Float32, no contraction: (x + 1) rounded once,
+// then an exact power-of-two scale.
+__device__ __forceinline__ uint32_t quantise(float x, float scale, float umax) {
+    float t = __fmul_rn(__fadd_rn(x, 1.0f), scale);
+    float f = floorf(t);
+    f = fmaxf(f, 0.0f);      // also maps NaN to 0
+    f = fminf(f, umax);
+    return static_cast<uint32_t>(f);
+}
+
+// Spread the low 21 bits of x so that bit j moves to bit 3j.
+__device__ __forceinline__ uint64_t dilate3(uint64_t x) {
+    x &= 0x1fffffull;
+    x = (x | (x << 32)) & 0x001f00000000ffffull;
+    x = (x | (x << 16)) & 0x001f0000ff0000ffull;
+    x = (x | (x << 8)) & 0x100f00f00f00f00full;
+    x = (x | (x << 4)) & 0x10c30c30c30c30c3ull;
+    x = (x | (x << 2)) & 0x1249249249249249ull;
+    return x;
+}
+
+// Spread the low 32 bits of x so that bit j moves to bit 2j.
+__device__ __forceinline__ uint64_t dilate2(uint64_t x) {
+    x &= 0xffffffffull;
+    x = (x | (x << 16)) & 0x0000ffff0000ffffull;
+    x = (x | (x << 8)) & 0x00ff00ff00ff00ffull;
+    x = (x | (x << 4)) & 0x0f0f0f0f0f0f0f0full;
+    x = (x | (x << 2)) & 0x3333333333333333ull;
+    x = (x | (x << 1)) & 0x5555555555555555ull;
+    return x;
+}
+
+template <typename CodeT>
+__global__ void encode_kernel(const float *__restrict__ x, CodeT *__restrict__ codes,
+                              int64_t ntok, int dK, int bits) {
+    const float scale = __int_as_float((126 + bits) << 23);   // 2^(bits-1)
+    const float umax = static_cast<float>((1u << bits) - 1u);
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < ntok;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const float *xt = x + t * dK;
+        uint64_t code = 0;
+        if (dK == 3) {
+            uint32_t u0 = quantise(xt[0], scale, umax);
+            uint32_t u1 = quantise(xt[1], scale, umax);
+            uint32_t u2 = quantise(xt[2], scale, umax);
+            code = (dilate3(u0) << 2) | (dilate3(u1) << 1) | dilate3(u2);
+        } else if (dK == 2) {
+            uint32_t u0 = quantise(xt[0], scale, umax);
+            uint32_t u1 = quantise(xt[1], scale, umax);
+            code = (dilate2(u0) << 1) | dilate2(u1);
+        } else if (dK == 1) {
+            code = quantise(xt[0], scale, umax);
+        } else {
+            for (int d = 0; d < dK; ++d) {
+                uint32_t u = quantise(xt[d], scale, umax);
+                const int sh = dK - 1 - d;
+                for (int j = 0; j < bits; ++j)
+                    code |= static_cast<uint64_t>((u >> j) & 1u) << (j * dK + sh);
+            }
+        }
+        codes[t] = static_cast<CodeT>(code);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_encode(const Prob &p, const float *x, void *codes, cudaStream_t st) {
+    const int64_t ntok = p.S * p.N;
+    const int threads = 256;
+    int64_t blocks = (ntok + threads - 1) / threads;
+    if (blocks > 152 * 64) blocks = 152 * 64;
+    if (p.code64)
+        encode_kernel<uint64_t><<<(unsigned)blocks, threads, 0, st>>>(
+            x, static_cast<uint64_t *>(codes), ntok, p.dK, p.bits);
+    else
+        encode_kernel<uint32_t><<<(unsigned)blocks, threads, 0, st>>>(
+            x, static_cast<uint32_t *>(codes), ntok, p.dK, p.bits);
+    return cudaGetLastError();
+}
+
+}  // namespace zeta

@@ -1,0 +1,291 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the CPU oracle.
+
+Integer results (codes, prefix tables, selected indices) must match bit for
+bit.  Floating-point results use the stated tolerances: float32 tensors
+max |x - x_ref| <= 1e-5 (relative above magnitude 1); bf16 tensors
+max |x - x_ref| <= 2e-2 * max |x_ref| with the oracle fed the same
+bf16-rounded inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from order_retrieval_gb300 import binding as zb
+from order_retrieval_gb300 import workloads as W
+
+from gpu_util import (Run, assert_close_bf16, assert_close_f32, codes_np, dev_vals,
+                      slice_inputs)
+
+pytestmark = [
+    pytest.mark.gpu,
+    pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU"),
+]
+
+
+def _prefix_is_sorted_permutation(pc, pi, w):
+    """Property check of a whole prefix table: each prefix c is a permutation
+    of 0..cC-1 sorted by (code, index)."""
+    for c in range(1, w.n_chunks):
+        off = w.C * c * (c - 1) // 2
+        M = c * w.C
+        codes = pc[off:off + M]
+        idx = pi[off:off + M].astype(np.int64)
+        assert np.array_equal(np.sort(idx), np.arange(M))
+        key = codes.astype(np.uint64)
+        assert (key[1:] >= key[:-1]).all()
+        tie = key[1:] == key[:-1]
+        assert (idx[1:][tie] > idx[:-1][tie]).all()
+
+
+def _check_forward_slice(run, s, rows=None, bf16=False):
+    w, g = run.w, run.g
+    q, k, v, gamma, _ = slice_inputs(w, g, s)
+    qc = oracle.encode(q, w.bits)
+    kc = oracle.encode(k, w.bits)
+    idx_ref = oracle.select(qc[None], kc[None], w.C, w.k, rows=rows)[0]
+    idx_gpu = run.idx()[s] if rows is None else run.idx()[s][rows]
+    assert np.array_equal(idx_gpu, idx_ref)
+    out_ref, rs_ref = oracle.attend_fwd(q, k, v, gamma, idx_ref, w.C, rows=rows)
+    out = run.out()[s] if rows is None else run.out()[s][rows]
+    rs = run.rowsum()[s] if rows is None else run.rowsum()[s][rows]
+    assert_close_f32(rs, rs_ref, what="rowsum")
+    if bf16:
+        assert_close_bf16(out, out_ref, what="out")
+    else:
+        assert_close_f32(out, out_ref, what="out")
+
+
+# ------------------------------------------------------------------ encode ---
+
+@pytest.mark.parametrize("w", [W.TINY, W.CLUSTERED, *W.SWEEP], ids=lambda w: w.name)
+def test_encode_bit_exact(w):
+    run_w = w.replace(B=1, H=2) if w.B * w.H > 2 else w
+    g = W.generate(run_w)
+    p = zb.problem_of(run_w)
+    for name in ("q", "k"):
+        x = torch.from_numpy(g[name]).cuda().reshape(-1)
+        codes = torch.empty(run_w.B * run_w.H * run_w.N, dtype=zb.code_dtype(p), device="cuda")
+        zb.zeta_encode(p, x, codes)
+        torch.cuda.synchronize()
+        assert np.array_equal(codes_np(codes), oracle.encode(g[name], run_w.bits).reshape(-1))
+
+
+@pytest.mark.parametrize("d_K,bits", [(1, 24), (2, 21), (3, 10), (3, 12), (8, 8), (5, 12)])
+def test_encode_edge_values(d_K, bits):
+    """Grid edges, clamping, NaN and infinities."""
+    half = 2.0 ** (bits - 1)
+    vals = [-1.0, -1.0 + 1 / half, -0.5, 0.0, 1 / half, 0.999, np.nextafter(np.float32(1), 0),
+            1.0, 5.0, -7.0, np.nan, np.inf, -np.inf, -1.0 - 1e-7, 2.0 ** -30]
+    vals = np.array(vals, dtype=np.float32)
+    rng = np.random.default_rng(d_K * 100 + bits)
+    x = rng.choice(vals, size=(1, 1, 4096, d_K)).astype(np.float32)
+    p = zb.problem(1, 1, 4096, d_K, 8, 1, 4096, bits, "f32")
+    codes = torch.empty(4096, dtype=zb.code_dtype(p), device="cuda")
+    zb.zeta_encode(p, torch.from_numpy(x).cuda().reshape(-1), codes)
+    torch.cuda.synchronize()
+    assert np.array_equal(codes_np(codes), oracle.encode(x, bits).reshape(-1))
+
+
+# ---------------------------------------------------------- sort / select ---
+
+@pytest.mark.parametrize("w", [W.TINY, W.CLUSTERED], ids=lambda w: w.name)
+def test_prefix_and_select_bit_exact(w):
+    run = Run(w)
+    g = run.g
+    qc = oracle.encode(g["q"], w.bits).reshape(run.S, w.N)
+    kc = oracle.encode(g["k"], w.bits).reshape(run.S, w.N)
+    assert np.array_equal(run.q_codes(), qc)
+    assert np.array_equal(run.k_codes(), kc)
+    pc_ref, pi_ref = oracle.prefix_table(kc, w.C)
+    pc, pi = run.prefix()
+    assert np.array_equal(pi, pi_ref)
+    assert np.array_equal(pc, pc_ref)
+    assert np.array_equal(run.idx(), oracle.select(qc, kc, w.C, w.k))
+
+
+# ----------------------------------------------------------------- forward ---
+
+def test_forward_tiny_f32():
+    run = Run(W.TINY)
+    assert run.status() == 0
+    _check_forward_slice(run, 0)
+
+
+def test_forward_clustered_bf16():
+    run = Run(W.CLUSTERED)
+    assert run.status() == 0
+    for s in range(run.S):
+        _check_forward_slice(run, s, bf16=True)
+
+
+def test_forward_efficiency_sampled():
+    """The 65,536-token workload in the timed launch configuration: prefix
+    tables of every slice checked by property, one slice's table exactly, and
+    sampled queries of every slice against the oracle."""
+    w = W.EFFICIENCY
+    run = Run(w)
+    assert run.status() == 0
+    g = run.g
+    kc_ref = oracle.encode(g["k"], w.bits).reshape(run.S, w.N)
+    qc_ref = oracle.encode(g["q"], w.bits).reshape(run.S, w.N)
+    assert np.array_equal(run.k_codes(), kc_ref)
+    assert np.array_equal(run.q_codes(), qc_ref)
+    pc, pi = run.prefix()
+    for s in range(run.S):
+        _prefix_is_sorted_permutation(pc[s], pi[s], w)
+    for c in (1, 2, 31, 63):
+        off = w.C * c * (c - 1) // 2
+        M = c * w.C
+        want = np.lexsort((np.arange(M), kc_ref[3, :M]))
+        assert np.array_equal(pi[3, off:off + M], want)
+    rng = np.random.default_rng(0)
+    rows = np.sort(np.concatenate([rng.choice(w.N, 120, replace=False),
+                                   [0, w.C - 1, w.C, 2 * w.C - 1, w.N - 1]]))
+    for s in range(run.S):
+        _check_forward_slice(run, s, rows=rows, bf16=True)
+
+
+# ---------------------------------------------------------------- backward ---
+
+def _check_backward_slice(run, s, bf16=False):
+    w, g = run.w, run.g
+    q, k, v, gamma, dout = slice_inputs(w, g, s)
+    idx = run.idx()[s]
+    dq_r, dk_r, dv_r, _ = oracle.attend_bwd(q, k, v, gamma, idx, dout, w.C)
+    dq, dk, dv, _ = run.grads()
+    if bf16:
+        assert_close_bf16(dq[s], dq_r, what="dq")
+        assert_close_bf16(dk[s], dk_r, what="dk")
+        assert_close_bf16(dv[s], dv_r, what="dv")
+    else:
+        assert_close_f32(dq[s], dq_r, what="dq")
+        assert_close_f32(dk[s], dk_r, what="dk")
+        assert_close_f32(dv[s], dv_r, what="dv")
+
+
+def _dgamma_ref(run):
+    w, g = run.w, run.g
+    ref = np.zeros(w.H)
+    for s in range(run.S):
+        q, k, v, gamma, dout = slice_inputs(w, g, s)
+        ref[s % w.H] += oracle.attend_bwd(q, k, v, gamma, run.idx()[s], dout, w.C)[3]
+    return ref
+
+
+def test_backward_tiny_f32():
+    run = Run(W.TINY, backward=True)
+    assert run.status() == 0
+    _check_backward_slice(run, 0)
+    dg = run.grads()[3]
+    assert_close_f32(dg, _dgamma_ref(run), what="dgamma")
+
+
+def test_backward_fd_workload_f32():
+    w = W.FD.replace(v_dtype="f32")
+    run = Run(w, backward=True)
+    for s in range(run.S):
+        _check_backward_slice(run, s)
+    assert_close_f32(run.grads()[3], _dgamma_ref(run), what="dgamma")
+
+
+def test_backward_train_f32_sampled():
+    """The training workload (B=4, H=8, N=65536, k=48, C=1024) with float32
+    values and upstream gradients, two slices against the oracle."""
+    w = W.TRAIN.replace(v_dtype="f32")
+    run = Run(w, backward=True)
+    assert run.status() == 0
+    for s in (0, 29):
+        _check_backward_slice(run, s)
+
+
+def test_backward_clustered_bf16():
+    w = W.CLUSTERED.replace(B=1)
+    run = Run(w, backward=True)
+    assert run.status() == 0
+    for s in (0, 5):
+        _check_backward_slice(run, s, bf16=True)
+
+
+def test_backward_is_deterministic():
+    w = W.CLUSTERED.replace(B=1, H=2)
+    a = Run(w, backward=True)
+    ga = [t.copy() for t in a.grads()]
+    a.plan.backward(a.q, a.k, a.v, a.gamma, a.dout)
+    torch.cuda.synchronize()
+    for x, y in zip(ga, a.grads()):
+        assert np.array_equal(x, y)
+
+
+# -------------------------------------------------------------- edge cases ---
+
+EDGE = [
+    dict(N=96, C=32, k=32, d_V=8),          # k = C, ragged tiles
+    dict(N=200, C=40, k=7, d_V=40),         # odd k, d_V not a multiple of 32
+    dict(N=256, C=256, k=16),               # one chunk: everything is local
+    dict(N=512, C=64, k=8, bits=1),         # 3-bit codes: massive ties
+    dict(N=512, C=16, k=16, d_V=1),         # many chunks, d_V = 1
+    dict(N=384, C=128, k=5, d_K=1, bits=21),
+    dict(N=384, C=128, k=9, d_K=2, bits=21),   # 42-bit codes
+    dict(N=384, C=128, k=12, d_K=8, bits=8),   # 64-bit codes
+    dict(N=4096, C=4, k=4, d_V=16),         # 1024 chunks (the limit)
+]
+
+
+@pytest.mark.parametrize("kw", EDGE, ids=lambda kw: "-".join(f"{a}{b}" for a, b in kw.items()))
+@pytest.mark.parametrize("vd", ["f32", "bf16"])
+def test_edge_shapes(kw, vd):
+    base = dict(name="edge", B=1, H=2, N=256, d_K=3, d_V=32, k=8, C=64, bits=10, v_dtype=vd,
+                gamma=(0.3, 1.0), dist="uniform", v_dist="normal", seed=11)
+    base.update(kw)
+    w = W.Workload(**base)
+    run = Run(w, backward=True)
+    assert run.status() == 0
+    g = run.g
+    qc = oracle.encode(g["q"], w.bits).reshape(run.S, w.N)
+    kc = oracle.encode(g["k"], w.bits).reshape(run.S, w.N)
+    if w.n_chunks > 1:
+        pc_ref, pi_ref = oracle.prefix_table(kc, w.C)
+        pc, pi = run.prefix()
+        assert np.array_equal(pi, pi_ref)
+        assert np.array_equal(pc, pc_ref)
+    assert np.array_equal(run.idx(), oracle.select(qc, kc, w.C, w.k))
+    for s in range(run.S):
+        _check_forward_slice(run, s, bf16=(vd == "bf16"))
+        _check_backward_slice(run, s, bf16=(vd == "bf16"))
+    ref = _dgamma_ref(run)
+    if vd == "bf16":
+        assert_close_bf16(run.grads()[3], ref, what="dgamma")
+    else:
+        assert_close_f32(run.grads()[3], ref, what="dgamma")
+
+
+def test_empty_problem_is_a_no_op():
+    p = zb.problem(1, 2, 0, 3, 32, 8, 64, 10, "f32")
+    x = torch.empty(0, device="cuda")
+    codes = torch.empty(0, dtype=torch.int32, device="cuda")
+    zb.zeta_encode(p, x, codes)
+    torch.cuda.synchronize()
+
+
+def test_out_of_range_indices_are_flagged_and_skipped():
+    w = W.TINY.replace(N=256, C=64, k=8)
+    g = W.generate(w)
+    run = Run(w)
+    idx = run.plan.idx.clone()
+    bad = idx.view(w.N, w.k)
+    bad[100, 0] = 200            # a key of the query's own chunk or later: illegal
+    bad[150, 3] = -5
+    bad[255, 7] = 10_000_000
+    out = torch.empty_like(run.plan.out)
+    rs = torch.empty_like(run.plan.rowsum)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    zb.zeta_attend_fwd(run.p, run.q, run.k, run.v, run.gamma, idx, out, rs, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 6
+    ref_idx = bad.cpu().numpy().copy()
+    ref_idx[100, 0] = ref_idx[150, 3] = ref_idx[255, 7] = -1
+    q, k, v, gamma, _ = slice_inputs(w, g, 0)
+    o_ref, s_ref = oracle.attend_fwd(q, k, v, gamma, ref_idx, w.C)
+    assert_close_f32(out.cpu().numpy().reshape(w.N, w.d_V), o_ref, what="out")
+    assert_close_f32(rs.cpu().numpy(), s_ref, what="rowsum")
