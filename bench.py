@@ -1,0 +1,447 @@
+"""Benchmark of the ZETA hot path (prints one JSON line on rank 0).
+
+One step = the whole path over one batch: Z-order encode of q and k, sorted
+causal prefixes, window select, Cauchy attend forward and backward, on the
+training workload (B=4, H=8, N=65536, d_K=3, d_V=64, k=48, C=1024, 10 bits,
+bf16 values).  `value` is forward+backward tokens/s (B*N per step) with inputs
+resident in HBM; the forward alone is also timed on that workload and on the
+efficiency workload (B=1, H=8, N=65536, k=64), whose attend-forward kernel
+carries the HBM roofline figure.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (single thread) on a bounded sample of
+the same workload.  Under torchrun every rank runs its own batch (weak scaling)
+and the gamma gradient is summed across ranks (the only exchange the path has).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ZETA attention tokens/s (fwd, fwd+bwd) at N=65536 and % of GB300 HBM roofline"
+L2_FLUSH_BYTES = 256 << 20
+CPU_SAMPLE_TOKENS = 8192
+
+
+# ------------------------------------------------------------ byte models ---
+
+def fwd_attend_bytes(w) -> int:
+    """Algorithmic bytes of one attend-forward launch: per query, the k window
+    rows of v (d_V values) and k (d_K floats) and their indices, its own q, its
+    output row and row sum; per key, its own-chunk k and v row once."""
+    vb = 2 if w.v_dtype == "bf16" else 4
+    rows = w.B * w.H * w.N
+    per_q = w.k * (w.d_V * vb + w.d_K * 4 + 4) + w.d_K * 4 + w.d_V * vb + 4
+    per_key_local = w.d_K * 4 + w.d_V * vb
+    return rows * (per_q + per_key_local)
+
+
+def bwd_attend_bytes(w) -> int:
+    """Algorithmic bytes of one attend-backward call: per query, the window v
+    rows again (query side) and the window dO rows gathered on the key side,
+    window k / q rows, indices read twice plus the transpose (read + write),
+    dO, dq; per key, own-chunk k, v, dO rows, dk, dv."""
+    vb = 2 if w.v_dtype == "bf16" else 4
+    rows = w.B * w.H * w.N
+    per_q = (w.k * (2 * w.d_V * vb + 2 * w.d_K * 4 + 4 * 4)
+             + w.d_V * vb + 2 * w.d_K * 4 + 16)
+    per_key = 3 * (w.d_K * 4 + w.d_V * vb) + w.d_K * 4 + w.d_V * vb
+    return rows * (per_q + per_key)
+
+
+# ---------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.t is not None:
+                self.t.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def physical_gpu_index(local: int) -> int:
+    """nvidia-smi index of this process's GPU (CUDA_VISIBLE_DEVICES aware)."""
+    vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    if local < len(vis) and vis[local].isdigit():
+        return int(vis[local])
+    return local
+
+
+# ------------------------------------------------------------ reference arm ---
+
+def cpu_sample(w):
+    """Bounded sample: the first CPU_SAMPLE_TOKENS tokens of slice (b=0, h=0),
+    run as their own causal problem.  Causality makes its forward identical
+    to the full workload's for those tokens."""
+    from order_retrieval_gb300 import workloads as W
+    g = W.generate(w.replace(B=1, H=1), with_dout=True)
+    n = CPU_SAMPLE_TOKENS
+    q, k = g["q"][0, 0, :n], g["k"][0, 0, :n]
+    v = W.values_f64(w, g["v"][0, 0, :n])
+    do = W.values_f64(w, g["dout"][0, 0, :n])
+    return q, k, v, do, float(g["gamma"][0])
+
+
+def oracle_step(w, sample):
+    import oracle
+    q, k, v, do, gamma = sample
+    qc = oracle.encode(q, w.bits)
+    kc = oracle.encode(k, w.bits)
+    idx = oracle.select(qc[None], kc[None], w.C, w.k)[0]
+    oracle.attend_fwd(q, k, v, gamma, idx, w.C)
+    oracle.attend_bwd(q, k, v, gamma, idx, do, w.C)
+
+
+def cpu_tokens_per_s(w, sample, seconds: float) -> float:
+    """Tokens of the sample are single-head tokens: H of them make one token."""
+    return CPU_SAMPLE_TOKENS / w.H / seconds
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    sample = cpu_sample(w)
+    for _ in range(args.warmup):
+        oracle_step(w, sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, sample)
+    dt = (time.perf_counter() - t0) / args.steps
+    val = cpu_tokens_per_s(w, sample, dt)
+    desc = (f"first {CPU_SAMPLE_TOKENS} tokens of one (b,h) slice of {w.name}, as their own "
+            "causal problem: encode, select, attend fwd + bwd")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d_K": w.d_K,
+                   "d_V": w.d_V, "k": w.k, "C": w.C, "bits": w.bits},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- our arm ---
+
+def launches_per_step(w, fwd_only=False) -> int:
+    """Kernel launches the library makes for one step (encode x2, sort, select,
+    attend fwd, attend bwd), following its launch structure."""
+    n = w.N // w.C
+    code_passes = max(1, -(-(w.d_K * w.bits) // 8))
+    sort = 3 * code_passes + 3 if n >= 2 else 0
+    fwd = 2 + sort + 1 + 1
+    if fwd_only:
+        return fwd
+    key_bits = max(1, int(np.ceil(np.log2(max(w.N, 2)))))
+    idx_passes = max(1, -(-key_bits // 8))
+    bwd = 1 + 3 * idx_passes + 1 + 1 + 1
+    return fwd + bwd
+
+
+def run_ours(args, w, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from order_retrieval_gb300 import binding as zb
+    from order_retrieval_gb300 import workloads as W
+    from order_retrieval_gb300.pipeline import ZetaPlan
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    wr = w.replace(seed=w.seed + 1000 * rank)
+    g = W.generate(wr, with_dout=True)
+    p = zb.problem_of(wr)
+
+    def to_dev(a, vals=False):
+        t = torch.from_numpy(np.ascontiguousarray(a)).reshape(-1)
+        if vals and a.dtype == np.int16:
+            t = t.view(torch.bfloat16)
+        return t.pin_memory(), t.to(dev)
+
+    (q_h, q), (k_h, k), (v_h, v), (g_h, gamma), (do_h, dout) = (
+        to_dev(g["q"]), to_dev(g["k"]), to_dev(g["v"], True), to_dev(g["gamma"]),
+        to_dev(g["dout"], True))
+    plan = ZetaPlan(p, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        plan.forward(q, k, v, gamma)
+        plan.backward(q, k, v, gamma, dout)
+        if world > 1:
+            dist.all_reduce(plan.dgamma)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+        flush.zero_()
+    barrier()
+    if int(plan.status.item()) != 0:
+        raise RuntimeError(f"device status {plan.status.item()}")
+
+    # --- timed: K steps, events around every library call, L2 flushed between steps
+    calls = ["encode", "sort", "select", "attend_fwd", "attend_bwd"]
+    per_call = {c: 0.0 for c in calls}
+    step_ms = []
+    with ClockSampler(physical_gpu_index(dev.index or 0)) as clk:
+        barrier()
+        t_wall = time.perf_counter()
+        for _ in range(args.steps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            ev[0].record(stream)
+            zb.zeta_encode(p, q, plan.q_codes)
+            zb.zeta_encode(p, k, plan.k_codes)
+            ev[1].record(stream)
+            zb.zeta_sort_chunks(p, plan.k_codes, plan.prefix_codes, plan.prefix_idx, plan.sort_ws)
+            ev[2].record(stream)
+            zb.zeta_select_topk(p, plan.q_codes, plan.prefix_codes, plan.prefix_idx, plan.idx)
+            ev[3].record(stream)
+            zb.zeta_attend_fwd(p, q, k, v, gamma, plan.idx, plan.out, plan.rowsum, plan.status)
+            ev[4].record(stream)
+            zb.zeta_attend_bwd(p, q, k, v, gamma, plan.idx, dout, plan.dq, plan.dk, plan.dv,
+                               plan.dgamma, plan.bwd_ws, plan.status)
+            if world > 1:
+                dist.all_reduce(plan.dgamma)
+            ev[5].record(stream)
+            flush.zero_()
+            torch.cuda.synchronize()
+            for c, (a, b) in zip(calls, zip(ev[:-1], ev[1:])):
+                per_call[c] += a.elapsed_time(b)
+            step_ms.append(ev[0].elapsed_time(ev[5]))
+        barrier()
+        wall = time.perf_counter() - t_wall
+    dev_ms = sum(step_ms) / len(step_ms)
+    t = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev_ms = float(t.item())
+    tokens = wr.B * wr.N * world
+    value = tokens / (dev_ms * 1e-3)
+
+    # --- forward alone on this workload
+    fwd_ms = []
+    for _ in range(max(3, args.warmup)):
+        plan.forward(q, k, v, gamma)
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        plan.forward(q, k, v, gamma)
+        b.record(stream)
+        torch.cuda.synchronize()
+        fwd_ms.append(a.elapsed_time(b))
+    fwd_train_ms = sum(fwd_ms) / len(fwd_ms)
+
+    # --- end to end through the C ABI with host buffers (pinned)
+    out_h = torch.empty(plan.out.numel(), dtype=plan.out.dtype).pin_memory()
+    dq_h = torch.empty(plan.dq.numel(), dtype=torch.float32).pin_memory()
+    dk_h = torch.empty(plan.dk.numel(), dtype=torch.float32).pin_memory()
+    dv_h = torch.empty(plan.dv.numel(), dtype=plan.dv.dtype).pin_memory()
+    dg_h = torch.empty(plan.dgamma.numel(), dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h, g_h, do_h))
+    d2h = sum(x.numel() * x.element_size() for x in (out_h, dq_h, dk_h, dv_h, dg_h))
+    e2e_ms = []
+    for it in range(max(3, args.warmup) + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for src, dst in ((q_h, q), (k_h, k), (v_h, v), (g_h, gamma), (do_h, dout)):
+            dst.copy_(src, non_blocking=True)
+        plan.forward(q, k, v, gamma)
+        plan.backward(q, k, v, gamma, dout)
+        if world > 1:
+            dist.all_reduce(plan.dgamma)
+        for src, dst in ((plan.out, out_h), (plan.dq, dq_h), (plan.dk, dk_h), (plan.dv, dv_h),
+                         (plan.dgamma, dg_h)):
+            dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if it >= max(3, args.warmup):
+            e2e_ms.append(a.elapsed_time(b))
+    e2e = tokens / (sum(e2e_ms) / len(e2e_ms) * 1e-3)
+
+    # --- efficiency workload: forward alone, and the attend-forward kernel roofline
+    from order_retrieval_gb300 import workloads as W2
+    we = W2.EFFICIENCY.replace(seed=W2.EFFICIENCY.seed + 1000 * rank)
+    ge = W2.generate(we)
+    pe = zb.problem_of(we)
+    qe, ke = to_dev(ge["q"])[1], to_dev(ge["k"])[1]
+    ve, gme = to_dev(ge["v"], True)[1], to_dev(ge["gamma"])[1]
+    plan_e = ZetaPlan(pe, dev, backward=False)
+    for _ in range(max(3, args.warmup)):
+        plan_e.forward(qe, ke, ve, gme)
+    fwd_e, att_e = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        zb.zeta_encode(pe, qe, plan_e.q_codes)
+        zb.zeta_encode(pe, ke, plan_e.k_codes)
+        zb.zeta_sort_chunks(pe, plan_e.k_codes, plan_e.prefix_codes, plan_e.prefix_idx,
+                            plan_e.sort_ws)
+        zb.zeta_select_topk(pe, plan_e.q_codes, plan_e.prefix_codes, plan_e.prefix_idx,
+                            plan_e.idx)
+        ev[1].record(stream)
+        zb.zeta_attend_fwd(pe, qe, ke, ve, gme, plan_e.idx, plan_e.out, plan_e.rowsum,
+                           plan_e.status)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        fwd_e.append(ev[0].elapsed_time(ev[2]))
+        att_e.append(ev[1].elapsed_time(ev[2]))
+    fwd_e_ms = sum(fwd_e) / len(fwd_e)
+    att_e_ms = sum(att_e) / len(att_e)
+
+    if rank != 0:
+        return
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    fb = fwd_attend_bytes(we)
+    achieved = fb / (att_e_ms * 1e-3) / 1e9
+    bb = bwd_attend_bytes(wr)
+    bwd_gbs = bb / (per_call["attend_bwd"] / args.steps * 1e-3) / 1e9
+
+    # CPU baseline: the oracle on a bounded sample of this workload
+    import oracle
+    oracle.build()
+    sample = cpu_sample(w)
+    t0 = time.perf_counter()
+    oracle_step(w, sample)
+    cpu_dt = time.perf_counter() - t0
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": dev_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "dtype_detail": "v, dO, out, dv bf16; q, k, weights and accumulation f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d_K": w.d_K,
+                   "d_V": w.d_V, "k": w.k, "C": w.C, "bits": w.bits,
+                   "l2": "flushed between steps (256 MiB write); inputs larger than L2",
+                   "parallelism": f"dp{world} (independent batches per GPU)"},
+        "fwd_tokens_per_s": tokens / (fwd_train_ms * 1e-3),
+        "fwd_efficiency": {"workload": we.name, "tokens_per_s": we.B * we.N * world /
+                           (fwd_e_ms * 1e-3), "ms": fwd_e_ms, "attend_fwd_ms": att_e_ms},
+        "per_call_ms": {c: per_call[c] / args.steps for c in calls},
+        "roofline": {"kernel": "attend_fwd (efficiency workload)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "algorithmic_bytes": fb, "peak_source": peak_src},
+        "roofline_bwd": {"call": "attend_bwd (training workload)", "achieved": bwd_gbs,
+                         "unit": "GB/s", "frac": bwd_gbs / hbm_peak, "algorithmic_bytes": bb},
+        "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step(w) * args.steps,
+        "cpu_baseline": {"value": cpu_tokens_per_s(w, sample, cpu_dt), "unit": "tokens/s",
+                         "cores": 1, "kind": "oracle",
+                         "sample": f"first {CPU_SAMPLE_TOKENS} tokens of one (b,h) slice of "
+                                   f"{w.name} as their own causal problem; fwd+bwd"},
+        "clocks": clk.summary(),
+        "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    from order_retrieval_gb300 import workloads as W
+    w = W.TRAIN
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, w, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -157,26 +157,29 @@ zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, const flo
  * zeta_attend_bwd -- gradients through the Cauchy weights, selection fixed.
  * Passage: the forward/backward timings of the OpenReview replies A3/A4 (the
  * method is trained end to end) and the forward definition above.
- * With a_ij = w_ij / s_i, g_ij = dO_i . v_j and gbar_i = dO_i . out_i:
+ * With a_ij = w_ij / s_i, g_ij = dO_i . v_j and gbar_i = sum_j a_ij g_ij
+ * (= dO_i . out_i for the exact output):
  *   dL/dw_ij = (g_ij - gbar_i) / s_i
  *   dq_i     = sum_j dL/dw_ij * (-2 w_ij^2 / gamma^2) (q_i - k_j)
  *   dk_j     = sum_i dL/dw_ij * ( 2 w_ij^2 / gamma^2) (q_i - k_j)
  *   dv_j     = sum_i a_ij dO_i
  *   dgamma_h = sum_{b,i,j} dL/dw_ij * 2 w_ij (1 - w_ij) / gamma_h
- *   out, rowsum  in : the forward's outputs
- *   dout         in : v_dtype [B, H, N, d_V]
+ * s_i and gbar_i are recomputed from q, k, v and idx (one pass over each
+ * query's set), so the forward's rounded output is not needed.
+ *   q, k, v, gamma, idx  in : as for zeta_attend_fwd
+ *   dout         in : v_dtype [B, H, N, d_V]  (16-B aligned)
  *   dq, dk       out: float [B, H, N, d_K]
- *   dv           out: v_dtype [B, H, N, d_V]
+ *   dv           out: v_dtype [B, H, N, d_V]  (16-B aligned)
  *   dgamma       out: float [H]
  *   workspace    scratch of at least zeta_bwd_workspace_bytes, 256-B aligned
+ *   dev_status   optional int32 device word (ZETA_ERR_BOUNDS as for the forward)
  * Every output is overwritten.  Reductions run in a fixed order, so results
  * are bit-reproducible run to run.
  * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED, ZETA_ERR_WORKSPACE.
  */
 zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, const float *k,
                               const void *v, const float *gamma, const int32_t *idx,
-                              const void *out, const float *rowsum, const void *dout,
-                              float *dq, float *dk, void *dv, float *dgamma,
+                              const void *dout, float *dq, float *dk, void *dv, float *dgamma,
                               void *workspace, size_t ws_bytes, int32_t *dev_status,
                               cudaStream_t stream);
 

@@ -85,7 +85,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.zeta_select_topk.restype = S
     L.zeta_attend_fwd.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.zeta_attend_fwd.restype = S
-    L.zeta_attend_bwd.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+    L.zeta_attend_bwd.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
     L.zeta_attend_bwd.restype = S
     _lib = L
     return L
@@ -207,7 +207,7 @@ def zeta_attend_fwd(p, q, k, v, gamma, idx, out, rowsum, dev_status=None, stream
                                  _stream(stream)))
 
 
-def zeta_attend_bwd(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv, dgamma, workspace,
+def zeta_attend_bwd(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, workspace,
                     dev_status=None, stream=None):
     S = p.B * p.H * p.N
     vt = v_torch_dtype(p)
@@ -216,8 +216,6 @@ def zeta_attend_bwd(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv, dgamm
     _expect(v, "v", vt, S * p.d_V)
     _expect(gamma, "gamma", torch.float32, p.H)
     _expect(idx, "idx", torch.int32, S * p.k)
-    _expect(out, "out", vt, S * p.d_V)
-    _expect(rowsum, "rowsum", torch.float32, S)
     _expect(dout, "dout", vt, S * p.d_V)
     _expect(dq, "dq", torch.float32, S * p.d_K)
     _expect(dk, "dk", torch.float32, S * p.d_K)
@@ -227,6 +225,6 @@ def zeta_attend_bwd(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv, dgamm
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("zeta_attend_bwd",
            lib().zeta_attend_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
-                                 _ptr(idx), _ptr(out), _ptr(rowsum), _ptr(dout), _ptr(dq),
-                                 _ptr(dk), _ptr(dv), _ptr(dgamma), _ptr(workspace), ws_bytes,
-                                 _ptr(dev_status), _stream(stream)))
+                                 _ptr(idx), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 _ptr(dgamma), _ptr(workspace), ws_bytes, _ptr(dev_status),
+                                 _stream(stream)))

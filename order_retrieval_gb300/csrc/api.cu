@@ -135,10 +135,9 @@ ZETA_API zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, 
 
 ZETA_API zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, const float *k,
                                        const void *v, const float *gamma, const int32_t *idx,
-                                       const void *out, const float *rowsum, const void *dout,
-                                       float *dq, float *dk, void *dv, float *dgamma,
-                                       void *workspace, size_t ws_bytes, int32_t *dev_status,
-                                       cudaStream_t stream) {
+                                       const void *dout, float *dq, float *dk, void *dv,
+                                       float *dgamma, void *workspace, size_t ws_bytes,
+                                       int32_t *dev_status, cudaStream_t stream) {
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -147,13 +146,11 @@ ZETA_API zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, 
         if (pr.H > 0) return from_cuda(cudaMemsetAsync(dgamma, 0, sizeof(float) * pr.H, stream));
         return ZETA_OK;
     }
-    if (!q || !k || !v || !gamma || !idx || !out || !rowsum || !dout || !dq || !dk || !dv ||
-        !dgamma)
+    if (!q || !k || !v || !gamma || !idx || !dout || !dq || !dk || !dv || !dgamma)
         return ZETA_ERR_INVALID_ARG;
-    if (!aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dv))
-        return ZETA_ERR_INVALID_ARG;
+    if (!aligned16(v) || !aligned16(dout) || !aligned16(dv)) return ZETA_ERR_INVALID_ARG;
     if (!workspace || ws_bytes < zeta::bwd_ws_bytes(pr)) return ZETA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ZETA_ERR_WORKSPACE;
-    return from_cuda(zeta::launch_attend_bwd(pr, q, k, v, gamma, idx, out, rowsum, dout, dq, dk,
-                                             dv, dgamma, workspace, dev_status, stream));
+    return from_cuda(zeta::launch_attend_bwd(pr, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma,
+                                             workspace, dev_status, stream));
 }

@@ -6,11 +6,11 @@
 // length 65536 forward + backward row), so the method is trained end to end.
 // The window is not differentiated: idx is an input.
 //
-// With a_ij = w_ij / s_i, g_ij = dO_i . v_j, gbar_i = dO_i . out_i:
+// With a_ij = w_ij / s_i, g_ij = dO_i . v_j, gbar_i = sum_j a_ij g_ij:
 //   dL/dw_ij = (g_ij - gbar_i) / s_i,   dw/d(d^2) = -w^2 / gamma^2,
 //   dw/dgamma = 2 w (1 - w) / gamma.
-// Query side (one warp per query): gbar_i, dq_i and the query's share of
-// dgamma.  Key side (one warp per key): dv_j and dk_j, reducing over the
+// Query side (one warp per query): s_i, gbar_i, dq_i and the query's share
+// of dgamma.  Key side (one warp per key): dv_j and dk_j, reducing over the
 // queries that selected j.  Those are found through a transpose of idx built
 // by a stable radix sort of (key, query) pairs, so every key reads its
 // queries in ascending order and all sums run in a fixed order: the results
@@ -47,14 +47,19 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 // ---------------------------------------------------------- query side ---
+// One pass over the attended set of query i.  With c_ij = -2 w^2 / gamma^2 and
+// e_ij = 2 w (1 - w) / gamma, and dL/dw_ij = (g_ij - gbar_i) / s_i:
+//   s      = sum w,          G  = sum w g        -> gbar = G / s
+//   A_d    = sum g c (q-k)_d, Bd = sum c (q-k)_d -> dq_d  = (A_d - gbar Bd) / s
+//   E1     = sum g e,        E2 = sum e          -> dgamma_i = (E1 - gbar E2) / s
+// so gbar is exact (from the values themselves, not the rounded output).
 
 template <typename V, int VPL>
 __global__ void __launch_bounds__(256)
 bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
                   const V *__restrict__ v, const float *__restrict__ gamma,
-                  const int32_t *__restrict__ idx, const V *__restrict__ out,
-                  const float *__restrict__ rowsum, const V *__restrict__ dout,
-                  float *__restrict__ dq, float *__restrict__ gbar_out,
+                  const int32_t *__restrict__ idx, const V *__restrict__ dout,
+                  float *__restrict__ dq, float *__restrict__ s_out, float *__restrict__ gbar_out,
                   float *__restrict__ dg_part, int32_t *status, int64_t S, int N, int H, int dK,
                   int dV, int k, int C) {
     __shared__ float sdo[8][kMaxDV];
@@ -70,32 +75,32 @@ bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
     float qi[kMaxDK];
 #pragma unroll
     for (int d = 0; d < kMaxDK; ++d) qi[d] = d < dK ? q[row * dK + d] : 0.f;
-    float gb = 0.f;
-    for (int e = lane; e < dV; e += 32) {
-        const float x = VT<V>::ld(dout + row * dV + e);
-        sdo[wib][e] = x;
-        gb = __fmaf_rn(x, VT<V>::ld(out + row * dV + e), gb);
-    }
-    gb = warp_sum(gb);
+    for (int e = lane; e < dV; e += 32) sdo[wib][e] = VT<V>::ld(dout + row * dV + e);
     __syncwarp();
-    const float inv_s = __frcp_rn(rowsum[row]);
     const float *kb = kx + seg * N * dK;
     const V *vb = v + seg * N * dV;
     const int cC = (i / C) * C;
-    float dqa[kMaxDK];
+    float A[kMaxDK], Bd[kMaxDK];
 #pragma unroll
-    for (int d = 0; d < kMaxDK; ++d) dqa[d] = 0.f;
-    float dgp = 0.f;
+    for (int d = 0; d < kMaxDK; ++d) A[d] = Bd[d] = 0.f;
+    float sw = 0.f, G = 0.f, E1 = 0.f, E2 = 0.f;
     auto visit = [&](int j) {
         const float *kj = kb + (int64_t)j * dK;
         const float w = cauchy_w(dist2b(qi, kj, dK), inv_g2);
         const float gij = dot_row<V>(sdo[wib], vb + (int64_t)j * dV, dV);
-        const float dldw = (gij - gb) * inv_s;
-        const float coef = dldw * (-2.f * w * w * inv_g2);
+        const float c = -2.f * w * w * inv_g2;
+        const float e = 2.f * w * (1.f - w) * inv_g;
+        sw += w;
+        G = __fmaf_rn(w, gij, G);
+        E1 = __fmaf_rn(gij, e, E1);
+        E2 += e;
 #pragma unroll
         for (int d = 0; d < kMaxDK; ++d)
-            if (d < dK) dqa[d] = __fmaf_rn(coef, qi[d] - kj[d], dqa[d]);
-        dgp = __fmaf_rn(dldw, 2.f * w * (1.f - w) * inv_g, dgp);
+            if (d < dK) {
+                const float t = c * (qi[d] - kj[d]);
+                A[d] = __fmaf_rn(gij, t, A[d]);
+                Bd[d] += t;
+            }
     };
     const int32_t *irow = idx + row * (int64_t)k;
     for (int t = lane; t < k; t += 32) {
@@ -105,13 +110,22 @@ bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
         visit(j);
     }
     for (int j = cC + lane; j <= i; j += 32) visit(j);
+    sw = warp_sum(sw);
+    G = warp_sum(G);
+    E1 = warp_sum(E1);
+    E2 = warp_sum(E2);
+    const float inv_s = __frcp_rn(sw);
+    const float gb = G * inv_s;
 #pragma unroll
-    for (int d = 0; d < kMaxDK; ++d) dqa[d] = warp_sum(dqa[d]);
-    dgp = warp_sum(dgp);
+    for (int d = 0; d < kMaxDK; ++d) {
+        A[d] = warp_sum(A[d]);
+        Bd[d] = warp_sum(Bd[d]);
+    }
     if (lane == 0) {
-        for (int d = 0; d < dK; ++d) dq[row * dK + d] = dqa[d];
+        for (int d = 0; d < dK; ++d) dq[row * dK + d] = (A[d] - gb * Bd[d]) * inv_s;
+        s_out[row] = sw;
         gbar_out[row] = gb;
-        dg_part[row] = dgp;
+        dg_part[row] = (E1 - gb * E2) * inv_s;
     }
 }
 
@@ -232,6 +246,7 @@ dgamma_reduce(const float *__restrict__ part, int B, int H, int N, float *__rest
 }
 
 struct BwdWs {
+    float *s;
     float *gbar;
     float *dgp;
     RadixWs rw;
@@ -243,6 +258,7 @@ BwdWs carve_bwd(const Prob &p, void *base, size_t *bytes) {
     BwdWs w;
     const int64_t rows = p.S * p.N;
     const int64_t L = p.N * (int64_t)p.k;
+    w.s = cv.take<float>(rows);
     w.gbar = cv.take<float>(rows);
     w.dgp = cv.take<float>(rows);
     w.rw.keys[0] = cv.take<uint32_t>(p.S * L);
@@ -258,16 +274,15 @@ BwdWs carve_bwd(const Prob &p, void *base, size_t *bytes) {
 
 template <typename V, int VPL>
 cudaError_t bwd_generic(const Prob &p, const float *q, const float *k, const void *v,
-                        const float *gamma, const int32_t *idx, const void *out,
-                        const float *rowsum, const void *dout, float *dq, float *dk, void *dv,
-                        float *dgamma, void *ws, int32_t *status, cudaStream_t st) {
+                        const float *gamma, const int32_t *idx, const void *dout, float *dq,
+                        float *dk, void *dv, float *dgamma, void *ws, int32_t *status,
+                        cudaStream_t st) {
     BwdWs w = carve_bwd(p, ws, nullptr);
     const int64_t warps = p.S * p.N;
     const unsigned blocks = (unsigned)((warps + 7) / 8);
     bwd_query_generic<V, VPL><<<blocks, 256, 0, st>>>(
-        q, k, static_cast<const V *>(v), gamma, idx, static_cast<const V *>(out), rowsum,
-        static_cast<const V *>(dout), dq, w.gbar, w.dgp, status, p.S, p.N, p.H, p.dK, p.dV, p.k,
-        p.C);
+        q, k, static_cast<const V *>(v), gamma, idx, static_cast<const V *>(dout), dq, w.s,
+        w.gbar, w.dgp, status, p.S, p.N, p.H, p.dK, p.dV, p.k, p.C);
     int ob = 0;
     cudaError_t e = radix_sort_idx(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st);
     if (e != cudaSuccess) return e;
@@ -275,7 +290,7 @@ cudaError_t bwd_generic(const Prob &p, const float *q, const float *k, const voi
     csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(
         static_cast<const uint32_t *>(w.rw.keys[ob]), w.rw.seglen, L, p.N, w.off);
     bwd_key_generic<V, VPL><<<blocks, 256, 0, st>>>(
-        q, k, static_cast<const V *>(v), gamma, rowsum, static_cast<const V *>(dout), w.gbar,
+        q, k, static_cast<const V *>(v), gamma, w.s, static_cast<const V *>(dout), w.gbar,
         w.rw.vals[ob], w.off, L, dk, static_cast<V *>(dv), p.S, p.N, p.H, p.dK, p.dV, p.C);
     dgamma_reduce<<<(unsigned)p.H, 256, 0, st>>>(w.dgp, p.B, p.H, p.N, dgamma);
     return cudaGetLastError();
@@ -283,12 +298,11 @@ cudaError_t bwd_generic(const Prob &p, const float *q, const float *k, const voi
 
 template <typename V>
 cudaError_t bwd_dispatch(const Prob &p, const float *q, const float *k, const void *v,
-                         const float *gamma, const int32_t *idx, const void *out,
-                         const float *rowsum, const void *dout, float *dq, float *dk, void *dv,
-                         float *dgamma, void *ws, int32_t *status, cudaStream_t st) {
+                         const float *gamma, const int32_t *idx, const void *dout, float *dq,
+                         float *dk, void *dv, float *dgamma, void *ws, int32_t *status,
+                         cudaStream_t st) {
 #define ZETA_BWD(VPL) \
-    return bwd_generic<V, VPL>(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv, dgamma, ws, \
-                               status, st)
+    return bwd_generic<V, VPL>(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, ws, status, st)
     if (p.dV <= 32) ZETA_BWD(1);
     if (p.dV <= 64) ZETA_BWD(2);
     if (p.dV <= 128) ZETA_BWD(4);
@@ -305,15 +319,13 @@ size_t bwd_ws_bytes(const Prob &p) {
 }
 
 cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, const void *v,
-                              const float *gamma, const int32_t *idx, const void *out,
-                              const float *rowsum, const void *dout, float *dq, float *dk,
-                              void *dv, float *dgamma, void *ws, int32_t *status,
+                              const float *gamma, const int32_t *idx, const void *dout, float *dq,
+                              float *dk, void *dv, float *dgamma, void *ws, int32_t *status,
                               cudaStream_t st) {
     if (p.vdt == ZETA_BF16)
-        return bwd_dispatch<__nv_bfloat16>(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv,
-                                           dgamma, ws, status, st);
-    return bwd_dispatch<float>(p, q, k, v, gamma, idx, out, rowsum, dout, dq, dk, dv, dgamma, ws,
-                               status, st);
+        return bwd_dispatch<__nv_bfloat16>(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, ws,
+                                           status, st);
+    return bwd_dispatch<float>(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, ws, status, st);
 }
 
 }  // namespace zeta

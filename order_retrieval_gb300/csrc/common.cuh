@@ -73,9 +73,8 @@ cudaError_t launch_attend_fwd(const Prob &p, const float *q, const float *k, con
 
 size_t bwd_ws_bytes(const Prob &p);
 cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, const void *v,
-                              const float *gamma, const int32_t *idx, const void *out,
-                              const float *rowsum, const void *dout, float *dq, float *dk,
-                              void *dv, float *dgamma, void *ws, int32_t *status,
+                              const float *gamma, const int32_t *idx, const void *dout, float *dq,
+                              float *dk, void *dv, float *dgamma, void *ws, int32_t *status,
                               cudaStream_t st);
 
 // Segmented stable LSD radix sort of (key, value) pairs, 8-bit digits.

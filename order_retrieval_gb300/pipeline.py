@@ -60,8 +60,8 @@ class ZetaPlan:
     def backward(self, q, k, v, gamma, dout, stream=None):
         """Gradients for the last forward.  Returns (dq, dk, dv, dgamma) views."""
         p = self.p
-        zb.zeta_attend_bwd(p, q, k, v, gamma, self.idx, self.out, self.rowsum, dout, self.dq,
-                           self.dk, self.dv, self.dgamma, self.bwd_ws, self.status, stream)
+        zb.zeta_attend_bwd(p, q, k, v, gamma, self.idx, dout, self.dq, self.dk, self.dv,
+                           self.dgamma, self.bwd_ws, self.status, stream)
         return self.dq, self.dk, self.dv, self.dgamma
 
 

@@ -98,7 +98,7 @@ def test_null_pointers_and_workspace(L):
     assert L.zeta_sort_chunks(P, fake, fake, fake, ctypes.c_void_p(0x10000), ws - 1, None) == 3
     assert L.zeta_sort_chunks(P, fake, fake, fake, ctypes.c_void_p(0x10010), ws, None) == 3
     bws = zb.zeta_bwd_workspace_bytes(p)
-    args = [fake] * 12
+    args = [fake] * 10
     assert L.zeta_attend_bwd(P, *args, None, bws, None, None) == 3
     # Unaligned value pointers are refused.
     odd = ctypes.c_void_p(0x1002)
