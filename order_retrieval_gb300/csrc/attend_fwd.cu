@@ -15,7 +15,8 @@
 //
 // Generic path: one warp per query, one key per lane for the weights, then the
 // warp walks the 32 keys with lanes spread over the value columns.  Any d_V up
-// to 256, float32 or bf16 values.
+// to 256, float32 or bf16 values.  bf16 values with d_V = 64 and d_K <= 4 take
+// the tensor-core kernel in attend_fwd_tc.cu instead.
 #include "common.cuh"
 
 namespace zeta {
@@ -138,6 +139,8 @@ cudaError_t fwd_generic_dispatch(const Prob &p, const float *q, const float *k, 
 cudaError_t launch_attend_fwd(const Prob &p, const float *q, const float *k, const void *v,
                               const float *gamma, const int32_t *idx, void *out, float *rowsum,
                               int32_t *status, cudaStream_t st) {
+    if (attend_fwd_tc_supported(p))
+        return launch_attend_fwd_tc(p, q, k, v, gamma, idx, out, rowsum, status, st);
     if (p.vdt == ZETA_BF16)
         return fwd_generic_dispatch<__nv_bfloat16>(p, q, k, v, gamma, idx, out, rowsum, status,
                                                    st);

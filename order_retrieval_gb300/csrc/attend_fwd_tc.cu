@@ -1,0 +1,323 @@
+// attend_fwd_tc.cu -- fast forward for bf16 values with d_V = 64 and d_K <= 4.
+//
+// Same definition as attend_fwd.cu (Cauchy softmax over window keys plus the
+// own-chunk causal keys; OpenReview discussion of "ZETA: Leveraging Z-order
+// Curves for Efficient Top-k Attention", reply A2 "Discussion on its
+// robustness" and reply A3 "Justification for Euclidean Distance Claim"),
+// organised for GB300:
+//
+//  * One CTA = 64 consecutive queries of one chunk (4 warps x 16 rows).
+//  * Window part (HBM-bound gather): a warp takes one query at a time; each
+//    lane computes the Cauchy weight of one selected key, then eight lanes read
+//    one 128-byte bf16 value row with 16-byte loads (four rows per warp load,
+//    all loads of a 32-key group issued before any is used) and accumulate in
+//    float32.  Partial sums (sum w v, sum w) go to shared memory.
+//  * Own-chunk part (a dense causal C x C/2 x 64 contraction per chunk): key
+//    tiles of 64 rows are staged by cp.async into XOR-swizzled shared memory
+//    (double buffered); each thread builds its slice of the weight tile P
+//    straight into mma A fragments (bf16), B fragments come from ldmatrix.trans,
+//    and mma.sync m16n8k16 accumulates in float32 registers.  Row sums of P are
+//    kept in float32 from the unrounded weights.
+//  * The two partial sums simply add (weights are in (0, 1], no rescaling).
+#include "common.cuh"
+
+namespace zeta {
+namespace {
+
+constexpr int TQ = 64;            // queries per CTA
+constexpr int TK = 64;            // keys per own-chunk tile
+constexpr int DV = 64;
+constexpr int THREADS = 128;
+constexpr int WPAD = DV + 4;      // padded window-partial row
+
+struct __align__(16) FwdSmem {
+    __nv_bfloat16 v[2][TK * DV];  // swizzled: 16-byte chunk c of row r at c ^ (r & 7)
+    float4 kt[2][TK];
+    float win[TQ][WPAD];
+    float swin[TQ];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void bf16x8_fma(float (&acc)[8], uint4 raw, float w) {
+    const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        acc[2 * e] = __fmaf_rn(w, __uint_as_float(u[e] << 16), acc[2 * e]);
+        acc[2 * e + 1] = __fmaf_rn(w, __uint_as_float(u[e] & 0xffff0000u), acc[2 * e + 1]);
+    }
+}
+
+__device__ __forceinline__ float d2_4(const float (&a)[4], float4 b) {
+    const float e0 = a[0] - b.x, e1 = a[1] - b.y, e2 = a[2] - b.z, e3 = a[3] - b.w;
+    float d = e0 * e0;
+    d = __fmaf_rn(e1, e1, d);
+    d = __fmaf_rn(e2, e2, d);
+    return __fmaf_rn(e3, e3, d);
+}
+
+// Stage own-chunk key tile `kt` (keys cC + kt*TK ...) into buffer b.
+__device__ __forceinline__ void load_tile(FwdSmem &sm, int b, const float *kb,
+                                          const __nv_bfloat16 *vb, int key0, int key_end,
+                                          int dK) {
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int r = 0; r < (TK * DV / 8) / THREADS; ++r) {     // 4 chunks of 16 B per thread
+        const int id = r * THREADS + t;
+        const int row = id >> 3, ch = id & 7;
+        const int key = key0 + row;
+        const bool ok = key < key_end;
+        const __nv_bfloat16 *src = vb + (int64_t)(ok ? key : key0) * DV + ch * 8;
+        cp_async16(smem_u32(&sm.v[b][row * DV + ((ch ^ (row & 7)) * 8)]), src, ok ? 16 : 0);
+    }
+    if (t < TK) {
+        const int key = key0 + t;
+        float4 kk = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (key < key_end) {
+            const float *p = kb + (int64_t)key * dK;
+            kk.x = p[0];
+            if (dK > 1) kk.y = p[1];
+            if (dK > 2) kk.z = p[2];
+            if (dK > 3) kk.w = p[3];
+        }
+        sm.kt[b][t] = kk;
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 4)
+attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
+              const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
+              const int32_t *__restrict__ idx, __nv_bfloat16 *__restrict__ out,
+              float *__restrict__ rowsum, int32_t *status, int N, int H, int dK, int k, int C,
+              int tiles_per_chunk) {
+    __shared__ FwdSmem sm;
+    const int64_t seg = blockIdx.y;
+    const int c = blockIdx.x / tiles_per_chunk;
+    const int qt = blockIdx.x % tiles_per_chunk;
+    const int cC = c * C;
+    const int cend = cC + C;
+    const int i0 = cC + qt * TQ;
+    const int iend = min(cend, i0 + TQ);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float gm = gamma[seg % H];
+    const float inv_g2 = __frcp_rn(gm * gm);
+    const float *kb = kx + seg * (int64_t)N * dK;
+    const float *qb = q + seg * (int64_t)N * dK;
+    const __nv_bfloat16 *vb = v + seg * (int64_t)N * DV;
+
+    const int nkt = (iend - 1 - cC) / TK + 1;     // own-chunk key tiles up to the last query
+    load_tile(sm, 0, kb, vb, cC, cend, dK);
+    cp_async_commit();
+
+    // ------------------------------------------------------ window part ---
+    for (int r = 0; r < 16; ++r) {
+        const int row = warp * 16 + r;
+        const int i = i0 + row;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        float sw = 0.f;
+        if (c > 0 && i < iend) {
+            float qi[4];
+#pragma unroll
+            for (int d = 0; d < 4; ++d) qi[d] = d < dK ? qb[(int64_t)i * dK + d] : 0.f;
+            const int32_t *irow = idx + (seg * N + i) * (int64_t)k;
+            for (int t0 = 0; t0 < k; t0 += 32) {
+                int j = -1;
+                if (t0 + lane < k) {
+                    j = __ldg(irow + t0 + lane);
+                    if (j != -1 && (unsigned)j >= (unsigned)cC) {
+                        set_status(status, ZETA_ERR_BOUNDS);
+                        j = -1;
+                    }
+                }
+                float w = 0.f;
+                if (j >= 0) {
+                    const float *p = kb + (int64_t)j * dK;
+                    float4 kk = make_float4(p[0], dK > 1 ? p[1] : 0.f, dK > 2 ? p[2] : 0.f,
+                                            dK > 3 ? p[3] : 0.f);
+                    w = cauchy_w(d2_4(qi, kk), inv_g2);
+                }
+                sw += w;
+                uint4 buf[8];
+                float wr[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int src = u * 4 + (lane >> 3);
+                    const int jr = __shfl_sync(kFull, j, src);
+                    wr[u] = __shfl_sync(kFull, w, src);
+                    buf[u] = jr >= 0 ? ld_stream16(vb + (int64_t)jr * DV + (lane & 7) * 8)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) bf16x8_fma(acc, buf[u], wr[u]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                acc[e] += __shfl_xor_sync(kFull, acc[e], 8);
+                acc[e] += __shfl_xor_sync(kFull, acc[e], 16);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(kFull, sw, o);
+        }
+        if (lane < 8) {
+            float4 *dst = reinterpret_cast<float4 *>(&sm.win[row][lane * 8]);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        if (lane == 0) sm.swin[row] = sw;
+    }
+
+    // --------------------------------------------------- own-chunk part ---
+    const int g = lane >> 2, tig = lane & 3;
+    const int ra = i0 + warp * 16 + g, rb = ra + 8;
+    float qa[4], qbv[4];
+#pragma unroll
+    for (int d = 0; d < 4; ++d) {
+        qa[d] = (ra < iend && d < dK) ? qb[(int64_t)ra * dK + d] : 0.f;
+        qbv[d] = (rb < iend && d < dK) ? qb[(int64_t)rb * dK + d] : 0.f;
+    }
+    const int lim_a = ra < iend ? ra : -1;        // last key index row a may see
+    const int lim_b = rb < iend ? rb : -1;
+    float acc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+    float sa = 0.f, sb = 0.f;
+    const int warp_last = min(i0 + warp * 16 + 15, iend - 1);
+
+    for (int kt = 0; kt < nkt; ++kt) {
+        if (kt + 1 < nkt) load_tile(sm, (kt + 1) & 1, kb, vb, cC + (kt + 1) * TK, cend, dK);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const int key0 = cC + kt * TK;
+        if (key0 <= warp_last) {                   // else every weight of this warp is 0
+            const float4 *Ks = sm.kt[kt & 1];
+            const uint32_t vbase = smem_u32(sm.v[kt & 1]);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const int kk0 = ks * 16 + 2 * tig;
+                float wv[8];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {      // keys kk0, kk0+1, kk0+8, kk0+9
+                    const int kl = kk0 + (h & 1) + (h >> 1) * 8;
+                    const float4 kv = Ks[kl];
+                    const int key = key0 + kl;
+                    const float wa = key <= lim_a ? cauchy_w(d2_4(qa, kv), inv_g2) : 0.f;
+                    const float wb = key <= lim_b ? cauchy_w(d2_4(qbv, kv), inv_g2) : 0.f;
+                    wv[h] = wa;
+                    wv[4 + h] = wb;
+                    sa += wa;
+                    sb += wb;
+                }
+                uint32_t a[4];
+                a[0] = pack_bf16(wv[0], wv[1]);
+                a[1] = pack_bf16(wv[4], wv[5]);
+                a[2] = pack_bf16(wv[2], wv[3]);
+                a[3] = pack_bf16(wv[6], wv[7]);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    const int m = lane >> 3, rr = lane & 7;
+                    const int key = ks * 16 + (m & 1) * 8 + rr;
+                    const int ch = np * 2 + (m >> 1);
+                    uint32_t b[4];
+                    ldsm_x4_trans(b, vbase + (uint32_t)(key * DV + ((ch ^ (key & 7)) * 8)) * 2u);
+                    mma16816(acc[2 * np], a, b[0], b[1]);
+                    mma16816(acc[2 * np + 1], a, b[2], b[3]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // --------------------------------------------------------- epilogue ---
+    sa += __shfl_xor_sync(kFull, sa, 1);
+    sa += __shfl_xor_sync(kFull, sa, 2);
+    sb += __shfl_xor_sync(kFull, sb, 1);
+    sb += __shfl_xor_sync(kFull, sb, 2);
+    const int rowa = warp * 16 + g, rowb = rowa + 8;
+    const float ta = sa + sm.swin[rowa], tb = sb + sm.swin[rowb];
+    const float ia = ra < iend ? __frcp_rn(ta) : 0.f;
+    const float ib = rb < iend ? __frcp_rn(tb) : 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+        const int col = nt * 8 + 2 * tig;
+        if (ra < iend) {
+            const float o0 = (acc[nt][0] + sm.win[rowa][col]) * ia;
+            const float o1 = (acc[nt][1] + sm.win[rowa][col + 1]) * ia;
+            *reinterpret_cast<__nv_bfloat162 *>(out + (seg * N + ra) * (int64_t)DV + col) =
+                __floats2bfloat162_rn(o0, o1);
+        }
+        if (rb < iend) {
+            const float o0 = (acc[nt][2] + sm.win[rowb][col]) * ib;
+            const float o1 = (acc[nt][3] + sm.win[rowb][col + 1]) * ib;
+            *reinterpret_cast<__nv_bfloat162 *>(out + (seg * N + rb) * (int64_t)DV + col) =
+                __floats2bfloat162_rn(o0, o1);
+        }
+    }
+    if (tig == 0) {
+        if (ra < iend) rowsum[seg * N + ra] = ta;
+        if (rb < iend) rowsum[seg * N + rb] = tb;
+    }
+}
+
+}  // namespace
+
+bool attend_fwd_tc_supported(const Prob &p) {
+    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4;
+}
+
+cudaError_t launch_attend_fwd_tc(const Prob &p, const float *q, const float *k, const void *v,
+                                 const float *gamma, const int32_t *idx, void *out,
+                                 float *rowsum, int32_t *status, cudaStream_t st) {
+    const int tpc = (p.C + TQ - 1) / TQ;
+    const int64_t gx = p.n * tpc;
+    attend_fwd_tc<<<dim3((unsigned)gx, (unsigned)p.S), THREADS, 0, st>>>(
+        q, k, static_cast<const __nv_bfloat16 *>(v), gamma, idx,
+        static_cast<__nv_bfloat16 *>(out), rowsum, status, p.N, p.H, p.dK, p.k, p.C, tpc);
+    return cudaGetLastError();
+}
+
+}  // namespace zeta

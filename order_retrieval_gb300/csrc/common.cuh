@@ -71,6 +71,12 @@ cudaError_t launch_attend_fwd(const Prob &p, const float *q, const float *k, con
                               const float *gamma, const int32_t *idx, void *out, float *rowsum,
                               int32_t *status, cudaStream_t st);
 
+// Tensor-core forward for bf16 values, d_V = 64, d_K <= 4.
+bool attend_fwd_tc_supported(const Prob &p);
+cudaError_t launch_attend_fwd_tc(const Prob &p, const float *q, const float *k, const void *v,
+                                 const float *gamma, const int32_t *idx, void *out,
+                                 float *rowsum, int32_t *status, cudaStream_t st);
+
 size_t bwd_ws_bytes(const Prob &p);
 cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, const void *v,
                               const float *gamma, const int32_t *idx, const void *dout, float *dq,

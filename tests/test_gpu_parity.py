@@ -260,6 +260,31 @@ def test_edge_shapes(kw, vd):
         assert_close_f32(run.grads()[3], ref, what="dgamma")
 
 
+TC = [
+    dict(N=200, C=40, k=7),                 # chunks shorter than a query tile
+    dict(N=480, C=96, k=33),                # one full tile plus a ragged one, k > 32
+    dict(N=256, C=256, k=16),               # a single chunk: all local, four tiles
+    dict(N=1024, C=128, k=128, d_K=1, bits=20),
+    dict(N=768, C=192, k=64, d_K=2, bits=12),
+    dict(N=512, C=128, k=20, d_K=4, bits=6),
+    dict(N=512, C=64, k=64, bits=1),        # heavy code ties
+]
+
+
+@pytest.mark.parametrize("kw", TC, ids=lambda kw: "-".join(f"{a}{b}" for a, b in kw.items()))
+def test_forward_tensor_core_path(kw):
+    """bf16 values with d_V = 64 run the tensor-core forward; ragged tiles,
+    k up to C, d_K from 1 to 4."""
+    base = dict(name="tc", B=2, H=2, N=256, d_K=3, d_V=64, k=8, C=64, bits=10, v_dtype="bf16",
+                gamma=(0.3, 1.0), dist="uniform", v_dist="normal", seed=21)
+    base.update(kw)
+    w = W.Workload(**base)
+    run = Run(w)
+    assert run.status() == 0
+    for s in range(run.S):
+        _check_forward_slice(run, s, bf16=True)
+
+
 def test_empty_problem_is_a_no_op():
     p = zb.problem(1, 2, 0, 3, 32, 8, 64, 10, "f32")
     x = torch.empty(0, device="cuda")
