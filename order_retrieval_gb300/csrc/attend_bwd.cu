@@ -249,6 +249,7 @@ struct BwdWs {
     float *s;
     float *gbar;
     float *dgp;
+    void *rec;
     RadixWs rw;
     uint32_t *off;
 };
@@ -261,6 +262,7 @@ BwdWs carve_bwd(const Prob &p, void *base, size_t *bytes) {
     w.s = cv.take<float>(rows);
     w.gbar = cv.take<float>(rows);
     w.dgp = cv.take<float>(rows);
+    w.rec = cv.take<char>(bwd_tc_rec_bytes(p));
     w.rw.keys[0] = cv.take<uint32_t>(p.S * L);
     w.rw.keys[1] = cv.take<uint32_t>(p.S * L);
     w.rw.vals[0] = cv.take<uint32_t>(p.S * L);
@@ -322,6 +324,22 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
                               const float *gamma, const int32_t *idx, const void *dout, float *dq,
                               float *dk, void *dv, float *dgamma, void *ws, int32_t *status,
                               cudaStream_t st) {
+    if (attend_bwd_tc_supported(p)) {
+        BwdWs w = carve_bwd(p, ws, nullptr);
+        cudaError_t e = launch_bwd_query_tc(p, q, k, v, gamma, idx, dout, dq, w.rec, w.dgp,
+                                            status, st);
+        if (e != cudaSuccess) return e;
+        int ob = 0;
+        e = radix_sort_idx(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st);
+        if (e != cudaSuccess) return e;
+        const int64_t L = p.N * (int64_t)p.k;
+        csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(
+            static_cast<const uint32_t *>(w.rw.keys[ob]), w.rw.seglen, L, p.N, w.off);
+        e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, w.rw.vals[ob], w.off, L, dk, dv, st);
+        if (e != cudaSuccess) return e;
+        dgamma_reduce<<<(unsigned)p.H, 256, 0, st>>>(w.dgp, p.B, p.H, p.N, dgamma);
+        return cudaGetLastError();
+    }
     if (p.vdt == ZETA_BF16)
         return bwd_dispatch<__nv_bfloat16>(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, ws,
                                            status, st);

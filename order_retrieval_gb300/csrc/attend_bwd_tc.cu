@@ -1,0 +1,580 @@
+// attend_bwd_tc.cu -- fast backward for bf16 values with d_V = 64 and d_K <= 4.
+//
+// Same definitions as attend_bwd.cu (gradients through the Cauchy weights of
+// "ZETA: Leveraging Z-order Curves for Efficient Top-k Attention", selection
+// held fixed), organised like the fast forward:
+//
+// Query side, one CTA per 64 queries of a chunk:
+//   window part  - eight lanes per gathered value row: g_ij = dO_i . v_j by a
+//                  16-byte slice dot plus a 3-step shuffle, then the Cauchy
+//                  terms of the pair (w, c = -2 w^2 / gamma^2, e = 2 w (1-w) /
+//                  gamma) accumulate sum w, sum w g, sum g e, sum e,
+//                  sum g c (q-k), sum c (q-k).
+//   own chunk    - G = dO . V^T on tensor cores (mma.sync, dO fragments held
+//                  in registers, V tiles cp.async-staged), then the same terms
+//                  per element.
+//   result       - s_i, gbar_i = G / s, dq_i, the query's dgamma share, and a
+//                  32-byte record {q_i, 1/s_i, gbar_i} for the key side.
+// Key side, one CTA per 64 keys of a chunk:
+//   window part  - the queries that selected key j (a transpose of idx sorted
+//                  by query), four at a time, eight lanes per dO row:
+//                  dv_j += a_ij dO_i and dk_j += dL/dw_ij 2 w^2/gamma^2 (q_i - k_j).
+//   own chunk    - S^T = V . dO^T on tensor cores, the element-wise terms, then
+//                  dV += P^T . dO with P^T re-packed from the accumulator
+//                  fragments (their layout is the A-fragment layout).
+#include "mma.cuh"
+
+namespace zeta {
+namespace {
+
+constexpr int T64 = 64;           // rows per CTA tile (queries or keys)
+constexpr int DV = 64;
+constexpr int THREADS = 128;
+
+// Per-query record for the key side: q (padded to 4), then {1/s, gbar, 0, 0}.
+struct __align__(16) QRec {
+    float4 q;
+    float4 sg;
+};
+
+__device__ __forceinline__ float warp_group8_sum(float x) {
+    x += __shfl_xor_sync(kFull, x, 1);
+    x += __shfl_xor_sync(kFull, x, 2);
+    x += __shfl_xor_sync(kFull, x, 4);
+    return x;
+}
+
+// 64 rows x 64 bf16 of a [.., 64] row-major array into a swizzled tile;
+// rows at or beyond `end` are zero-filled.
+__device__ __forceinline__ void stage_rows(__nv_bfloat16 *tile, const __nv_bfloat16 *base,
+                                           int row0, int end) {
+#pragma unroll
+    for (int r = 0; r < (T64 * DV / 8) / THREADS; ++r) {
+        const int id = r * THREADS + threadIdx.x;
+        const int row = id >> 3, ch = id & 7;
+        const int gr = row0 + row;
+        const bool ok = gr < end;
+        cp_async16(smem_u32(tile + swz(row, ch)), base + (int64_t)(ok ? gr : row0) * DV + ch * 8,
+                   ok ? 16 : 0);
+    }
+}
+
+// ============================================================ query side ===
+
+struct __align__(16) QSmem {
+    __nv_bfloat16 dO[T64 * DV];
+    __nv_bfloat16 v[2][T64 * DV];
+    float4 kt[2][T64];
+    float part[T64][12];
+};
+
+// Accumulators of one query row: x[0] = sum w, x[1] = sum w g, x[2] = sum g e,
+// x[3] = sum e, x[4..7] = sum g c (q-k), x[8..11] = sum c (q-k).
+struct QAcc {
+    float x[12];
+    __device__ void zero() {
+#pragma unroll
+        for (int y = 0; y < 12; ++y) x[y] = 0.f;
+    }
+    __device__ void add(float w, float g, const float (&qi)[4], float4 kk, float inv_g2,
+                        float inv_g) {
+        const float c = -2.f * w * w * inv_g2;
+        const float e = 2.f * w * (1.f - w) * inv_g;
+        x[0] += w;
+        x[1] = __fmaf_rn(w, g, x[1]);
+        x[2] = __fmaf_rn(g, e, x[2]);
+        x[3] += e;
+        const float dq[4] = {qi[0] - kk.x, qi[1] - kk.y, qi[2] - kk.z, qi[3] - kk.w};
+#pragma unroll
+        for (int d = 0; d < 4; ++d) {
+            const float t = c * dq[d];
+            x[4 + d] = __fmaf_rn(g, t, x[4 + d]);
+            x[8 + d] += t;
+        }
+    }
+};
+
+__global__ void __launch_bounds__(THREADS, 4)
+bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
+             const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
+             const int32_t *__restrict__ idx, const __nv_bfloat16 *__restrict__ dout,
+             float *__restrict__ dq, QRec *__restrict__ rec, float *__restrict__ dg_part,
+             int32_t *status, int N, int H, int dK, int k, int C, int tiles_per_chunk) {
+    __shared__ QSmem sm;
+    const int64_t seg = blockIdx.y;
+    const int c = blockIdx.x / tiles_per_chunk;
+    const int qt = blockIdx.x % tiles_per_chunk;
+    const int cC = c * C, cend = cC + C;
+    const int i0 = cC + qt * T64;
+    const int iend = min(cend, i0 + T64);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float gm = gamma[seg % H];
+    const float inv_g2 = __frcp_rn(gm * gm);
+    const float inv_g = __frcp_rn(gm);
+    const float *kb = kx + seg * (int64_t)N * dK;
+    const float *qb = q + seg * (int64_t)N * dK;
+    const __nv_bfloat16 *vb = v + seg * (int64_t)N * DV;
+    const __nv_bfloat16 *db = dout + seg * (int64_t)N * DV;
+    const int nkt = (iend - 1 - cC) / T64 + 1;
+
+    auto load_ktile = [&](int b, int key0) {
+        stage_rows(sm.v[b], vb, key0, cend);
+        if (threadIdx.x < T64) {
+            const int key = key0 + threadIdx.x;
+            sm.kt[b][threadIdx.x] =
+                key < cend ? load_k4(kb + (int64_t)key * dK, dK) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    stage_rows(sm.dO, db, i0, iend);
+    load_ktile(0, cC);
+    cp_async_commit();
+
+    // ---------------------------------------------------- window part ---
+    const int grp = lane >> 3, sub = lane & 7;
+    for (int r = 0; r < 16; ++r) {
+        const int row = warp * 16 + r;
+        const int i = i0 + row;
+        QAcc acc;
+        acc.zero();
+        if (c > 0 && i < iend) {
+            float qi[4];
+#pragma unroll
+            for (int d = 0; d < 4; ++d) qi[d] = d < dK ? qb[(int64_t)i * dK + d] : 0.f;
+            float do8[8];
+            unpack8(*reinterpret_cast<const uint4 *>(db + (int64_t)i * DV + sub * 8),
+                    do8);
+            const int32_t *irow = idx + (seg * N + i) * (int64_t)k;
+            for (int t0 = 0; t0 < k; t0 += 32) {
+                int j = -1;
+                if (t0 + lane < k) {
+                    j = __ldg(irow + t0 + lane);
+                    if (j != -1 && (unsigned)j >= (unsigned)cC) {
+                        set_status(status, ZETA_ERR_BOUNDS);
+                        j = -1;
+                    }
+                }
+                const int nu = min(8, (k - t0 + 3) >> 2);
+                uint4 buf[8];
+                float4 kk[8];
+                int jr[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    jr[u] = __shfl_sync(kFull, j, u * 4 + grp);
+                    if (u < nu && jr[u] >= 0) {
+                        buf[u] = ld_stream16(vb + (int64_t)jr[u] * DV + sub * 8);
+                        kk[u] = load_k4(kb + (int64_t)jr[u] * dK, dK);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (u >= nu) break;
+                    float g = 0.f;
+                    if (jr[u] >= 0) {
+                        float v8[8];
+                        unpack8(buf[u], v8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) g = __fmaf_rn(do8[e], v8[e], g);
+                    }
+                    g = warp_group8_sum(g);
+                    if (jr[u] >= 0) {
+                        const float w = cauchy_w(dist2_4(qi, kk[u]), inv_g2);
+                        acc.add(w, g, qi, kk[u], inv_g2, inv_g);
+                    }
+                }
+            }
+#pragma unroll
+            for (int y = 0; y < 12; ++y) {
+                acc.x[y] += __shfl_xor_sync(kFull, acc.x[y], 8);
+                acc.x[y] += __shfl_xor_sync(kFull, acc.x[y], 16);
+            }
+        }
+        if (lane < 12) {
+            float val = 0.f;
+#pragma unroll
+            for (int y = 0; y < 12; ++y)
+                if (y == lane) val = acc.x[y];
+            sm.part[row][lane] = val;
+        }
+    }
+
+    // ------------------------------------------------- own-chunk part ---
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int ra = i0 + warp * 16 + g8, rb = ra + 8;
+    float qa[4], qbv[4];
+#pragma unroll
+    for (int d = 0; d < 4; ++d) {
+        qa[d] = (ra < iend && d < dK) ? qb[(int64_t)ra * dK + d] : 0.f;
+        qbv[d] = (rb < iend && d < dK) ? qb[(int64_t)rb * dK + d] : 0.f;
+    }
+    const int lim_a = ra < iend ? ra : -1, lim_b = rb < iend ? rb : -1;
+    const int warp_last = min(i0 + warp * 16 + 15, iend - 1);
+    QAcc la, lb;
+    la.zero();
+    lb.zero();
+    uint32_t afr[4][4];
+    for (int kt = 0; kt < nkt; ++kt) {
+        if (kt + 1 < nkt) load_ktile((kt + 1) & 1, cC + (kt + 1) * T64);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        if (kt == 0) {
+            const uint32_t dbase = smem_u32(sm.dO);
+            const int m = lane >> 3, rr = lane & 7;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const int row = warp * 16 + (m & 1) * 8 + rr;
+                ldsm_x4(afr[ks], dbase + (uint32_t)swz(row, ks * 2 + (m >> 1)) * 2u);
+            }
+        }
+        const int key0 = cC + kt * T64;
+        if (key0 <= warp_last) {
+            float s[8][4];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+            const uint32_t vbase = smem_u32(sm.v[kt & 1]);
+            const int m = lane >> 3, rr = lane & 7;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    const int key = np * 16 + (m >> 1) * 8 + rr;
+                    uint32_t b[4];
+                    ldsm_x4(b, vbase + (uint32_t)swz(key, ks * 2 + (m & 1)) * 2u);
+                    mma16816(s[2 * np], afr[ks], b[0], b[1]);
+                    mma16816(s[2 * np + 1], afr[ks], b[2], b[3]);
+                }
+            const float4 *Ks = sm.kt[kt & 1];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int kl = nt * 8 + 2 * tig + e;
+                    const int key = key0 + kl;
+                    const float4 kv = Ks[kl];
+                    if (key <= lim_a)
+                        la.add(cauchy_w(dist2_4(qa, kv), inv_g2), s[nt][e], qa, kv, inv_g2, inv_g);
+                    if (key <= lim_b)
+                        lb.add(cauchy_w(dist2_4(qbv, kv), inv_g2), s[nt][2 + e], qbv, kv, inv_g2,
+                               inv_g);
+                }
+        }
+        __syncthreads();
+    }
+
+    // ------------------------------------------------------- epilogue ---
+#pragma unroll
+    for (int y = 0; y < 12; ++y) {
+        la.x[y] += __shfl_xor_sync(kFull, la.x[y], 1);
+        la.x[y] += __shfl_xor_sync(kFull, la.x[y], 2);
+        lb.x[y] += __shfl_xor_sync(kFull, lb.x[y], 1);
+        lb.x[y] += __shfl_xor_sync(kFull, lb.x[y], 2);
+    }
+    if (tig < 2) {
+        const int rloc = warp * 16 + g8 + tig * 8;
+        const int i = i0 + rloc;
+        if (i < iend) {
+            const float *pw = sm.part[rloc];
+            float t[12];
+#pragma unroll
+            for (int y = 0; y < 12; ++y) t[y] = (tig == 0 ? la.x[y] : lb.x[y]) + pw[y];
+            const float inv_s = __frcp_rn(t[0]);
+            const float gb = t[1] * inv_s;
+            const int64_t gi = seg * N + i;
+            for (int d = 0; d < dK; ++d) dq[gi * dK + d] = (t[4 + d] - gb * t[8 + d]) * inv_s;
+            dg_part[gi] = (t[2] - gb * t[3]) * inv_s;
+            const float *qq = tig == 0 ? qa : qbv;
+            QRec rcd;
+            rcd.q = make_float4(qq[0], qq[1], qq[2], qq[3]);
+            rcd.sg = make_float4(inv_s, gb, 0.f, 0.f);
+            rec[gi] = rcd;
+        }
+    }
+}
+
+// ============================================================== key side ===
+
+struct __align__(16) KSmem {
+    __nv_bfloat16 v[T64 * DV];
+    __nv_bfloat16 dO[2][T64 * DV];
+    QRec qr[2][T64];
+    float dvp[T64][DV + 4];
+    float dkp[T64][4];
+};
+
+__global__ void __launch_bounds__(THREADS, 4)
+bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
+           const float *__restrict__ gamma, const __nv_bfloat16 *__restrict__ dout,
+           const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q,
+           const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
+           __nv_bfloat16 *__restrict__ dv, int N, int H, int dK, int C, int tiles_per_chunk) {
+    __shared__ KSmem sm;
+    const int64_t seg = blockIdx.y;
+    const int c = blockIdx.x / tiles_per_chunk;
+    const int kt = blockIdx.x % tiles_per_chunk;
+    const int cC = c * C, cend = cC + C;
+    const int j0 = cC + kt * T64;
+    const int jend = min(cend, j0 + T64);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float gm = gamma[seg % H];
+    const float inv_g2 = __frcp_rn(gm * gm);
+    const float *kb = kx + seg * (int64_t)N * dK;
+    const __nv_bfloat16 *vb = v + seg * (int64_t)N * DV;
+    const __nv_bfloat16 *db = dout + seg * (int64_t)N * DV;
+    const QRec *rb_ = rec + seg * (int64_t)N;
+
+    auto load_qtile = [&](int b, int iq0) {
+        stage_rows(sm.dO[b], db, iq0, cend);
+        if (threadIdx.x < T64 * 2) {
+            const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
+            const int i = iq0 + r;
+            const bool ok = i < cend;
+            cp_async16(smem_u32(reinterpret_cast<float4 *>(&sm.qr[b][r]) + h),
+                       reinterpret_cast<const float4 *>(rb_ + (ok ? i : iq0)) + h, ok ? 16 : 0);
+        }
+    };
+    stage_rows(sm.v, vb, j0, jend);
+    load_qtile(0, j0);                // query tiles start at the key tile
+    cp_async_commit();
+
+    // ---------------------------------------------------- window part ---
+    const int grp = lane >> 3, sub = lane & 7;
+    const uint32_t *lst = csr_q + seg * csr_stride;
+    const uint32_t *ob = off + seg * (int64_t)(N + 1);
+    for (int r = 0; r < 16; ++r) {
+        const int row = warp * 16 + r;
+        const int j = j0 + row;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        float dka[4] = {0.f, 0.f, 0.f, 0.f};
+        if (j < jend) {
+            float v8[8];
+            unpack8(*reinterpret_cast<const uint4 *>(vb + (int64_t)j * DV + sub * 8), v8);
+            const float4 kj = load_k4(kb + (int64_t)j * dK, dK);
+            const int64_t p0 = ob[j], p1 = ob[j + 1];
+            for (int64_t p = p0; p < p1; p += 8) {
+                uint4 dbuf[2];
+                QRec qrec[2];
+                bool ok[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t pp = p + h * 4 + grp;
+                    ok[h] = pp < p1;
+                    if (ok[h]) {
+                        const uint32_t i = __ldg(lst + pp);
+                        dbuf[h] = ld_stream16(db + (int64_t)i * DV + sub * 8);
+                        qrec[h] = rb_[i];
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float d8[8];
+                    float g = 0.f;
+                    if (ok[h]) {
+                        unpack8(dbuf[h], d8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) g = __fmaf_rn(d8[e], v8[e], g);
+                    }
+                    g = warp_group8_sum(g);
+                    if (ok[h]) {
+                        const float4 qi = qrec[h].q;
+                        const float qv[4] = {qi.x, qi.y, qi.z, qi.w};
+                        const float w = cauchy_w(dist2_4(qv, kj), inv_g2);
+                        const float inv_s = qrec[h].sg.x;
+                        const float a = w * inv_s;
+                        const float dldw = (g - qrec[h].sg.y) * inv_s;
+                        const float coef = dldw * (2.f * w * w * inv_g2);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = __fmaf_rn(a, d8[e], acc[e]);
+                        dka[0] = __fmaf_rn(coef, qi.x - kj.x, dka[0]);
+                        dka[1] = __fmaf_rn(coef, qi.y - kj.y, dka[1]);
+                        dka[2] = __fmaf_rn(coef, qi.z - kj.z, dka[2]);
+                        dka[3] = __fmaf_rn(coef, qi.w - kj.w, dka[3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                acc[e] += __shfl_xor_sync(kFull, acc[e], 8);
+                acc[e] += __shfl_xor_sync(kFull, acc[e], 16);
+            }
+#pragma unroll
+            for (int d = 0; d < 4; ++d) {
+                dka[d] += __shfl_xor_sync(kFull, dka[d], 8);
+                dka[d] += __shfl_xor_sync(kFull, dka[d], 16);
+            }
+        }
+        if (lane < 8) {
+            float4 *dst = reinterpret_cast<float4 *>(&sm.dvp[row][lane * 8]);
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        if (lane == 0) *reinterpret_cast<float4 *>(sm.dkp[row]) =
+            make_float4(dka[0], dka[1], dka[2], dka[3]);
+    }
+
+    // ------------------------------------------------- own-chunk part ---
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int ka = j0 + warp * 16 + g8, kbi = ka + 8;      // this thread's two key rows
+    const float4 kva = ka < jend ? load_k4(kb + (int64_t)ka * dK, dK) : make_float4(0, 0, 0, 0);
+    const float4 kvb = kbi < jend ? load_k4(kb + (int64_t)kbi * dK, dK) : make_float4(0, 0, 0, 0);
+    const float kra[4] = {kva.x, kva.y, kva.z, kva.w};
+    const float krb[4] = {kvb.x, kvb.y, kvb.z, kvb.w};
+    const int first_a = ka < jend ? ka : 0x7fffffff;     // first query index row a may see
+    const int first_b = kbi < jend ? kbi : 0x7fffffff;
+    float dva[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dva[nt][e] = 0.f;
+    float dkl_a[4] = {0.f, 0.f, 0.f, 0.f}, dkl_b[4] = {0.f, 0.f, 0.f, 0.f};
+    const int nqt = tiles_per_chunk - kt;
+    const int m = lane >> 3, rr = lane & 7;
+    for (int t = 0; t < nqt; ++t) {
+        const int iq0 = j0 + t * T64;
+        if (t + 1 < nqt) load_qtile((t + 1) & 1, iq0 + T64);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const uint32_t vbase = smem_u32(sm.v);
+        const uint32_t dbase = smem_u32(sm.dO[t & 1]);
+        // S^T = V . dO^T : 16 keys x 64 queries per warp
+        float s[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, vbase + (uint32_t)swz(warp * 16 + (m & 1) * 8 + rr, ks * 2 + (m >> 1)) * 2u);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                const int qrow = np * 16 + (m >> 1) * 8 + rr;
+                uint32_t b[4];
+                ldsm_x4(b, dbase + (uint32_t)swz(qrow, ks * 2 + (m & 1)) * 2u);
+                mma16816(s[2 * np], a, b[0], b[1]);
+                mma16816(s[2 * np + 1], a, b[2], b[3]);
+            }
+        }
+        // element-wise terms; P^T packed into A fragments, then dV += P^T . dO
+        const QRec *qt_rec = sm.qr[t & 1];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            float pa_[8];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int nt = 2 * kk + hh;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int ql = nt * 8 + 2 * tig + e;
+                    const int i = iq0 + ql;
+                    const QRec qrc = qt_rec[ql];
+                    const float qv[4] = {qrc.q.x, qrc.q.y, qrc.q.z, qrc.q.w};
+                    const float inv_s = qrc.sg.x, gb = qrc.sg.y;
+                    float aa = 0.f, ab = 0.f;
+                    if (i >= first_a && i < cend) {
+                        const float w = cauchy_w(dist2_4(qv, kva), inv_g2);
+                        aa = w * inv_s;
+                        const float coef = (s[nt][e] - gb) * inv_s * (2.f * w * w * inv_g2);
+#pragma unroll
+                        for (int d = 0; d < 4; ++d)
+                            dkl_a[d] = __fmaf_rn(coef, qv[d] - kra[d], dkl_a[d]);
+                    }
+                    if (i >= first_b && i < cend) {
+                        const float w = cauchy_w(dist2_4(qv, kvb), inv_g2);
+                        ab = w * inv_s;
+                        const float coef = (s[nt][2 + e] - gb) * inv_s * (2.f * w * w * inv_g2);
+#pragma unroll
+                        for (int d = 0; d < 4; ++d)
+                            dkl_b[d] = __fmaf_rn(coef, qv[d] - krb[d], dkl_b[d]);
+                    }
+                    pa_[hh * 4 + e] = aa;
+                    pa_[hh * 4 + 2 + e] = ab;
+                }
+            }
+            uint32_t pa[4];
+            pa[0] = pack_bf16(pa_[0], pa_[1]);     // key row g,   queries 2tig..+1
+            pa[1] = pack_bf16(pa_[2], pa_[3]);     // key row g+8
+            pa[2] = pack_bf16(pa_[4], pa_[5]);     // key row g,   queries +8
+            pa[3] = pack_bf16(pa_[6], pa_[7]);     // key row g+8, queries +8
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                const int qrow = kk * 16 + (m & 1) * 8 + rr;
+                uint32_t b[4];
+                ldsm_x4_trans(b, dbase + (uint32_t)swz(qrow, np * 2 + (m >> 1)) * 2u);
+                mma16816(dva[2 * np], pa, b[0], b[1]);
+                mma16816(dva[2 * np + 1], pa, b[2], b[3]);
+            }
+        }
+        __syncthreads();
+    }
+
+    // ------------------------------------------------------- epilogue ---
+#pragma unroll
+    for (int d = 0; d < 4; ++d) {
+        dkl_a[d] += __shfl_xor_sync(kFull, dkl_a[d], 1);
+        dkl_a[d] += __shfl_xor_sync(kFull, dkl_a[d], 2);
+        dkl_b[d] += __shfl_xor_sync(kFull, dkl_b[d], 1);
+        dkl_b[d] += __shfl_xor_sync(kFull, dkl_b[d], 2);
+    }
+    const int rowa = warp * 16 + g8, rowb = rowa + 8;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+        const int col = nt * 8 + 2 * tig;
+        if (ka < jend) {
+            const float o0 = dva[nt][0] + sm.dvp[rowa][col];
+            const float o1 = dva[nt][1] + sm.dvp[rowa][col + 1];
+            *reinterpret_cast<__nv_bfloat162 *>(dv + (seg * N + ka) * (int64_t)DV + col) =
+                __floats2bfloat162_rn(o0, o1);
+        }
+        if (kbi < jend) {
+            const float o0 = dva[nt][2] + sm.dvp[rowb][col];
+            const float o1 = dva[nt][3] + sm.dvp[rowb][col + 1];
+            *reinterpret_cast<__nv_bfloat162 *>(dv + (seg * N + kbi) * (int64_t)DV + col) =
+                __floats2bfloat162_rn(o0, o1);
+        }
+    }
+    if (tig == 0) {
+        for (int d = 0; d < dK; ++d) {
+            if (ka < jend) dk[(seg * N + ka) * dK + d] = dkl_a[d] + sm.dkp[rowa][d];
+            if (kbi < jend) dk[(seg * N + kbi) * dK + d] = dkl_b[d] + sm.dkp[rowb][d];
+        }
+    }
+}
+
+}  // namespace
+
+bool attend_bwd_tc_supported(const Prob &p) {
+    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4;
+}
+
+size_t bwd_tc_rec_bytes(const Prob &p) { return sizeof(QRec) * (size_t)(p.S * p.N); }
+
+cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, const void *v,
+                                const float *gamma, const int32_t *idx, const void *dout,
+                                float *dq, void *rec, float *dg_part, int32_t *status,
+                                cudaStream_t st) {
+    const int tpc = (p.C + T64 - 1) / T64;
+    bwd_query_tc<<<dim3((unsigned)(p.n * tpc), (unsigned)p.S), THREADS, 0, st>>>(
+        q, k, static_cast<const __nv_bfloat16 *>(v), gamma, idx,
+        static_cast<const __nv_bfloat16 *>(dout), dq, static_cast<QRec *>(rec), dg_part, status,
+        p.N, p.H, p.dK, p.k, p.C, tpc);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
+                              const void *dout, const void *rec, const uint32_t *csr_q,
+                              const uint32_t *off, int64_t csr_stride, float *dk, void *dv,
+                              cudaStream_t st) {
+    const int tpc = (p.C + T64 - 1) / T64;
+    bwd_key_tc<<<dim3((unsigned)(p.n * tpc), (unsigned)p.S), THREADS, 0, st>>>(
+        k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout),
+        static_cast<const QRec *>(rec), csr_q, off, csr_stride, dk,
+        static_cast<__nv_bfloat16 *>(dv), p.N, p.H, p.dK, p.C, tpc);
+    return cudaGetLastError();
+}
+
+}  // namespace zeta

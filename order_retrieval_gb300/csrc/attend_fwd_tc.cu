@@ -19,7 +19,7 @@
 //    and mma.sync m16n8k16 accumulates in float32 registers.  Row sums of P are
 //    kept in float32 from the unrounded weights.
 //  * The two partial sums simply add (weights are in (0, 1], no rescaling).
-#include "common.cuh"
+#include "mma.cuh"
 
 namespace zeta {
 namespace {
@@ -37,48 +37,6 @@ struct __align__(16) FwdSmem {
     float swin[TQ];
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-                 "r"(src_bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
-        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint4 ld_stream16(const void *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
 __device__ __forceinline__ void bf16x8_fma(float (&acc)[8], uint4 raw, float w) {
     const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -86,14 +44,6 @@ __device__ __forceinline__ void bf16x8_fma(float (&acc)[8], uint4 raw, float w) 
         acc[2 * e] = __fmaf_rn(w, __uint_as_float(u[e] << 16), acc[2 * e]);
         acc[2 * e + 1] = __fmaf_rn(w, __uint_as_float(u[e] & 0xffff0000u), acc[2 * e + 1]);
     }
-}
-
-__device__ __forceinline__ float d2_4(const float (&a)[4], float4 b) {
-    const float e0 = a[0] - b.x, e1 = a[1] - b.y, e2 = a[2] - b.z, e3 = a[3] - b.w;
-    float d = e0 * e0;
-    d = __fmaf_rn(e1, e1, d);
-    d = __fmaf_rn(e2, e2, d);
-    return __fmaf_rn(e3, e3, d);
 }
 
 // Stage own-chunk key tile `kt` (keys cC + kt*TK ...) into buffer b.
@@ -176,7 +126,7 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     const float *p = kb + (int64_t)j * dK;
                     float4 kk = make_float4(p[0], dK > 1 ? p[1] : 0.f, dK > 2 ? p[2] : 0.f,
                                             dK > 3 ? p[3] : 0.f);
-                    w = cauchy_w(d2_4(qi, kk), inv_g2);
+                    w = cauchy_w(dist2_4(qi, kk), inv_g2);
                 }
                 sw += w;
                 uint4 buf[8];
@@ -245,8 +195,8 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     const int kl = kk0 + (h & 1) + (h >> 1) * 8;
                     const float4 kv = Ks[kl];
                     const int key = key0 + kl;
-                    const float wa = key <= lim_a ? cauchy_w(d2_4(qa, kv), inv_g2) : 0.f;
-                    const float wb = key <= lim_b ? cauchy_w(d2_4(qbv, kv), inv_g2) : 0.f;
+                    const float wa = key <= lim_a ? cauchy_w(dist2_4(qa, kv), inv_g2) : 0.f;
+                    const float wb = key <= lim_b ? cauchy_w(dist2_4(qbv, kv), inv_g2) : 0.f;
                     wv[h] = wa;
                     wv[4 + h] = wb;
                     sa += wa;

@@ -77,6 +77,18 @@ cudaError_t launch_attend_fwd_tc(const Prob &p, const float *q, const float *k, 
                                  const float *gamma, const int32_t *idx, void *out,
                                  float *rowsum, int32_t *status, cudaStream_t st);
 
+// Tensor-core backward kernels for bf16 values, d_V = 64, d_K <= 4.
+bool attend_bwd_tc_supported(const Prob &p);
+size_t bwd_tc_rec_bytes(const Prob &p);
+cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, const void *v,
+                                const float *gamma, const int32_t *idx, const void *dout,
+                                float *dq, void *rec, float *dg_part, int32_t *status,
+                                cudaStream_t st);
+cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
+                              const void *dout, const void *rec, const uint32_t *csr_q,
+                              const uint32_t *off, int64_t csr_stride, float *dk, void *dv,
+                              cudaStream_t st);
+
 size_t bwd_ws_bytes(const Prob &p);
 cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, const void *v,
                               const float *gamma, const int32_t *idx, const void *dout, float *dq,

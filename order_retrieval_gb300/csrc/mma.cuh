@@ -1,0 +1,88 @@
+// mma.cuh -- inline-PTX helpers shared by the tensor-core kernels:
+// cp.async staging, ldmatrix, mma.sync m16n8k16 (bf16 in, f32 accumulate),
+// streaming 16-byte loads and bf16 packing.
+#pragma once
+
+#include "common.cuh"
+
+namespace zeta {
+
+// Shared-memory tiles of 64 rows x 64 bf16 (128-byte rows) are stored with the
+// 16-byte chunk c of row r at chunk position c ^ (r & 7), so the eight row
+// addresses of every ldmatrix hit eight different bank groups.
+__device__ __forceinline__ int swz(int row, int chunk) { return row * 64 + ((chunk ^ (row & 7)) * 8); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 16-byte load through the non-coherent path without L1 allocation: gathered
+// rows are used once by the loading warp.
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Eight bf16 (one 16-byte chunk) -> eight floats, exactly.
+__device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
+    const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        f[2 * e] = __uint_as_float(u[e] << 16);
+        f[2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ float dist2_4(const float (&a)[4], float4 b) {
+    const float e0 = a[0] - b.x, e1 = a[1] - b.y, e2 = a[2] - b.z, e3 = a[3] - b.w;
+    float d = e0 * e0;
+    d = __fmaf_rn(e1, e1, d);
+    d = __fmaf_rn(e2, e2, d);
+    return __fmaf_rn(e3, e3, d);
+}
+
+__device__ __forceinline__ float4 load_k4(const float *row, int dK) {
+    return make_float4(row[0], dK > 1 ? row[1] : 0.f, dK > 2 ? row[2] : 0.f,
+                       dK > 3 ? row[3] : 0.f);
+}
+
+}  // namespace zeta

@@ -199,6 +199,15 @@ def test_backward_train_f32_sampled():
         _check_backward_slice(run, s)
 
 
+def test_backward_train_bf16_sampled():
+    """The timed training workload itself (bf16 values and dO, tensor-core
+    kernels), slices 0 and 31 against the oracle."""
+    run = Run(W.TRAIN, backward=True)
+    assert run.status() == 0
+    for s in (0, 31):
+        _check_backward_slice(run, s, bf16=True)
+
+
 def test_backward_clustered_bf16():
     w = W.CLUSTERED.replace(B=1)
     run = Run(w, backward=True)
@@ -272,17 +281,19 @@ TC = [
 
 
 @pytest.mark.parametrize("kw", TC, ids=lambda kw: "-".join(f"{a}{b}" for a, b in kw.items()))
-def test_forward_tensor_core_path(kw):
-    """bf16 values with d_V = 64 run the tensor-core forward; ragged tiles,
-    k up to C, d_K from 1 to 4."""
+def test_tensor_core_path(kw):
+    """bf16 values with d_V = 64 run the tensor-core forward and backward;
+    ragged tiles, k up to C, d_K from 1 to 4."""
     base = dict(name="tc", B=2, H=2, N=256, d_K=3, d_V=64, k=8, C=64, bits=10, v_dtype="bf16",
                 gamma=(0.3, 1.0), dist="uniform", v_dist="normal", seed=21)
     base.update(kw)
     w = W.Workload(**base)
-    run = Run(w)
+    run = Run(w, backward=True)
     assert run.status() == 0
     for s in range(run.S):
         _check_forward_slice(run, s, bf16=True)
+        _check_backward_slice(run, s, bf16=True)
+    assert_close_bf16(run.grads()[3], _dgamma_ref(run), what="dgamma")
 
 
 def test_empty_problem_is_a_no_op():
