@@ -225,24 +225,32 @@ bwd_key_generic(const float *__restrict__ q, const float *__restrict__ kx,
     }
 }
 
-// dgamma[h] = sum over b and i of the per-query partials, in double, fixed order.
-__global__ void __launch_bounds__(256)
-dgamma_reduce(const float *__restrict__ part, int B, int H, int N, float *__restrict__ dgamma) {
-    __shared__ double red[256];
-    const int h = blockIdx.x;
+// dgamma[h] = sum over b and i of the per-query partials, in double and in a
+// fixed order: one CTA per slice sums its N contiguous partials (tree order),
+// then one thread per head adds its B slice sums in b order.
+__global__ void __launch_bounds__(1024)
+dgamma_slices(const float *__restrict__ part, int N, double *__restrict__ slice_sum) {
+    __shared__ double red[32];
+    const float *p = part + (int64_t)blockIdx.x * N;
     double s = 0.0;
-    const int64_t total = (int64_t)B * N;
-    for (int64_t t = threadIdx.x; t < total; t += 256) {
-        const int64_t b = t / N, i = t % N;
-        s += (double)part[(b * H + h) * N + i];
-    }
-    red[threadIdx.x] = s;
+    for (int i = threadIdx.x; i < N; i += 1024) s += (double)p[i];
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
     __syncthreads();
-    for (int w = 128; w > 0; w >>= 1) {
-        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-        __syncthreads();
+    if (threadIdx.x < 32) {
+        s = red[threadIdx.x];
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+        if (threadIdx.x == 0) slice_sum[blockIdx.x] = s;
     }
-    if (threadIdx.x == 0) dgamma[h] = (float)red[0];
+}
+
+__global__ void dgamma_heads(const double *__restrict__ slice_sum, int B, int H,
+                             float *__restrict__ dgamma) {
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= H) return;
+    double s = 0.0;
+    for (int b = 0; b < B; ++b) s += slice_sum[(int64_t)b * H + h];
+    dgamma[h] = (float)s;
 }
 
 struct BwdWs {
@@ -250,6 +258,7 @@ struct BwdWs {
     float *gbar;
     float *dgp;
     void *rec;
+    double *slice_sum;
     RadixWs rw;
     uint32_t *off;
 };
@@ -263,15 +272,21 @@ BwdWs carve_bwd(const Prob &p, void *base, size_t *bytes) {
     w.gbar = cv.take<float>(rows);
     w.dgp = cv.take<float>(rows);
     w.rec = cv.take<char>(bwd_tc_rec_bytes(p));
+    w.slice_sum = cv.take<double>(p.S);
     w.rw.keys[0] = cv.take<uint32_t>(p.S * L);
     w.rw.keys[1] = cv.take<uint32_t>(p.S * L);
     w.rw.vals[0] = cv.take<uint32_t>(p.S * L);
     w.rw.vals[1] = cv.take<uint32_t>(p.S * L);
-    w.rw.hist = cv.take<uint32_t>(p.S * 256 * radix_tiles(L));
+    w.rw.hist = cv.take<uint32_t>(p.S * radix_tiles(L) * 256);
     w.rw.seglen = cv.take<uint32_t>(p.S);
     w.off = cv.take<uint32_t>(p.S * (p.N + 1));
     if (bytes) *bytes = cv.bytes();
     return w;
+}
+
+void dgamma_reduce(const Prob &p, const BwdWs &w, float *dgamma, cudaStream_t st) {
+    dgamma_slices<<<(unsigned)p.S, 1024, 0, st>>>(w.dgp, p.N, w.slice_sum);
+    dgamma_heads<<<(unsigned)((p.H + 127) / 128), 128, 0, st>>>(w.slice_sum, p.B, p.H, dgamma);
 }
 
 template <typename V, int VPL>
@@ -294,7 +309,7 @@ cudaError_t bwd_generic(const Prob &p, const float *q, const float *k, const voi
     bwd_key_generic<V, VPL><<<blocks, 256, 0, st>>>(
         q, k, static_cast<const V *>(v), gamma, w.s, static_cast<const V *>(dout), w.gbar,
         w.rw.vals[ob], w.off, L, dk, static_cast<V *>(dv), p.S, p.N, p.H, p.dK, p.dV, p.C);
-    dgamma_reduce<<<(unsigned)p.H, 256, 0, st>>>(w.dgp, p.B, p.H, p.N, dgamma);
+    dgamma_reduce(p, w, dgamma, st);
     return cudaGetLastError();
 }
 
@@ -337,7 +352,7 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
             static_cast<const uint32_t *>(w.rw.keys[ob]), w.rw.seglen, L, p.N, w.off);
         e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, w.rw.vals[ob], w.off, L, dk, dv, st);
         if (e != cudaSuccess) return e;
-        dgamma_reduce<<<(unsigned)p.H, 256, 0, st>>>(w.dgp, p.B, p.H, p.N, dgamma);
+        dgamma_reduce(p, w, dgamma, st);
         return cudaGetLastError();
     }
     if (p.vdt == ZETA_BF16)

@@ -100,11 +100,11 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
 struct RadixWs {
     void *keys[2];          // ping-pong key buffers, S * stride keys each
     uint32_t *vals[2];      // ping-pong value buffers
-    uint32_t *hist;         // S * 256 * tiles
+    uint32_t *hist;         // S * tiles * 256
     uint32_t *seglen;       // S, valid items per slice (filtered sources)
 };
 
-constexpr int kRadixThreads = 256;
+constexpr int kRadixThreads = 512;
 constexpr int kRadixItems = 8;
 constexpr int kRadixTile = kRadixThreads * kRadixItems;
 

@@ -228,7 +228,7 @@ size_t sort_ws_bytes(const Prob &p) {
     cv.take<char>(items * cb);
     cv.take<uint32_t>(items);
     cv.take<uint32_t>(items);
-    cv.take<uint32_t>(p.S * 256 * radix_tiles(p.N));
+    cv.take<uint32_t>(p.S * radix_tiles(p.N) * 256);
     cv.take<uint32_t>(p.S);
     const int64_t tiles2 = (p.N + kPT - 1) / kPT;
     cv.take<uint32_t>(p.S * tiles2 * (p.n + 1));
@@ -245,7 +245,7 @@ static cudaError_t sort_impl(const Prob &p, const K *kc, K *pcodes, int32_t *pid
     rw.keys[1] = cv.take<K>(items);
     rw.vals[0] = cv.take<uint32_t>(items);
     rw.vals[1] = cv.take<uint32_t>(items);
-    rw.hist = cv.take<uint32_t>(p.S * 256 * radix_tiles(p.N));
+    rw.hist = cv.take<uint32_t>(p.S * radix_tiles(p.N) * 256);
     rw.seglen = cv.take<uint32_t>(p.S);
     const int64_t tiles2 = (p.N + kPT - 1) / kPT;
     uint32_t *cnt = cv.take<uint32_t>(p.S * tiles2 * (p.n + 1));

@@ -6,7 +6,7 @@
 // coming from").  Here each (b, h) slice is one segment.  Every 8-bit digit pass
 // is three launches with no inter-block waiting (reduce, then scan, then
 // scatter), so nothing spins and the order is deterministic:
-//   upsweep   per tile of 2048 items: digit histogram -> hist[seg][digit][tile]
+//   upsweep   per tile of 4096 items: digit histogram -> hist[seg][tile][digit]
 //   scan      per segment: exclusive scan of hist in (digit, tile) order
 //   downsweep per tile: stable rank of every item among equal digits (warp
 //             match + per-warp counters), scatter to hist offset + rank.
@@ -50,8 +50,9 @@ struct IdxSrc {            // window indices: key = selected key, value = query
     __device__ bool load(int64_t seg, int64_t p, uint32_t &key, uint32_t &val, int32_t *st) const {
         const int32_t j = idx[seg * N * k + p];
         if (j == -1) return false;
-        const int32_t i = static_cast<int32_t>(p / k);
-        if (j < 0 || j >= (i / C) * C) { set_status(st, ZETA_ERR_BOUNDS); return false; }
+        const uint32_t i = static_cast<uint32_t>(p) / static_cast<uint32_t>(k);  // N*k < 2^31
+        const uint32_t cC = i - i % static_cast<uint32_t>(C);
+        if (static_cast<uint32_t>(j) >= cC) { set_status(st, ZETA_ERR_BOUNDS); return false; }
         key = static_cast<uint32_t>(j);
         val = static_cast<uint32_t>(i);
         return true;
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kRadixThreads)
 radix_upsweep(Src src, int shift, uint32_t *__restrict__ hist, int64_t tiles, int32_t *status) {
     __shared__ uint32_t sh[256];
     const int64_t seg = blockIdx.y, tile = blockIdx.x;
-    sh[threadIdx.x] = 0;
+    if (threadIdx.x < 256) sh[threadIdx.x] = 0;
     __syncthreads();
     const int64_t len = src.len(seg);
     const int64_t base = tile * kRadixTile;
@@ -77,44 +78,59 @@ radix_upsweep(Src src, int shift, uint32_t *__restrict__ hist, int64_t tiles, in
         }
     }
     __syncthreads();
-    hist[(seg * 256 + threadIdx.x) * tiles + tile] = sh[threadIdx.x];
+    if (threadIdx.x < 256) hist[(seg * tiles + tile) * 256 + threadIdx.x] = sh[threadIdx.x];
 }
 
-// Exclusive scan of one segment's 256*tiles counters; total -> seglen[seg].
+// Exclusive scan of one segment's counters in (digit, tile) order, stored as
+// hist[seg][tile][digit]; total -> seglen[seg].  1024 threads = 256 digits x 4
+// tile ranges; every load row is one coalesced 1 KB line.
 __global__ void __launch_bounds__(1024)
 radix_scan(uint32_t *__restrict__ hist, int64_t tiles, uint32_t *seglen) {
-    __shared__ uint32_t warp_sum[32];
-    const int64_t L = 256 * tiles;
-    uint32_t *h = hist + blockIdx.x * L;
-    const int64_t per = (L + 1023) / 1024;
-    const int64_t beg = threadIdx.x * per;
-    const int64_t end = beg + per < L ? beg + per : L;
-    uint32_t sum = 0;
-    for (int64_t i = beg; i < end; ++i) sum += h[i];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    uint32_t inc = sum;
-    for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(kFull, inc, o);
-        if (lane >= o) inc += y;
-    }
-    if (lane == 31) warp_sum[wid] = inc;
+    __shared__ uint32_t part[4][256];
+    __shared__ uint32_t dsum[256];
+    const int d = threadIdx.x & 255, qtr = threadIdx.x >> 8;
+    uint32_t *h = hist + blockIdx.x * tiles * 256;
+    const int64_t per = (tiles + 3) / 4;
+    const int64_t t0 = qtr * per;
+    const int64_t t1 = t0 + per < tiles ? t0 + per : tiles;
+    uint32_t s = 0;
+#pragma unroll 8
+    for (int64_t t = t0; t < t1; ++t) s += h[t * 256 + d];
+    part[qtr][d] = s;
     __syncthreads();
-    if (wid == 0) {
-        uint32_t x = warp_sum[lane], s = x;
+    if (threadIdx.x < 256) {
+        const uint32_t tot = part[0][d] + part[1][d] + part[2][d] + part[3][d];
+        // exclusive scan of the 256 digit totals by warps of 32 + a second level
+        const int lane = d & 31, w = d >> 5;
+        uint32_t inc = tot;
         for (int o = 1; o < 32; o <<= 1) {
-            uint32_t y = __shfl_up_sync(kFull, s, o);
-            if (lane >= o) s += y;
+            const uint32_t y = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += y;
         }
-        warp_sum[lane] = s - x;    // exclusive warp offsets
+        dsum[d] = inc;                        // inclusive within the warp
+        __syncwarp();
+        (void)w;
     }
     __syncthreads();
-    uint32_t run = warp_sum[wid] + inc - sum;
-    for (int64_t i = beg; i < end; ++i) {
-        uint32_t t = h[i];
-        h[i] = run;
-        run += t;
+    if (threadIdx.x == 0) {                   // carry across the 8 warps
+        uint32_t carry = 0;
+        for (int w = 0; w < 8; ++w) {
+            const uint32_t last = dsum[w * 32 + 31];
+            for (int l = 0; l < 32; ++l) dsum[w * 32 + l] += carry;
+            carry += last;
+        }
+        if (seglen) seglen[blockIdx.x] = carry;
     }
-    if (threadIdx.x == 1023 && seglen) seglen[blockIdx.x] = run;
+    __syncthreads();
+    const uint32_t tot_d = part[0][d] + part[1][d] + part[2][d] + part[3][d];
+    uint32_t run = dsum[d] - tot_d;           // exclusive digit base
+    for (int q = 0; q < qtr; ++q) run += part[q][d];
+#pragma unroll 8
+    for (int64_t t = t0; t < t1; ++t) {
+        const uint32_t x = h[t * 256 + d];
+        h[t * 256 + d] = run;
+        run += x;
+    }
 }
 
 template <typename K, typename Src>
@@ -128,8 +144,8 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
     const int64_t len = src.len(seg);
     const int64_t base = tile * kRadixTile;
     if (base >= len) return;
-    soff[threadIdx.x] = hist[(seg * 256 + threadIdx.x) * tiles + tile];
-    for (int w = 0; w < W; ++w) wcnt[w][threadIdx.x] = 0;
+    if (threadIdx.x < 256) soff[threadIdx.x] = hist[(seg * tiles + tile) * 256 + threadIdx.x];
+    for (int x = threadIdx.x; x < W * 256; x += kRadixThreads) (&wcnt[0][0])[x] = 0;
     __syncthreads();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const unsigned lt = lanemask_lt();
@@ -154,7 +170,7 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
         __syncwarp();
     }
     __syncthreads();
-    {
+    if (threadIdx.x < 256) {
         uint32_t run = 0;
         for (int ww = 0; ww < W; ++ww) {
             uint32_t c = wcnt[ww][threadIdx.x];
