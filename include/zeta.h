@@ -113,6 +113,31 @@ zeta_status_t zeta_sort_chunks(const zeta_problem_t *p, const void *key_codes,
                                void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * zeta_sort_chunks_noalloc -- zeta_sort_chunks without a workspace argument,
+ * for callers that cannot allocate device memory when they need the sorted
+ * prefixes (code running inside an allocator or memory-pool callback, plug-ins
+ * whose host framework owns every device allocation, processes whose device
+ * footprint must stay fixed after start-up).  The pages have no counterpart:
+ * this is an interface convenience, not part of the method.
+ * Scratch: one file-scope device array of 32 MiB, which every GPU that loads
+ * this library holds until the process exits.  Problems whose
+ * zeta_sort_workspace_bytes exceeds 32 MiB are rejected with
+ * ZETA_ERR_WORKSPACE before anything is launched.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress and caches it; make that
+ * first call before any stream capture on that device.
+ * Sharing: every call uses the same array, which keeps the previous call's
+ * contents (nothing in it needs to start at zero).  Calls whose work overlaps
+ * on the GPU (different streams, or different host threads on one device)
+ * race on the array; order them on one stream.
+ * Arguments, results and other errors are those of zeta_sort_chunks.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+zeta_status_t zeta_sort_chunks_noalloc(const zeta_problem_t *p, const void *key_codes,
+                                       void *prefix_codes, int32_t *prefix_idx,
+                                       cudaStream_t stream);
+
+/*
  * zeta_select_topk -- the k keys around each query's insertion rank.
  * Passage: OpenReview reply A3 (binary search of the insertion position) and
  * reply A2 "Clarification" (the window centred at the insertion position).

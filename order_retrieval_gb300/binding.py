@@ -181,6 +181,24 @@ def zeta_sort_chunks(p, key_codes, prefix_codes, prefix_idx, workspace, stream=N
                                   _ptr(prefix_idx), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
+def zeta_sort_chunks_noalloc(p, key_codes, prefix_codes, prefix_idx, stream=None):
+    """zeta_sort_chunks with the library's own fixed 32 MiB device scratch
+    (for callers that cannot allocate a workspace)."""
+    L = lib()
+    fn = L.zeta_sort_chunks_noalloc
+    fn.argtypes = [ctypes.POINTER(zeta_problem_t), ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    S = p.B * p.H
+    T = zeta_prefix_entries(p)
+    _expect(key_codes, "key_codes", code_dtype(p), S * p.N)
+    _expect(prefix_codes, "prefix_codes", code_dtype(p), S * T)
+    _expect(prefix_idx, "prefix_idx", torch.int32, S * T)
+    _check("zeta_sort_chunks_noalloc",
+           fn(ctypes.byref(p), _ptr(key_codes), _ptr(prefix_codes), _ptr(prefix_idx),
+              _stream(stream)))
+
+
 def zeta_select_topk(p, q_codes, prefix_codes, prefix_idx, idx, stream=None):
     S = p.B * p.H
     _expect(q_codes, "q_codes", code_dtype(p), S * p.N)
