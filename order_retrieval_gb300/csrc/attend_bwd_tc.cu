@@ -37,6 +37,44 @@ struct __align__(16) QRec {
     float4 sg;
 };
 
+// Sums over the warp of 16 values per lane with 16 shuffles (recursive
+// halving); lane L returns the total of value (L >> 1).
+__device__ __forceinline__ float warp_transpose_sum16(float (&v)[16], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const float r = __shfl_xor_sync(kFull, b4 ? v[m] : v[m + 8], 16);
+        v[m] = (b4 ? v[m + 8] : v[m]) + r;
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float r = __shfl_xor_sync(kFull, b3 ? v[m] : v[m + 4], 8);
+        v[m] = (b3 ? v[m + 4] : v[m]) + r;
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const float r = __shfl_xor_sync(kFull, b2 ? v[m] : v[m + 2], 4);
+        v[m] = (b2 ? v[m + 2] : v[m]) + r;
+    }
+    {
+        const float r = __shfl_xor_sync(kFull, b1 ? v[0] : v[1], 2);
+        v[0] = (b1 ? v[1] : v[0]) + r;
+    }
+    return v[0] + __shfl_xor_sync(kFull, v[0], 1);
+}
+
+template <int DK>
+__device__ __forceinline__ float dist2k(const float (&a)[4], float4 b) {
+    float d = 0.f;
+    const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int x = 0; x < DK; ++x) {
+        const float e = a[x] - bb[x];
+        d = __fmaf_rn(e, e, d);
+    }
+    return d;
+}
+
 __device__ __forceinline__ float warp_group8_sum(float x) {
     x += __shfl_xor_sync(kFull, x, 1);
     x += __shfl_xor_sync(kFull, x, 2);
@@ -94,12 +132,13 @@ struct QAcc {
     }
 };
 
+template <int DK>
 __global__ void __launch_bounds__(THREADS, 4)
 bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
              const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
              const int32_t *__restrict__ idx, const __nv_bfloat16 *__restrict__ dout,
              float *__restrict__ dq, QRec *__restrict__ rec, float *__restrict__ dg_part,
-             int32_t *status, int N, int H, int dK, int k, int C, int tiles_per_chunk) {
+             int32_t *status, int N, int H, int k, int C, int tiles_per_chunk) {
     __shared__ QSmem sm;
     const int64_t seg = blockIdx.y;
     const int c = blockIdx.x / tiles_per_chunk;
@@ -111,8 +150,8 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
     const float gm = gamma[seg % H];
     const float inv_g2 = __frcp_rn(gm * gm);
     const float inv_g = __frcp_rn(gm);
-    const float *kb = kx + seg * (int64_t)N * dK;
-    const float *qb = q + seg * (int64_t)N * dK;
+    const float *kb = kx + seg * (int64_t)N * DK;
+    const float *qb = q + seg * (int64_t)N * DK;
     const __nv_bfloat16 *vb = v + seg * (int64_t)N * DV;
     const __nv_bfloat16 *db = dout + seg * (int64_t)N * DV;
     const int nkt = (iend - 1 - cC) / T64 + 1;
@@ -122,7 +161,7 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
         if (threadIdx.x < T64) {
             const int key = key0 + threadIdx.x;
             sm.kt[b][threadIdx.x] =
-                key < cend ? load_k4(kb + (int64_t)key * dK, dK) : make_float4(0.f, 0.f, 0.f, 0.f);
+                key < cend ? load_k4(kb + (int64_t)key * DK, DK) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
     stage_rows(sm.dO, db, i0, iend);
@@ -130,71 +169,85 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
     cp_async_commit();
 
     // ---------------------------------------------------- window part ---
+    // A pass covers up to 64 selected keys.  Lane L owns slots L and L+32 (index,
+    // coordinates, the pair's Cauchy terms); eight lanes form g_ij for one value
+    // row (16-byte slice dot + 3 shuffles) and the owner picks it up with one
+    // shuffle.  The next query's indices are fetched while this one runs.
     const int grp = lane >> 3, sub = lane & 7;
+    const int wq0 = i0 + warp * 16;
+    const int nqw = c > 0 ? max(0, min(16, iend - wq0)) : 0;
+    auto load_idx = [&](int i, int t0, int (&j)[2]) {
+        const int32_t *irow = idx + (seg * N + i) * (int64_t)k + t0;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const int t = t0 + s * 32 + lane;
+            j[s] = t < k ? __ldg(irow + s * 32 + lane) : -1;
+        }
+    };
+    int jn[2] = {-1, -1};
+    if (nqw > 0) load_idx(wq0, 0, jn);
     for (int r = 0; r < 16; ++r) {
         const int row = warp * 16 + r;
-        const int i = i0 + row;
         QAcc acc;
         acc.zero();
-        if (c > 0 && i < iend) {
+        if (r < nqw) {
+            const int i = wq0 + r;
             float qi[4];
 #pragma unroll
-            for (int d = 0; d < 4; ++d) qi[d] = d < dK ? qb[(int64_t)i * dK + d] : 0.f;
+            for (int d = 0; d < 4; ++d) qi[d] = d < DK ? qb[(int64_t)i * DK + d] : 0.f;
             float do8[8];
-            unpack8(*reinterpret_cast<const uint4 *>(db + (int64_t)i * DV + sub * 8),
-                    do8);
-            const int32_t *irow = idx + (seg * N + i) * (int64_t)k;
-            for (int t0 = 0; t0 < k; t0 += 32) {
-                int j = -1;
-                if (t0 + lane < k) {
-                    j = __ldg(irow + t0 + lane);
-                    if (j != -1 && (unsigned)j >= (unsigned)cC) {
+            unpack8(*reinterpret_cast<const uint4 *>(db + (int64_t)i * DV + sub * 8), do8);
+            for (int t0 = 0; t0 < k; t0 += 64) {
+                int j[2] = {jn[0], jn[1]};
+                if (t0 + 64 < k) load_idx(i, t0 + 64, jn);
+                else if (r + 1 < nqw) load_idx(i + 1, 0, jn);
+                float4 kk[2];
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    if (j[s] != -1 && (unsigned)j[s] >= (unsigned)cC) {
                         set_status(status, ZETA_ERR_BOUNDS);
-                        j = -1;
+                        j[s] = -1;
                     }
+                    kk[s] = j[s] >= 0 ? load_k4(kb + (int64_t)j[s] * DK, DK)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                const int nu = min(8, (k - t0 + 3) >> 2);
-                uint4 buf[8];
-                float4 kk[8];
-                int jr[8];
+                const int nu = min(16, (k - t0 + 3) >> 2);
+                uint4 buf[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    jr[u] = __shfl_sync(kFull, j, u * 4 + grp);
-                    if (u < nu && jr[u] >= 0) {
-                        buf[u] = ld_stream16(vb + (int64_t)jr[u] * DV + sub * 8);
-                        kk[u] = load_k4(kb + (int64_t)jr[u] * dK, dK);
-                    }
+                for (int u = 0; u < 16; ++u) {
+                    const int jr = __shfl_sync(kFull, j[u >> 3], (u * 4 + grp) & 31);
+                    buf[u] = (u < nu && jr >= 0) ? ld_stream16(vb + (int64_t)jr * DV + sub * 8)
+                                                 : make_uint4(0u, 0u, 0u, 0u);
                 }
+                float gown[2] = {0.f, 0.f};
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (u >= nu) break;
-                    float g = 0.f;
-                    if (jr[u] >= 0) {
+                for (int u = 0; u < 16; ++u) {
+                    if (u < nu) {
                         float v8[8];
                         unpack8(buf[u], v8);
+                        float g0 = 0.f, g1 = 0.f;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) g = __fmaf_rn(do8[e], v8[e], g);
-                    }
-                    g = warp_group8_sum(g);
-                    if (jr[u] >= 0) {
-                        const float w = cauchy_w(dist2_4(qi, kk[u]), inv_g2);
-                        acc.add(w, g, qi, kk[u], inv_g2, inv_g);
+                        for (int e = 0; e < 8; e += 2) {
+                            g0 = __fmaf_rn(do8[e], v8[e], g0);
+                            g1 = __fmaf_rn(do8[e + 1], v8[e + 1], g1);
+                        }
+                        const float g = warp_group8_sum(g0 + g1);
+                        const float gx = __shfl_sync(kFull, g, (lane & 3) * 8);
+                        if ((u & 7) == (lane >> 2)) gown[u >> 3] = gx;
                     }
                 }
-            }
 #pragma unroll
-            for (int y = 0; y < 12; ++y) {
-                acc.x[y] += __shfl_xor_sync(kFull, acc.x[y], 8);
-                acc.x[y] += __shfl_xor_sync(kFull, acc.x[y], 16);
+                for (int s = 0; s < 2; ++s)
+                    if (j[s] >= 0)
+                        acc.add(cauchy_w_fast(dist2k<DK>(qi, kk[s]), inv_g2), gown[s], qi, kk[s],
+                                inv_g2, inv_g);
             }
         }
-        if (lane < 12) {
-            float val = 0.f;
+        float tv[16];
 #pragma unroll
-            for (int y = 0; y < 12; ++y)
-                if (y == lane) val = acc.x[y];
-            sm.part[row][lane] = val;
-        }
+        for (int y = 0; y < 16; ++y) tv[y] = y < 12 ? acc.x[y] : 0.f;
+        const float tot = warp_transpose_sum16(tv, lane);      // value (lane >> 1)
+        if (!(lane & 1) && (lane >> 1) < 12) sm.part[row][lane >> 1] = tot;
     }
 
     // ------------------------------------------------- own-chunk part ---
@@ -203,8 +256,8 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
     float qa[4], qbv[4];
 #pragma unroll
     for (int d = 0; d < 4; ++d) {
-        qa[d] = (ra < iend && d < dK) ? qb[(int64_t)ra * dK + d] : 0.f;
-        qbv[d] = (rb < iend && d < dK) ? qb[(int64_t)rb * dK + d] : 0.f;
+        qa[d] = (ra < iend && d < DK) ? qb[(int64_t)ra * DK + d] : 0.f;
+        qbv[d] = (rb < iend && d < DK) ? qb[(int64_t)rb * DK + d] : 0.f;
     }
     const int lim_a = ra < iend ? ra : -1, lim_b = rb < iend ? rb : -1;
     const int warp_last = min(i0 + warp * 16 + 15, iend - 1);
@@ -254,9 +307,9 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     const int key = key0 + kl;
                     const float4 kv = Ks[kl];
                     if (key <= lim_a)
-                        la.add(cauchy_w(dist2_4(qa, kv), inv_g2), s[nt][e], qa, kv, inv_g2, inv_g);
+                        la.add(cauchy_w_fast(dist2k<DK>(qa, kv), inv_g2), s[nt][e], qa, kv, inv_g2, inv_g);
                     if (key <= lim_b)
-                        lb.add(cauchy_w(dist2_4(qbv, kv), inv_g2), s[nt][2 + e], qbv, kv, inv_g2,
+                        lb.add(cauchy_w_fast(dist2k<DK>(qbv, kv), inv_g2), s[nt][2 + e], qbv, kv, inv_g2,
                                inv_g);
                 }
         }
@@ -282,7 +335,7 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
             const float inv_s = __frcp_rn(t[0]);
             const float gb = t[1] * inv_s;
             const int64_t gi = seg * N + i;
-            for (int d = 0; d < dK; ++d) dq[gi * dK + d] = (t[4 + d] - gb * t[8 + d]) * inv_s;
+            for (int d = 0; d < DK; ++d) dq[gi * DK + d] = (t[4 + d] - gb * t[8 + d]) * inv_s;
             dg_part[gi] = (t[2] - gb * t[3]) * inv_s;
             const float *qq = tig == 0 ? qa : qbv;
             QRec rcd;
@@ -303,12 +356,13 @@ struct __align__(16) KSmem {
     float dkp[T64][4];
 };
 
+template <int DK>
 __global__ void __launch_bounds__(THREADS, 4)
 bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
            const float *__restrict__ gamma, const __nv_bfloat16 *__restrict__ dout,
            const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q,
            const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
-           __nv_bfloat16 *__restrict__ dv, int N, int H, int dK, int C, int tiles_per_chunk) {
+           __nv_bfloat16 *__restrict__ dv, int N, int H, int C, int tiles_per_chunk) {
     __shared__ KSmem sm;
     const int64_t seg = blockIdx.y;
     const int c = blockIdx.x / tiles_per_chunk;
@@ -319,7 +373,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float gm = gamma[seg % H];
     const float inv_g2 = __frcp_rn(gm * gm);
-    const float *kb = kx + seg * (int64_t)N * dK;
+    const float *kb = kx + seg * (int64_t)N * DK;
     const __nv_bfloat16 *vb = v + seg * (int64_t)N * DV;
     const __nv_bfloat16 *db = dout + seg * (int64_t)N * DV;
     const QRec *rb_ = rec + seg * (int64_t)N;
@@ -352,36 +406,51 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
         if (j < jend) {
             float v8[8];
             unpack8(*reinterpret_cast<const uint4 *>(vb + (int64_t)j * DV + sub * 8), v8);
-            const float4 kj = load_k4(kb + (int64_t)j * dK, dK);
+            const float4 kj = load_k4(kb + (int64_t)j * DK, DK);
+            // Sixteen listed queries per step (four per lane group), their list
+            // positions fetched one step ahead.
             const int64_t p0 = ob[j], p1 = ob[j + 1];
-            for (int64_t p = p0; p < p1; p += 8) {
-                uint4 dbuf[2];
-                QRec qrec[2];
-                bool ok[2];
+            uint32_t inext[4];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int64_t pp = p + h * 4 + grp;
-                    ok[h] = pp < p1;
-                    if (ok[h]) {
-                        const uint32_t i = __ldg(lst + pp);
-                        dbuf[h] = ld_stream16(db + (int64_t)i * DV + sub * 8);
-                        qrec[h] = rb_[i];
+            for (int h = 0; h < 4; ++h) {
+                const int64_t pp = p0 + h * 4 + grp;
+                inext[h] = pp < p1 ? __ldg(lst + pp) : 0xffffffffu;
+            }
+            for (int64_t p = p0; p < p1; p += 16) {
+                uint32_t ic[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    ic[h] = inext[h];
+                    const int64_t pp = p + 16 + h * 4 + grp;
+                    inext[h] = pp < p1 ? __ldg(lst + pp) : 0xffffffffu;
+                }
+                uint4 dbuf[4];
+                QRec qrec[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    if (ic[h] != 0xffffffffu) {
+                        dbuf[h] = ld_stream16(db + (int64_t)ic[h] * DV + sub * 8);
+                        qrec[h] = rb_[ic[h]];
                     }
                 }
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < 4; ++h) {
+                    const bool ok = ic[h] != 0xffffffffu;
                     float d8[8];
-                    float g = 0.f;
-                    if (ok[h]) {
+                    float g0 = 0.f, g1 = 0.f;
+                    if (ok) {
                         unpack8(dbuf[h], d8);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) g = __fmaf_rn(d8[e], v8[e], g);
+                        for (int e = 0; e < 8; e += 2) {
+                            g0 = __fmaf_rn(d8[e], v8[e], g0);
+                            g1 = __fmaf_rn(d8[e + 1], v8[e + 1], g1);
+                        }
                     }
-                    g = warp_group8_sum(g);
-                    if (ok[h]) {
+                    const float g = warp_group8_sum(g0 + g1);
+                    if (ok) {
                         const float4 qi = qrec[h].q;
                         const float qv[4] = {qi.x, qi.y, qi.z, qi.w};
-                        const float w = cauchy_w(dist2_4(qv, kj), inv_g2);
+                        const float w = cauchy_w_fast(dist2k<DK>(qv, kj), inv_g2);
                         const float inv_s = qrec[h].sg.x;
                         const float a = w * inv_s;
                         const float dldw = (g - qrec[h].sg.y) * inv_s;
@@ -418,8 +487,8 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     // ------------------------------------------------- own-chunk part ---
     const int g8 = lane >> 2, tig = lane & 3;
     const int ka = j0 + warp * 16 + g8, kbi = ka + 8;      // this thread's two key rows
-    const float4 kva = ka < jend ? load_k4(kb + (int64_t)ka * dK, dK) : make_float4(0, 0, 0, 0);
-    const float4 kvb = kbi < jend ? load_k4(kb + (int64_t)kbi * dK, dK) : make_float4(0, 0, 0, 0);
+    const float4 kva = ka < jend ? load_k4(kb + (int64_t)ka * DK, DK) : make_float4(0, 0, 0, 0);
+    const float4 kvb = kbi < jend ? load_k4(kb + (int64_t)kbi * DK, DK) : make_float4(0, 0, 0, 0);
     const float kra[4] = {kva.x, kva.y, kva.z, kva.w};
     const float krb[4] = {kvb.x, kvb.y, kvb.z, kvb.w};
     const int first_a = ka < jend ? ka : 0x7fffffff;     // first query index row a may see
@@ -476,7 +545,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                     const float inv_s = qrc.sg.x, gb = qrc.sg.y;
                     float aa = 0.f, ab = 0.f;
                     if (i >= first_a && i < cend) {
-                        const float w = cauchy_w(dist2_4(qv, kva), inv_g2);
+                        const float w = cauchy_w_fast(dist2k<DK>(qv, kva), inv_g2);
                         aa = w * inv_s;
                         const float coef = (s[nt][e] - gb) * inv_s * (2.f * w * w * inv_g2);
 #pragma unroll
@@ -484,7 +553,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                             dkl_a[d] = __fmaf_rn(coef, qv[d] - kra[d], dkl_a[d]);
                     }
                     if (i >= first_b && i < cend) {
-                        const float w = cauchy_w(dist2_4(qv, kvb), inv_g2);
+                        const float w = cauchy_w_fast(dist2k<DK>(qv, kvb), inv_g2);
                         ab = w * inv_s;
                         const float coef = (s[nt][2 + e] - gb) * inv_s * (2.f * w * w * inv_g2);
 #pragma unroll
@@ -538,9 +607,9 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
         }
     }
     if (tig == 0) {
-        for (int d = 0; d < dK; ++d) {
-            if (ka < jend) dk[(seg * N + ka) * dK + d] = dkl_a[d] + sm.dkp[rowa][d];
-            if (kbi < jend) dk[(seg * N + kbi) * dK + d] = dkl_b[d] + sm.dkp[rowb][d];
+        for (int d = 0; d < DK; ++d) {
+            if (ka < jend) dk[(seg * N + ka) * DK + d] = dkl_a[d] + sm.dkp[rowa][d];
+            if (kbi < jend) dk[(seg * N + kbi) * DK + d] = dkl_b[d] + sm.dkp[rowb][d];
         }
     }
 }
@@ -558,10 +627,19 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
                                 float *dq, void *rec, float *dg_part, int32_t *status,
                                 cudaStream_t st) {
     const int tpc = (p.C + T64 - 1) / T64;
-    bwd_query_tc<<<dim3((unsigned)(p.n * tpc), (unsigned)p.S), THREADS, 0, st>>>(
-        q, k, static_cast<const __nv_bfloat16 *>(v), gamma, idx,
-        static_cast<const __nv_bfloat16 *>(dout), dq, static_cast<QRec *>(rec), dg_part, status,
-        p.N, p.H, p.dK, p.k, p.C, tpc);
+    const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
+#define ZETA_BQ(D)                                                                              \
+    bwd_query_tc<D><<<grid, THREADS, 0, st>>>(                                                 \
+        q, k, static_cast<const __nv_bfloat16 *>(v), gamma, idx,                              \
+        static_cast<const __nv_bfloat16 *>(dout), dq, static_cast<QRec *>(rec), dg_part, status, \
+        p.N, p.H, p.k, p.C, tpc)
+    switch (p.dK) {
+        case 1: ZETA_BQ(1); break;
+        case 2: ZETA_BQ(2); break;
+        case 3: ZETA_BQ(3); break;
+        default: ZETA_BQ(4); break;
+    }
+#undef ZETA_BQ
     return cudaGetLastError();
 }
 
@@ -570,10 +648,19 @@ cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, cons
                               const uint32_t *off, int64_t csr_stride, float *dk, void *dv,
                               cudaStream_t st) {
     const int tpc = (p.C + T64 - 1) / T64;
-    bwd_key_tc<<<dim3((unsigned)(p.n * tpc), (unsigned)p.S), THREADS, 0, st>>>(
-        k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout),
-        static_cast<const QRec *>(rec), csr_q, off, csr_stride, dk,
-        static_cast<__nv_bfloat16 *>(dv), p.N, p.H, p.dK, p.C, tpc);
+    const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
+#define ZETA_BK(D)                                                                              \
+    bwd_key_tc<D><<<grid, THREADS, 0, st>>>(                                                   \
+        k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout), \
+        static_cast<const QRec *>(rec), csr_q, off, csr_stride, dk,                           \
+        static_cast<__nv_bfloat16 *>(dv), p.N, p.H, p.C, tpc)
+    switch (p.dK) {
+        case 1: ZETA_BK(1); break;
+        case 2: ZETA_BK(2); break;
+        case 3: ZETA_BK(3); break;
+        default: ZETA_BK(4); break;
+    }
+#undef ZETA_BK
     return cudaGetLastError();
 }
 

@@ -7,11 +7,12 @@
 // organised for GB300:
 //
 //  * One CTA = 64 consecutive queries of one chunk (4 warps x 16 rows).
-//  * Window part (HBM-bound gather): a warp takes one query at a time; each
-//    lane computes the Cauchy weight of one selected key, then eight lanes read
-//    one 128-byte bf16 value row with 16-byte loads (four rows per warp load,
-//    all loads of a 32-key group issued before any is used) and accumulate in
-//    float32.  Partial sums (sum w v, sum w) go to shared memory.
+//  * Window part (a gather): a warp takes one query at a time; each lane owns
+//    two selected keys (index, coordinates, Cauchy weight), and eight lanes read
+//    one 128-byte bf16 value row with 16-byte loads, four rows per warp load,
+//    all 16 loads of a 64-key pass in flight together; the next query's indices
+//    are fetched while the current query is processed.  Partial sums
+//    (sum w v, sum w) go to shared memory in float32.
 //  * Own-chunk part (a dense causal C x C/2 x 64 contraction per chunk): key
 //    tiles of 64 rows are staged by cp.async into XOR-swizzled shared memory
 //    (double buffered); each thread builds its slice of the weight tile P
@@ -36,6 +37,18 @@ struct __align__(16) FwdSmem {
     float win[TQ][WPAD];
     float swin[TQ];
 };
+
+template <int DK>
+__device__ __forceinline__ float dist2k(const float (&a)[4], float4 b) {
+    float d = 0.f;
+    const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int x = 0; x < DK; ++x) {
+        const float e = a[x] - bb[x];
+        d = __fmaf_rn(e, e, d);
+    }
+    return d;
+}
 
 __device__ __forceinline__ void bf16x8_fma(float (&acc)[8], uint4 raw, float w) {
     const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -74,11 +87,12 @@ __device__ __forceinline__ void load_tile(FwdSmem &sm, int b, const float *kb,
     }
 }
 
+template <int DK>
 __global__ void __launch_bounds__(THREADS, 4)
 attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
               const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
               const int32_t *__restrict__ idx, __nv_bfloat16 *__restrict__ out,
-              float *__restrict__ rowsum, int32_t *status, int N, int H, int dK, int k, int C,
+              float *__restrict__ rowsum, int32_t *status, int N, int H, int k, int C,
               int tiles_per_chunk) {
     __shared__ FwdSmem sm;
     const int64_t seg = blockIdx.y;
@@ -91,56 +105,82 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float gm = gamma[seg % H];
     const float inv_g2 = __frcp_rn(gm * gm);
-    const float *kb = kx + seg * (int64_t)N * dK;
-    const float *qb = q + seg * (int64_t)N * dK;
+    const float *kb = kx + seg * (int64_t)N * DK;
+    const float *qb = q + seg * (int64_t)N * DK;
     const __nv_bfloat16 *vb = v + seg * (int64_t)N * DV;
 
     const int nkt = (iend - 1 - cC) / TK + 1;     // own-chunk key tiles up to the last query
-    load_tile(sm, 0, kb, vb, cC, cend, dK);
+    load_tile(sm, 0, kb, vb, cC, cend, DK);
     cp_async_commit();
 
     // ------------------------------------------------------ window part ---
+    // A pass covers up to 64 selected keys: lane L owns slots L and L+32
+    // (index, key coordinates, weight); the 16 value-row loads of the pass are
+    // all issued before any is used, and the first pass's indices of the next
+    // query are fetched while the current one is processed.
+    const int wq0 = i0 + warp * 16;
+    const int nqw = c > 0 ? max(0, min(16, iend - wq0)) : 0;
+    const int grp = lane >> 3, sub = lane & 7;
+    auto load_idx = [&](int i, int t0, int (&j)[2]) {
+        const int32_t *irow = idx + (seg * N + i) * (int64_t)k + t0;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const int t = t0 + s * 32 + lane;
+            j[s] = t < k ? __ldg(irow + s * 32 + lane) : -1;
+        }
+    };
+    int jn[2] = {-1, -1};
+    if (nqw > 0) load_idx(wq0, 0, jn);
     for (int r = 0; r < 16; ++r) {
         const int row = warp * 16 + r;
-        const int i = i0 + row;
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
         float sw = 0.f;
-        if (c > 0 && i < iend) {
+        if (r < nqw) {
+            const int i = wq0 + r;
             float qi[4];
 #pragma unroll
-            for (int d = 0; d < 4; ++d) qi[d] = d < dK ? qb[(int64_t)i * dK + d] : 0.f;
-            const int32_t *irow = idx + (seg * N + i) * (int64_t)k;
-            for (int t0 = 0; t0 < k; t0 += 32) {
-                int j = -1;
-                if (t0 + lane < k) {
-                    j = __ldg(irow + t0 + lane);
-                    if (j != -1 && (unsigned)j >= (unsigned)cC) {
+            for (int d = 0; d < 4; ++d) qi[d] = d < DK ? qb[(int64_t)i * DK + d] : 0.f;
+            for (int t0 = 0; t0 < k; t0 += 64) {
+                int j[2] = {jn[0], jn[1]};
+                if (t0 + 64 < k) {
+                    load_idx(i, t0 + 64, jn);              // next pass of this query
+                } else if (r + 1 < nqw) {
+                    load_idx(i + 1, 0, jn);                // first pass of the next query
+                }
+                float4 kk[2];
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    if (j[s] != -1 && (unsigned)j[s] >= (unsigned)cC) {
                         set_status(status, ZETA_ERR_BOUNDS);
-                        j = -1;
+                        j[s] = -1;
+                    }
+                    kk[s] = j[s] >= 0 ? load_k4(kb + (int64_t)j[s] * DK, DK)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                const int nu = min(16, (k - t0 + 3) >> 2);   // 4-row loads in this pass
+                uint4 buf[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int src = u * 4 + grp;
+                    const int jr = __shfl_sync(kFull, j[u >> 3], src & 31);
+                    buf[u] = (u < nu && jr >= 0) ? ld_stream16(vb + (int64_t)jr * DV + sub * 8)
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+                }
+                float w[2];
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    w[s] = j[s] >= 0 ? cauchy_w_fast(dist2k<DK>(qi, kk[s]), inv_g2) : 0.f;
+                    sw += w[s];
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    if (u < nu) {
+                        const float wr = __shfl_sync(kFull, w[u >> 3], (u * 4 + grp) & 31);
+                        bf16x8_fma(acc, buf[u], wr);
                     }
                 }
-                float w = 0.f;
-                if (j >= 0) {
-                    const float *p = kb + (int64_t)j * dK;
-                    float4 kk = make_float4(p[0], dK > 1 ? p[1] : 0.f, dK > 2 ? p[2] : 0.f,
-                                            dK > 3 ? p[3] : 0.f);
-                    w = cauchy_w(dist2_4(qi, kk), inv_g2);
-                }
-                sw += w;
-                uint4 buf[8];
-                float wr[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int src = u * 4 + (lane >> 3);
-                    const int jr = __shfl_sync(kFull, j, src);
-                    wr[u] = __shfl_sync(kFull, w, src);
-                    buf[u] = jr >= 0 ? ld_stream16(vb + (int64_t)jr * DV + (lane & 7) * 8)
-                                     : make_uint4(0u, 0u, 0u, 0u);
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) bf16x8_fma(acc, buf[u], wr[u]);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -164,8 +204,8 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     float qa[4], qbv[4];
 #pragma unroll
     for (int d = 0; d < 4; ++d) {
-        qa[d] = (ra < iend && d < dK) ? qb[(int64_t)ra * dK + d] : 0.f;
-        qbv[d] = (rb < iend && d < dK) ? qb[(int64_t)rb * dK + d] : 0.f;
+        qa[d] = (ra < iend && d < DK) ? qb[(int64_t)ra * DK + d] : 0.f;
+        qbv[d] = (rb < iend && d < DK) ? qb[(int64_t)rb * DK + d] : 0.f;
     }
     const int lim_a = ra < iend ? ra : -1;        // last key index row a may see
     const int lim_b = rb < iend ? rb : -1;
@@ -178,7 +218,7 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     const int warp_last = min(i0 + warp * 16 + 15, iend - 1);
 
     for (int kt = 0; kt < nkt; ++kt) {
-        if (kt + 1 < nkt) load_tile(sm, (kt + 1) & 1, kb, vb, cC + (kt + 1) * TK, cend, dK);
+        if (kt + 1 < nkt) load_tile(sm, (kt + 1) & 1, kb, vb, cC + (kt + 1) * TK, cend, DK);
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
@@ -195,8 +235,8 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     const int kl = kk0 + (h & 1) + (h >> 1) * 8;
                     const float4 kv = Ks[kl];
                     const int key = key0 + kl;
-                    const float wa = key <= lim_a ? cauchy_w(dist2_4(qa, kv), inv_g2) : 0.f;
-                    const float wb = key <= lim_b ? cauchy_w(dist2_4(qbv, kv), inv_g2) : 0.f;
+                    const float wa = key <= lim_a ? cauchy_w_fast(dist2k<DK>(qa, kv), inv_g2) : 0.f;
+                    const float wb = key <= lim_b ? cauchy_w_fast(dist2k<DK>(qbv, kv), inv_g2) : 0.f;
                     wv[h] = wa;
                     wv[4 + h] = wb;
                     sa += wa;
@@ -263,10 +303,19 @@ cudaError_t launch_attend_fwd_tc(const Prob &p, const float *q, const float *k, 
                                  const float *gamma, const int32_t *idx, void *out,
                                  float *rowsum, int32_t *status, cudaStream_t st) {
     const int tpc = (p.C + TQ - 1) / TQ;
-    const int64_t gx = p.n * tpc;
-    attend_fwd_tc<<<dim3((unsigned)gx, (unsigned)p.S), THREADS, 0, st>>>(
-        q, k, static_cast<const __nv_bfloat16 *>(v), gamma, idx,
-        static_cast<__nv_bfloat16 *>(out), rowsum, status, p.N, p.H, p.dK, p.k, p.C, tpc);
+    const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
+    const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(v);
+    __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(out);
+#define ZETA_FWD_TC(D)                                                                        \
+    attend_fwd_tc<D><<<grid, THREADS, 0, st>>>(q, k, vb, gamma, idx, ob, rowsum, status, p.N, \
+                                               p.H, p.k, p.C, tpc)
+    switch (p.dK) {
+        case 1: ZETA_FWD_TC(1); break;
+        case 2: ZETA_FWD_TC(2); break;
+        case 3: ZETA_FWD_TC(3); break;
+        default: ZETA_FWD_TC(4); break;
+    }
+#undef ZETA_FWD_TC
     return cudaGetLastError();
 }
 
