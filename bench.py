@@ -203,7 +203,7 @@ def launches_per_step(w, fwd_only=False) -> int:
         return fwd
     key_bits = max(1, int(np.ceil(np.log2(max(w.N, 2)))))
     idx_passes = max(1, -(-key_bits // 8))
-    bwd = 1 + 3 * idx_passes + 1 + 1 + 1
+    bwd = 1 + 3 * idx_passes + 1 + 1 + 2
     return fwd + bwd
 
 
@@ -217,10 +217,10 @@ def run_ours(args, w, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
-    wr = w.replace(seed=w.seed + 1000 * rank)
+    wr = w.replace(seed=w.seed + 1000 * rank)          # every rank its own batch
     g = W.generate(wr, with_dout=True)
     p = zb.problem_of(wr)
+    warm = max(3, args.warmup)
 
     def to_dev(a, vals=False):
         t = torch.from_numpy(np.ascontiguousarray(a)).reshape(-1)
@@ -234,53 +234,53 @@ def run_ours(args, w, rank, world):
     plan = ZetaPlan(p, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def step():
-        plan.forward(q, k, v, gamma)
-        plan.backward(q, k, v, gamma, dout)
-        if world > 1:
-            dist.all_reduce(plan.dgamma)
-
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # --- the step as one CUDA graph: encode x2, sort, select, attend fwd, attend bwd
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warm):
+            plan.forward(q, k, v, gamma)
+            plan.backward(q, k, v, gamma, dout)
+    torch.cuda.current_stream().wait_stream(side)
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph):
+        plan.forward(q, k, v, gamma)
+        plan.backward(q, k, v, gamma, dout)
+    fwd_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(fwd_graph):
+        plan.forward(q, k, v, gamma)
+    for _ in range(warm):
+        step_graph.replay()
+        if world > 1:
+            dist.all_reduce(plan.dgamma)
         flush.zero_()
     barrier()
     if int(plan.status.item()) != 0:
         raise RuntimeError(f"device status {plan.status.item()}")
 
-    # --- timed: K steps, events around every library call, L2 flushed between steps
-    calls = ["encode", "sort", "select", "attend_fwd", "attend_bwd"]
-    per_call = {c: 0.0 for c in calls}
+    # --- timed: K graph replays, each bracketed by events; L2 flushed between steps
     step_ms = []
     with ClockSampler(physical_gpu_index(dev.index or 0)) as clk:
         barrier()
         t_wall = time.perf_counter()
         for _ in range(args.steps):
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-            ev[0].record(stream)
-            zb.zeta_encode(p, q, plan.q_codes)
-            zb.zeta_encode(p, k, plan.k_codes)
-            ev[1].record(stream)
-            zb.zeta_sort_chunks(p, plan.k_codes, plan.prefix_codes, plan.prefix_idx, plan.sort_ws)
-            ev[2].record(stream)
-            zb.zeta_select_topk(p, plan.q_codes, plan.prefix_codes, plan.prefix_idx, plan.idx)
-            ev[3].record(stream)
-            zb.zeta_attend_fwd(p, q, k, v, gamma, plan.idx, plan.out, plan.rowsum, plan.status)
-            ev[4].record(stream)
-            zb.zeta_attend_bwd(p, q, k, v, gamma, plan.idx, dout, plan.dq, plan.dk, plan.dv,
-                               plan.dgamma, plan.bwd_ws, plan.status)
+            a, b = ev(), ev()
+            a.record()
+            step_graph.replay()
             if world > 1:
                 dist.all_reduce(plan.dgamma)
-            ev[5].record(stream)
+            b.record()
             flush.zero_()
-            torch.cuda.synchronize()
-            for c, (a, b) in zip(calls, zip(ev[:-1], ev[1:])):
-                per_call[c] += a.elapsed_time(b)
-            step_ms.append(ev[0].elapsed_time(ev[5]))
+            b.synchronize()
+            step_ms.append(a.elapsed_time(b))
         barrier()
         wall = time.perf_counter() - t_wall
     dev_ms = sum(step_ms) / len(step_ms)
@@ -291,21 +291,41 @@ def run_ours(args, w, rank, world):
     tokens = wr.B * wr.N * world
     value = tokens / (dev_ms * 1e-3)
 
-    # --- forward alone on this workload
+    # --- forward alone (graph), and a per-call breakdown of the step (direct calls)
     fwd_ms = []
-    for _ in range(max(3, args.warmup)):
-        plan.forward(q, k, v, gamma)
     for _ in range(args.steps):
         flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        plan.forward(q, k, v, gamma)
-        b.record(stream)
-        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record()
+        fwd_graph.replay()
+        b.record()
+        b.synchronize()
         fwd_ms.append(a.elapsed_time(b))
     fwd_train_ms = sum(fwd_ms) / len(fwd_ms)
+    calls = ["encode", "sort", "select", "attend_fwd", "attend_bwd"]
+    per_call = {c: 0.0 for c in calls}
+    for _ in range(args.steps):
+        flush.zero_()
+        e = [ev() for _ in range(6)]
+        e[0].record()
+        zb.zeta_encode(p, q, plan.q_codes)
+        zb.zeta_encode(p, k, plan.k_codes)
+        e[1].record()
+        zb.zeta_sort_chunks(p, plan.k_codes, plan.prefix_codes, plan.prefix_idx, plan.sort_ws)
+        e[2].record()
+        zb.zeta_select_topk(p, plan.q_codes, plan.prefix_codes, plan.prefix_idx, plan.idx)
+        e[3].record()
+        zb.zeta_attend_fwd(p, q, k, v, gamma, plan.idx, plan.out, plan.rowsum, plan.status)
+        e[4].record()
+        zb.zeta_attend_bwd(p, q, k, v, gamma, plan.idx, dout, plan.dq, plan.dk, plan.dv,
+                           plan.dgamma, plan.bwd_ws, plan.status)
+        e[5].record()
+        e[5].synchronize()
+        for c, (x, y) in zip(calls, zip(e[:-1], e[1:])):
+            per_call[c] += x.elapsed_time(y) / args.steps
 
-    # --- end to end through the C ABI with host buffers (pinned)
+    # --- end to end through the C ABI with host buffers (pinned): H2D of the
+    # step's inputs, the five calls, D2H of its results
     out_h = torch.empty(plan.out.numel(), dtype=plan.out.dtype).pin_memory()
     dq_h = torch.empty(plan.dq.numel(), dtype=torch.float32).pin_memory()
     dk_h = torch.empty(plan.dk.numel(), dtype=torch.float32).pin_memory()
@@ -314,10 +334,10 @@ def run_ours(args, w, rank, world):
     h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h, g_h, do_h))
     d2h = sum(x.numel() * x.element_size() for x in (out_h, dq_h, dk_h, dv_h, dg_h))
     e2e_ms = []
-    for it in range(max(3, args.warmup) + args.steps):
+    for it in range(warm + args.steps):
         flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        a, b = ev(), ev()
+        a.record()
         for src, dst in ((q_h, q), (k_h, k), (v_h, v), (g_h, gamma), (do_h, dout)):
             dst.copy_(src, non_blocking=True)
         plan.forward(q, k, v, gamma)
@@ -327,40 +347,39 @@ def run_ours(args, w, rank, world):
         for src, dst in ((plan.out, out_h), (plan.dq, dq_h), (plan.dk, dk_h), (plan.dv, dv_h),
                          (plan.dgamma, dg_h)):
             dst.copy_(src, non_blocking=True)
-        b.record(stream)
-        torch.cuda.synchronize()
-        if it >= max(3, args.warmup):
+        b.record()
+        b.synchronize()
+        if it >= warm:
             e2e_ms.append(a.elapsed_time(b))
     e2e = tokens / (sum(e2e_ms) / len(e2e_ms) * 1e-3)
 
     # --- efficiency workload: forward alone, and the attend-forward kernel roofline
-    from order_retrieval_gb300 import workloads as W2
-    we = W2.EFFICIENCY.replace(seed=W2.EFFICIENCY.seed + 1000 * rank)
-    ge = W2.generate(we)
+    we = W.EFFICIENCY.replace(seed=W.EFFICIENCY.seed + 1000 * rank)
+    ge = W.generate(we)
     pe = zb.problem_of(we)
     qe, ke = to_dev(ge["q"])[1], to_dev(ge["k"])[1]
     ve, gme = to_dev(ge["v"], True)[1], to_dev(ge["gamma"])[1]
     plan_e = ZetaPlan(pe, dev, backward=False)
-    for _ in range(max(3, args.warmup)):
+    for _ in range(warm):
         plan_e.forward(qe, ke, ve, gme)
     fwd_e, att_e = [], []
     for _ in range(args.steps):
         flush.zero_()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        ev[0].record(stream)
+        e = [ev() for _ in range(3)]
+        e[0].record()
         zb.zeta_encode(pe, qe, plan_e.q_codes)
         zb.zeta_encode(pe, ke, plan_e.k_codes)
         zb.zeta_sort_chunks(pe, plan_e.k_codes, plan_e.prefix_codes, plan_e.prefix_idx,
                             plan_e.sort_ws)
         zb.zeta_select_topk(pe, plan_e.q_codes, plan_e.prefix_codes, plan_e.prefix_idx,
                             plan_e.idx)
-        ev[1].record(stream)
+        e[1].record()
         zb.zeta_attend_fwd(pe, qe, ke, ve, gme, plan_e.idx, plan_e.out, plan_e.rowsum,
                            plan_e.status)
-        ev[2].record(stream)
-        torch.cuda.synchronize()
-        fwd_e.append(ev[0].elapsed_time(ev[2]))
-        att_e.append(ev[1].elapsed_time(ev[2]))
+        e[2].record()
+        e[2].synchronize()
+        fwd_e.append(e[0].elapsed_time(e[2]))
+        att_e.append(e[1].elapsed_time(e[2]))
     fwd_e_ms = sum(fwd_e) / len(fwd_e)
     att_e_ms = sum(att_e) / len(att_e)
 
@@ -374,8 +393,8 @@ def run_ours(args, w, rank, world):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     fb = fwd_attend_bytes(we)
     achieved = fb / (att_e_ms * 1e-3) / 1e9
+    fbt = fwd_attend_bytes(wr)
     bb = bwd_attend_bytes(wr)
-    bwd_gbs = bb / (per_call["attend_bwd"] / args.steps * 1e-3) / 1e9
 
     # CPU baseline: the oracle on a bounded sample of this workload
     import oracle
@@ -387,24 +406,31 @@ def run_ours(args, w, rank, world):
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": dev_ms,
+        "steps": args.steps, "warmup": warm, "ms_per_step": dev_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "dtype_detail": "v, dO, out, dv bf16; q, k, weights and accumulation f32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d_K": w.d_K,
                    "d_V": w.d_V, "k": w.k, "C": w.C, "bits": w.bits,
                    "l2": "flushed between steps (256 MiB write); inputs larger than L2",
+                   "step": "one CUDA graph: encode q,k; sort; select; attend fwd; attend bwd",
                    "parallelism": f"dp{world} (independent batches per GPU)"},
         "fwd_tokens_per_s": tokens / (fwd_train_ms * 1e-3),
         "fwd_efficiency": {"workload": we.name, "tokens_per_s": we.B * we.N * world /
                            (fwd_e_ms * 1e-3), "ms": fwd_e_ms, "attend_fwd_ms": att_e_ms},
-        "per_call_ms": {c: per_call[c] / args.steps for c in calls},
-        "roofline": {"kernel": "attend_fwd (efficiency workload)", "bound": "hbm",
+        "per_call_ms": per_call,
+        "roofline": {"kernel": "attend_fwd_tc (efficiency workload, L2 flushed)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": None,
                      "algorithmic_bytes": fb, "peak_source": peak_src},
-        "roofline_bwd": {"call": "attend_bwd (training workload)", "achieved": bwd_gbs,
-                         "unit": "GB/s", "frac": bwd_gbs / hbm_peak, "algorithmic_bytes": bb},
+        "roofline_train": {
+            "attend_fwd": {"achieved": fbt / (per_call["attend_fwd"] * 1e-3) / 1e9,
+                           "frac": fbt / (per_call["attend_fwd"] * 1e-3) / 1e9 / hbm_peak,
+                           "algorithmic_bytes": fbt},
+            "attend_bwd": {"achieved": bb / (per_call["attend_bwd"] * 1e-3) / 1e9,
+                           "frac": bb / (per_call["attend_bwd"] * 1e-3) / 1e9 / hbm_peak,
+                           "algorithmic_bytes": bb},
+            "unit": "GB/s"},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step(w) * args.steps,
@@ -421,7 +447,7 @@ def run_ours(args, w, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     args = ap.parse_args()

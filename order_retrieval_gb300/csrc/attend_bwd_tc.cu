@@ -22,6 +22,8 @@
 //   own chunk    - S^T = V . dO^T on tensor cores, the element-wise terms, then
 //                  dV += P^T . dO with P^T re-packed from the accumulator
 //                  fragments (their layout is the A-fragment layout).
+#include <type_traits>
+
 #include "mma.cuh"
 
 namespace zeta {
@@ -132,6 +134,31 @@ struct QAcc {
     }
 };
 
+// The same twelve sums for two rows (a, b) at once, packed f32x2; a weight of
+// 0 (masked pair) contributes nothing.
+struct QAcc2 {
+    float2 x[12];
+    __device__ void zero() {
+#pragma unroll
+        for (int y = 0; y < 12; ++y) x[y] = make_float2(0.f, 0.f);
+    }
+    template <int DK>
+    __device__ void add(float2 w, float2 g, const float2 (&dq)[4], float2 m2ig2, float2 two_ig) {
+        const float2 c = mul2(mul2(w, w), m2ig2);                 // -2 w^2 / gamma^2
+        const float2 e = mul2(mul2(w, sub2(dup2(1.f), w)), two_ig); // 2 w (1 - w) / gamma
+        x[0] = add2(x[0], w);
+        x[1] = fma2(w, g, x[1]);
+        x[2] = fma2(g, e, x[2]);
+        x[3] = add2(x[3], e);
+#pragma unroll
+        for (int d = 0; d < DK; ++d) {
+            const float2 t = mul2(c, dq[d]);
+            x[4 + d] = fma2(g, t, x[4 + d]);
+            x[8 + d] = add2(x[8 + d], t);
+        }
+    }
+};
+
 template <int DK>
 __global__ void __launch_bounds__(THREADS, 4)
 bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
@@ -195,8 +222,13 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
             float qi[4];
 #pragma unroll
             for (int d = 0; d < 4; ++d) qi[d] = d < DK ? qb[(int64_t)i * DK + d] : 0.f;
-            float do8[8];
-            unpack8(*reinterpret_cast<const uint4 *>(db + (int64_t)i * DV + sub * 8), do8);
+            float2 do2[4];
+            {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(db + (int64_t)i * DV + sub * 8);
+                const uint32_t uw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) do2[e] = bf2_to_f2(uw[e]);
+            }
             for (int t0 = 0; t0 < k; t0 += 64) {
                 int j[2] = {jn[0], jn[1]};
                 if (t0 + 64 < k) load_idx(i, t0 + 64, jn);
@@ -223,15 +255,11 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     if (u < nu) {
-                        float v8[8];
-                        unpack8(buf[u], v8);
-                        float g0 = 0.f, g1 = 0.f;
+                        const uint32_t uw[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+                        float2 gg = mul2(do2[0], bf2_to_f2(uw[0]));
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            g0 = __fmaf_rn(do8[e], v8[e], g0);
-                            g1 = __fmaf_rn(do8[e + 1], v8[e + 1], g1);
-                        }
-                        const float g = warp_group8_sum(g0 + g1);
+                        for (int e = 1; e < 4; ++e) gg = fma2(do2[e], bf2_to_f2(uw[e]), gg);
+                        const float g = warp_group8_sum(gg.x + gg.y);
                         const float gx = __shfl_sync(kFull, g, (lane & 3) * 8);
                         if ((u & 7) == (lane >> 2)) gown[u >> 3] = gx;
                     }
@@ -260,11 +288,56 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
         qbv[d] = (rb < iend && d < DK) ? qb[(int64_t)rb * DK + d] : 0.f;
     }
     const int lim_a = ra < iend ? ra : -1, lim_b = rb < iend ? rb : -1;
-    const int warp_last = min(i0 + warp * 16 + 15, iend - 1);
-    QAcc la, lb;
-    la.zero();
-    lb.zero();
+    const int warp_first = i0 + warp * 16;
+    const int warp_last = min(warp_first + 15, iend - 1);
+    const bool warp_rows_full = warp_first + 15 < iend;
+    float2 qab[4];
+#pragma unroll
+    for (int d = 0; d < 4; ++d) qab[d] = make_float2(qa[d], qbv[d]);
+    const float2 ig2 = dup2(inv_g2), m2ig2 = dup2(-2.f * inv_g2), two_ig = dup2(2.f * inv_g);
+    QAcc2 lab;
+    lab.zero();
     uint32_t afr[4][4];
+    auto tile = [&](const float4 *Ks, uint32_t vbase, int key0, auto masked) {
+        float s[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+        const int m = lane >> 3, rr = lane & 7;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                const int key = np * 16 + (m >> 1) * 8 + rr;
+                uint32_t b[4];
+                ldsm_x4(b, vbase + (uint32_t)swz(key, ks * 2 + (m & 1)) * 2u);
+                mma16816(s[2 * np], afr[ks], b[0], b[1]);
+                mma16816(s[2 * np + 1], afr[ks], b[2], b[3]);
+            }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int kl = nt * 8 + 2 * tig + e;
+                const float4 kv = Ks[kl];
+                const float kc[4] = {kv.x, kv.y, kv.z, kv.w};
+                float2 dq[4];
+                float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int d = 0; d < DK; ++d) {
+                    dq[d] = sub2(qab[d], dup2(kc[d]));
+                    d2 = fma2(dq[d], dq[d], d2);
+                }
+                float2 w = cauchy_w2(d2, ig2);
+                if (decltype(masked)::value) {
+                    const int key = key0 + kl;
+                    w.x = key <= lim_a ? w.x : 0.f;
+                    w.y = key <= lim_b ? w.y : 0.f;
+                }
+                lab.add<DK>(w, make_float2(s[nt][e], s[nt][2 + e]), dq, m2ig2, two_ig);
+            }
+    };
     for (int kt = 0; kt < nkt; ++kt) {
         if (kt + 1 < nkt) load_ktile((kt + 1) & 1, cC + (kt + 1) * T64);
         cp_async_commit();
@@ -281,39 +354,20 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
         }
         const int key0 = cC + kt * T64;
         if (key0 <= warp_last) {
-            float s[8][4];
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
-            const uint32_t vbase = smem_u32(sm.v[kt & 1]);
-            const int m = lane >> 3, rr = lane & 7;
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    const int key = np * 16 + (m >> 1) * 8 + rr;
-                    uint32_t b[4];
-                    ldsm_x4(b, vbase + (uint32_t)swz(key, ks * 2 + (m & 1)) * 2u);
-                    mma16816(s[2 * np], afr[ks], b[0], b[1]);
-                    mma16816(s[2 * np + 1], afr[ks], b[2], b[3]);
-                }
             const float4 *Ks = sm.kt[kt & 1];
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int kl = nt * 8 + 2 * tig + e;
-                    const int key = key0 + kl;
-                    const float4 kv = Ks[kl];
-                    if (key <= lim_a)
-                        la.add(cauchy_w_fast(dist2k<DK>(qa, kv), inv_g2), s[nt][e], qa, kv, inv_g2, inv_g);
-                    if (key <= lim_b)
-                        lb.add(cauchy_w_fast(dist2k<DK>(qbv, kv), inv_g2), s[nt][2 + e], qbv, kv, inv_g2,
-                               inv_g);
-                }
+            const uint32_t vbase = smem_u32(sm.v[kt & 1]);
+            if (warp_rows_full && key0 + T64 - 1 <= warp_first)
+                tile(Ks, vbase, key0, std::false_type{});
+            else
+                tile(Ks, vbase, key0, std::true_type{});
         }
         __syncthreads();
+    }
+    QAcc la, lb;
+#pragma unroll
+    for (int y = 0; y < 12; ++y) {
+        la.x[y] = lab.x[y].x;
+        lb.x[y] = lab.x[y].y;
     }
 
     // ------------------------------------------------------- epilogue ---
@@ -399,13 +453,18 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     for (int r = 0; r < 16; ++r) {
         const int row = warp * 16 + r;
         const int j = j0 + row;
-        float acc[8];
+        float2 acc[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
         float dka[4] = {0.f, 0.f, 0.f, 0.f};
         if (j < jend) {
-            float v8[8];
-            unpack8(*reinterpret_cast<const uint4 *>(vb + (int64_t)j * DV + sub * 8), v8);
+            float2 v2[4];
+            {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(vb + (int64_t)j * DV + sub * 8);
+                const uint32_t uw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v2[e] = bf2_to_f2(uw[e]);
+            }
             const float4 kj = load_k4(kb + (int64_t)j * DK, DK);
             // Sixteen listed queries per step (four per lane group), their list
             // positions fetched one step ahead.
@@ -436,17 +495,17 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const bool ok = ic[h] != 0xffffffffu;
-                    float d8[8];
-                    float g0 = 0.f, g1 = 0.f;
+                    float2 d2v[4];
+                    float2 gg = make_float2(0.f, 0.f);
                     if (ok) {
-                        unpack8(dbuf[h], d8);
+                        const uint32_t uw[4] = {dbuf[h].x, dbuf[h].y, dbuf[h].z, dbuf[h].w};
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            g0 = __fmaf_rn(d8[e], v8[e], g0);
-                            g1 = __fmaf_rn(d8[e + 1], v8[e + 1], g1);
+                        for (int e = 0; e < 4; ++e) {
+                            d2v[e] = bf2_to_f2(uw[e]);
+                            gg = fma2(d2v[e], v2[e], gg);
                         }
                     }
-                    const float g = warp_group8_sum(g0 + g1);
+                    const float g = warp_group8_sum(gg.x + gg.y);
                     if (ok) {
                         const float4 qi = qrec[h].q;
                         const float qv[4] = {qi.x, qi.y, qi.z, qi.w};
@@ -455,8 +514,9 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                         const float a = w * inv_s;
                         const float dldw = (g - qrec[h].sg.y) * inv_s;
                         const float coef = dldw * (2.f * w * w * inv_g2);
+                        const float2 a2 = dup2(a);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = __fmaf_rn(a, d8[e], acc[e]);
+                        for (int e = 0; e < 4; ++e) acc[e] = fma2(a2, d2v[e], acc[e]);
                         dka[0] = __fmaf_rn(coef, qi.x - kj.x, dka[0]);
                         dka[1] = __fmaf_rn(coef, qi.y - kj.y, dka[1]);
                         dka[2] = __fmaf_rn(coef, qi.z - kj.z, dka[2]);
@@ -465,9 +525,11 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                acc[e] += __shfl_xor_sync(kFull, acc[e], 8);
-                acc[e] += __shfl_xor_sync(kFull, acc[e], 16);
+            for (int e = 0; e < 4; ++e) {
+                acc[e].x += __shfl_xor_sync(kFull, acc[e].x, 8);
+                acc[e].y += __shfl_xor_sync(kFull, acc[e].y, 8);
+                acc[e].x += __shfl_xor_sync(kFull, acc[e].x, 16);
+                acc[e].y += __shfl_xor_sync(kFull, acc[e].y, 16);
             }
 #pragma unroll
             for (int d = 0; d < 4; ++d) {
@@ -477,8 +539,8 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
         }
         if (lane < 8) {
             float4 *dst = reinterpret_cast<float4 *>(&sm.dvp[row][lane * 8]);
-            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            dst[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+            dst[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
         }
         if (lane == 0) *reinterpret_cast<float4 *>(sm.dkp[row]) =
             make_float4(dka[0], dka[1], dka[2], dka[3]);
@@ -489,24 +551,29 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     const int ka = j0 + warp * 16 + g8, kbi = ka + 8;      // this thread's two key rows
     const float4 kva = ka < jend ? load_k4(kb + (int64_t)ka * DK, DK) : make_float4(0, 0, 0, 0);
     const float4 kvb = kbi < jend ? load_k4(kb + (int64_t)kbi * DK, DK) : make_float4(0, 0, 0, 0);
-    const float kra[4] = {kva.x, kva.y, kva.z, kva.w};
-    const float krb[4] = {kvb.x, kvb.y, kvb.z, kvb.w};
+    float2 kab[4];                                        // (row a, row b) coordinates
+    kab[0] = make_float2(kva.x, kvb.x);
+    kab[1] = make_float2(kva.y, kvb.y);
+    kab[2] = make_float2(kva.z, kvb.z);
+    kab[3] = make_float2(kva.w, kvb.w);
     const int first_a = ka < jend ? ka : 0x7fffffff;     // first query index row a may see
     const int first_b = kbi < jend ? kbi : 0x7fffffff;
+    const float2 ig2 = dup2(inv_g2), two_ig2 = dup2(2.f * inv_g2);
     float dva[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dva[nt][e] = 0.f;
-    float dkl_a[4] = {0.f, 0.f, 0.f, 0.f}, dkl_b[4] = {0.f, 0.f, 0.f, 0.f};
+    float2 dkab[4];
+#pragma unroll
+    for (int d = 0; d < 4; ++d) dkab[d] = make_float2(0.f, 0.f);
     const int nqt = tiles_per_chunk - kt;
     const int m = lane >> 3, rr = lane & 7;
-    for (int t = 0; t < nqt; ++t) {
-        const int iq0 = j0 + t * T64;
-        if (t + 1 < nqt) load_qtile((t + 1) & 1, iq0 + T64);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
+    // every key row of this warp sees every query of a query tile starting at
+    // or after its last key (within the chunk): no mask needed there
+    const int warp_key_last = j0 + warp * 16 + 15;
+    const bool warp_keys_full = warp_key_last < jend;
+    auto qtile = [&](int t, int iq0, auto masked) {
         const uint32_t vbase = smem_u32(sm.v);
         const uint32_t dbase = smem_u32(sm.dO[t & 1]);
         // S^T = V . dO^T : 16 keys x 64 queries per warp
@@ -528,7 +595,8 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 mma16816(s[2 * np + 1], a, b[2], b[3]);
             }
         }
-        // element-wise terms; P^T packed into A fragments, then dV += P^T . dO
+        // element-wise terms for key rows (a, b) packed; P^T into A fragments,
+        // then dV += P^T . dO
         const QRec *qt_rec = sm.qr[t & 1];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -539,29 +607,29 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int ql = nt * 8 + 2 * tig + e;
-                    const int i = iq0 + ql;
                     const QRec qrc = qt_rec[ql];
-                    const float qv[4] = {qrc.q.x, qrc.q.y, qrc.q.z, qrc.q.w};
-                    const float inv_s = qrc.sg.x, gb = qrc.sg.y;
-                    float aa = 0.f, ab = 0.f;
-                    if (i >= first_a && i < cend) {
-                        const float w = cauchy_w_fast(dist2k<DK>(qv, kva), inv_g2);
-                        aa = w * inv_s;
-                        const float coef = (s[nt][e] - gb) * inv_s * (2.f * w * w * inv_g2);
+                    const float qc[4] = {qrc.q.x, qrc.q.y, qrc.q.z, qrc.q.w};
+                    const float2 inv_s = dup2(qrc.sg.x), gb = dup2(qrc.sg.y);
+                    float2 dqk[4];
+                    float2 d2 = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int d = 0; d < 4; ++d)
-                            dkl_a[d] = __fmaf_rn(coef, qv[d] - kra[d], dkl_a[d]);
+                    for (int d = 0; d < DK; ++d) {
+                        dqk[d] = sub2(dup2(qc[d]), kab[d]);
+                        d2 = fma2(dqk[d], dqk[d], d2);
                     }
-                    if (i >= first_b && i < cend) {
-                        const float w = cauchy_w_fast(dist2k<DK>(qv, kvb), inv_g2);
-                        ab = w * inv_s;
-                        const float coef = (s[nt][2 + e] - gb) * inv_s * (2.f * w * w * inv_g2);
+                    float2 w = cauchy_w2(d2, ig2);
+                    if (decltype(masked)::value) {
+                        const int i = iq0 + ql;
+                        w.x = (i >= first_a && i < cend) ? w.x : 0.f;
+                        w.y = (i >= first_b && i < cend) ? w.y : 0.f;
+                    }
+                    const float2 aw = mul2(w, inv_s);
+                    const float2 dldw = mul2(sub2(make_float2(s[nt][e], s[nt][2 + e]), gb), inv_s);
+                    const float2 coef = mul2(dldw, mul2(mul2(w, w), two_ig2));
 #pragma unroll
-                        for (int d = 0; d < 4; ++d)
-                            dkl_b[d] = __fmaf_rn(coef, qv[d] - krb[d], dkl_b[d]);
-                    }
-                    pa_[hh * 4 + e] = aa;
-                    pa_[hh * 4 + 2 + e] = ab;
+                    for (int d = 0; d < DK; ++d) dkab[d] = fma2(coef, dqk[d], dkab[d]);
+                    pa_[hh * 4 + e] = aw.x;
+                    pa_[hh * 4 + 2 + e] = aw.y;
                 }
             }
             uint32_t pa[4];
@@ -578,7 +646,24 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 mma16816(dva[2 * np + 1], pa, b[2], b[3]);
             }
         }
+    };
+    for (int t = 0; t < nqt; ++t) {
+        const int iq0 = j0 + t * T64;
+        if (t + 1 < nqt) load_qtile((t + 1) & 1, iq0 + T64);
+        cp_async_commit();
+        cp_async_wait<1>();
         __syncthreads();
+        if (warp_keys_full && iq0 >= warp_key_last && iq0 + T64 <= cend)
+            qtile(t, iq0, std::false_type{});
+        else
+            qtile(t, iq0, std::true_type{});
+        __syncthreads();
+    }
+    float dkl_a[4], dkl_b[4];
+#pragma unroll
+    for (int d = 0; d < 4; ++d) {
+        dkl_a[d] = dkab[d].x;
+        dkl_b[d] = dkab[d].y;
     }
 
     // ------------------------------------------------------- epilogue ---

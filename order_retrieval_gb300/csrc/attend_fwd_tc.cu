@@ -20,6 +20,8 @@
 //    and mma.sync m16n8k16 accumulates in float32 registers.  Row sums of P are
 //    kept in float32 from the unrounded weights.
 //  * The two partial sums simply add (weights are in (0, 1], no rescaling).
+#include <type_traits>
+
 #include "mma.cuh"
 
 namespace zeta {
@@ -50,13 +52,12 @@ __device__ __forceinline__ float dist2k(const float (&a)[4], float4 b) {
     return d;
 }
 
-__device__ __forceinline__ void bf16x8_fma(float (&acc)[8], uint4 raw, float w) {
+// acc[e] += w * row chunk (8 bf16), four packed f32x2 FMAs.
+__device__ __forceinline__ void bf16x8_fma(float2 (&acc)[4], uint4 raw, float w) {
     const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+    const float2 ww = dup2(w);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        acc[2 * e] = __fmaf_rn(w, __uint_as_float(u[e] << 16), acc[2 * e]);
-        acc[2 * e + 1] = __fmaf_rn(w, __uint_as_float(u[e] & 0xffff0000u), acc[2 * e + 1]);
-    }
+    for (int e = 0; e < 4; ++e) acc[e] = fma2(ww, bf2_to_f2(u[e]), acc[e]);
 }
 
 // Stage own-chunk key tile `kt` (keys cC + kt*TK ...) into buffer b.
@@ -133,9 +134,9 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     if (nqw > 0) load_idx(wq0, 0, jn);
     for (int r = 0; r < 16; ++r) {
         const int row = warp * 16 + r;
-        float acc[8];
+        float2 acc[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
         float sw = 0.f;
         if (r < nqw) {
             const int i = wq0 + r;
@@ -183,17 +184,19 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                acc[e] += __shfl_xor_sync(kFull, acc[e], 8);
-                acc[e] += __shfl_xor_sync(kFull, acc[e], 16);
+            for (int e = 0; e < 4; ++e) {
+                acc[e].x += __shfl_xor_sync(kFull, acc[e].x, 8);
+                acc[e].y += __shfl_xor_sync(kFull, acc[e].y, 8);
+                acc[e].x += __shfl_xor_sync(kFull, acc[e].x, 16);
+                acc[e].y += __shfl_xor_sync(kFull, acc[e].y, 16);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(kFull, sw, o);
         }
         if (lane < 8) {
             float4 *dst = reinterpret_cast<float4 *>(&sm.win[row][lane * 8]);
-            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            dst[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+            dst[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
         }
         if (lane == 0) sm.swin[row] = sw;
     }
@@ -209,13 +212,63 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     }
     const int lim_a = ra < iend ? ra : -1;        // last key index row a may see
     const int lim_b = rb < iend ? rb : -1;
+    float2 qab[4];                                // (row a, row b) coordinates
+#pragma unroll
+    for (int d = 0; d < 4; ++d) qab[d] = make_float2(qa[d], qbv[d]);
+    const float2 ig2 = dup2(inv_g2);
     float acc[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-    float sa = 0.f, sb = 0.f;
-    const int warp_last = min(i0 + warp * 16 + 15, iend - 1);
+    float2 sab = make_float2(0.f, 0.f);           // row sums of rows a, b
+    const int warp_first = i0 + warp * 16;
+    const int warp_last = min(warp_first + 15, iend - 1);
+    const bool warp_rows_full = warp_first + 15 < iend;
+
+    // One 64-key tile: weights of rows (a, b) against 16 keys per k-step, packed.
+    auto tile = [&](const float4 *Ks, uint32_t vbase, int key0, auto masked) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const int kk0 = ks * 16 + 2 * tig;
+            float wv[8];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {              // keys kk0, kk0+1, kk0+8, kk0+9
+                const int kl = kk0 + (h & 1) + (h >> 1) * 8;
+                const float4 kv = Ks[kl];
+                const float kc[4] = {kv.x, kv.y, kv.z, kv.w};
+                float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int d = 0; d < DK; ++d) {
+                    const float2 e = sub2(qab[d], dup2(kc[d]));
+                    d2 = fma2(e, e, d2);
+                }
+                float2 w = cauchy_w2(d2, ig2);
+                if (decltype(masked)::value) {
+                    const int key = key0 + kl;
+                    w.x = key <= lim_a ? w.x : 0.f;
+                    w.y = key <= lim_b ? w.y : 0.f;
+                }
+                wv[h] = w.x;
+                wv[4 + h] = w.y;
+                sab = add2(sab, w);
+            }
+            uint32_t a[4];
+            a[0] = pack_bf16(wv[0], wv[1]);
+            a[1] = pack_bf16(wv[4], wv[5]);
+            a[2] = pack_bf16(wv[2], wv[3]);
+            a[3] = pack_bf16(wv[6], wv[7]);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                const int m = lane >> 3, rr = lane & 7;
+                const int key = ks * 16 + (m & 1) * 8 + rr;
+                uint32_t b[4];
+                ldsm_x4_trans(b, vbase + (uint32_t)swz(key, np * 2 + (m >> 1)) * 2u);
+                mma16816(acc[2 * np], a, b[0], b[1]);
+                mma16816(acc[2 * np + 1], a, b[2], b[3]);
+            }
+        }
+    };
 
     for (int kt = 0; kt < nkt; ++kt) {
         if (kt + 1 < nkt) load_tile(sm, (kt + 1) & 1, kb, vb, cC + (kt + 1) * TK, cend, DK);
@@ -226,41 +279,14 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
         if (key0 <= warp_last) {                   // else every weight of this warp is 0
             const float4 *Ks = sm.kt[kt & 1];
             const uint32_t vbase = smem_u32(sm.v[kt & 1]);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const int kk0 = ks * 16 + 2 * tig;
-                float wv[8];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {      // keys kk0, kk0+1, kk0+8, kk0+9
-                    const int kl = kk0 + (h & 1) + (h >> 1) * 8;
-                    const float4 kv = Ks[kl];
-                    const int key = key0 + kl;
-                    const float wa = key <= lim_a ? cauchy_w_fast(dist2k<DK>(qa, kv), inv_g2) : 0.f;
-                    const float wb = key <= lim_b ? cauchy_w_fast(dist2k<DK>(qbv, kv), inv_g2) : 0.f;
-                    wv[h] = wa;
-                    wv[4 + h] = wb;
-                    sa += wa;
-                    sb += wb;
-                }
-                uint32_t a[4];
-                a[0] = pack_bf16(wv[0], wv[1]);
-                a[1] = pack_bf16(wv[4], wv[5]);
-                a[2] = pack_bf16(wv[2], wv[3]);
-                a[3] = pack_bf16(wv[6], wv[7]);
-#pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    const int m = lane >> 3, rr = lane & 7;
-                    const int key = ks * 16 + (m & 1) * 8 + rr;
-                    const int ch = np * 2 + (m >> 1);
-                    uint32_t b[4];
-                    ldsm_x4_trans(b, vbase + (uint32_t)(key * DV + ((ch ^ (key & 7)) * 8)) * 2u);
-                    mma16816(acc[2 * np], a, b[0], b[1]);
-                    mma16816(acc[2 * np + 1], a, b[2], b[3]);
-                }
-            }
+            if (warp_rows_full && key0 + TK - 1 <= warp_first)
+                tile(Ks, vbase, key0, std::false_type{});
+            else
+                tile(Ks, vbase, key0, std::true_type{});
         }
         __syncthreads();
     }
+    float sa = sab.x, sb = sab.y;
 
     // --------------------------------------------------------- epilogue ---
     sa += __shfl_xor_sync(kFull, sa, 1);

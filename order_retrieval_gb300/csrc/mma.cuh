@@ -150,3 +150,55 @@ __device__ __forceinline__ float cauchy_w_fast(float d2, float inv_g2) {
 }
 
 }  // namespace zeta
+
+namespace zeta {
+
+// ------------------------------------------- packed float32x2 arithmetic ---
+// Two independent float32 lanes per instruction (Blackwell f32x2 forms),
+// each rounded exactly as the scalar operation would be.
+
+__device__ __forceinline__ uint64_t f2u(float2 a) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+    return r;
+}
+__device__ __forceinline__ float2 u2f(uint64_t r) {
+    float2 a;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+    return a;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(r);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(r);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)));
+    return u2f(r);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
+    return u2f(r);
+}
+__device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
+
+// Cauchy weights of two (query, key) pairs at once: d2 holds both squared
+// distances; the reciprocals stay scalar (fast division intrinsic).
+__device__ __forceinline__ float2 cauchy_w2(float2 d2, float2 inv_g2) {
+    const float2 t = fma2(d2, inv_g2, dup2(1.0f));
+    return make_float2(__fdividef(1.0f, t.x), __fdividef(1.0f, t.y));
+}
+
+// Two bf16 (one 32-bit word) -> float2, exactly.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+}  // namespace zeta

@@ -133,13 +133,25 @@ radix_scan(uint32_t *__restrict__ hist, int64_t tiles, uint32_t *seglen) {
     }
 }
 
+// Shared memory of one downsweep tile: the tile's items staged in digit order.
+template <typename K>
+constexpr size_t downsweep_smem() {
+    return sizeof(K) * kRadixTile + sizeof(uint32_t) * kRadixTile;
+}
+
 template <typename K, typename Src>
 __global__ void __launch_bounds__(kRadixThreads)
 radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t tiles,
                 K *__restrict__ keys_out, uint32_t *__restrict__ vals_out, int64_t out_stride) {
     constexpr int W = kRadixThreads / 32;
-    __shared__ uint32_t soff[256];
+    __shared__ uint32_t soff[256];          // global start of each digit's run of this tile
+    __shared__ uint32_t tds[256];           // tile-local start of each digit
+    __shared__ uint32_t wsum[8];
+    __shared__ uint32_t s_total;            // items of this tile that are sorted
     __shared__ uint16_t wcnt[W][256];
+    extern __shared__ __align__(16) unsigned char stage_raw[];
+    K *skey = reinterpret_cast<K *>(stage_raw);
+    uint32_t *sval = reinterpret_cast<uint32_t *>(stage_raw + sizeof(K) * kRadixTile);
     const int64_t seg = blockIdx.y, tile = blockIdx.x;
     const int64_t len = src.len(seg);
     const int64_t base = tile * kRadixTile;
@@ -170,22 +182,49 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
         __syncwarp();
     }
     __syncthreads();
-    if (threadIdx.x < 256) {
+    if (threadIdx.x < 256) {                // per digit: warp offsets, then the tile total
+        const int d = threadIdx.x;
         uint32_t run = 0;
         for (int ww = 0; ww < W; ++ww) {
-            uint32_t c = wcnt[ww][threadIdx.x];
-            wcnt[ww][threadIdx.x] = (uint16_t)run;
+            const uint32_t c = wcnt[ww][d];
+            wcnt[ww][d] = (uint16_t)run;
             run += c;
         }
+        uint32_t inc = run;                 // exclusive scan of tile totals over digits
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane == 31) wsum[w] = inc;
+        tds[d] = inc - run;
+        if (d == 255) s_total = inc;        // inclusive within the last warp
     }
     __syncthreads();
+    if (threadIdx.x < 256) {
+        uint32_t carry = 0;
+        for (int ww = 0; ww < (threadIdx.x >> 5); ++ww) carry += wsum[ww];
+        tds[threadIdx.x] += carry;
+        if (threadIdx.x == 255) s_total += carry;
+    }
+    __syncthreads();
+    const uint32_t nvalid = s_total;
+    // stage the items in digit order
 #pragma unroll
     for (int r = 0; r < kRadixItems; ++r) {
         if (dig[r] < 256) {
-            const int64_t dst = (int64_t)soff[dig[r]] + wcnt[w][dig[r]] + rank[r];
-            keys_out[seg * out_stride + dst] = key[r];
-            vals_out[seg * out_stride + dst] = val[r];
+            const uint32_t tp = tds[dig[r]] + wcnt[w][dig[r]] + rank[r];
+            skey[tp] = key[r];
+            sval[tp] = val[r];
         }
+    }
+    __syncthreads();
+    // write each digit's run of the tile contiguously
+    for (uint32_t t = threadIdx.x; t < nvalid; t += kRadixThreads) {
+        const K kk = skey[t];
+        const int d = (int)((unsigned)(kk >> shift) & 255u);
+        const int64_t dst = (int64_t)soff[d] + (t - tds[d]);
+        keys_out[seg * out_stride + dst] = kk;
+        vals_out[seg * out_stride + dst] = sval[t];
     }
 }
 
@@ -196,7 +235,15 @@ cudaError_t run_pass(const Src &src, int shift, int64_t S, int64_t maxlen, Radix
     dim3 grid((unsigned)tiles, (unsigned)S);
     radix_upsweep<K, Src><<<grid, kRadixThreads, 0, st>>>(src, shift, ws.hist, tiles, status);
     radix_scan<<<(unsigned)S, 1024, 0, st>>>(ws.hist, tiles, seglen_out);
-    radix_downsweep<K, Src><<<grid, kRadixThreads, 0, st>>>(
+    static bool smem_set = false;           // the attribute is set once, outside any capture
+    if (!smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(radix_downsweep<K, Src>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)downsweep_smem<K>());
+        if (e != cudaSuccess) return e;
+        smem_set = true;
+    }
+    radix_downsweep<K, Src><<<grid, kRadixThreads, downsweep_smem<K>(), st>>>(
         src, shift, ws.hist, tiles, static_cast<K *>(ws.keys[nxt]), ws.vals[nxt], out_stride);
     return cudaGetLastError();
 }
