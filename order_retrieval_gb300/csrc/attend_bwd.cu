@@ -131,17 +131,18 @@ bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
 
 // ------------------------------------------------------------ key side ---
 
-// off[seg][j] = first position of key j in the sorted (key, query) list.
+// off[seg][j] = first position of key j in the sorted (key, query) list; the
+// key of a sorted word is word >> key_shift (0: plain keys, 16: packed words).
 __global__ void csr_offsets(const uint32_t *__restrict__ skeys, const uint32_t *__restrict__ seglen,
-                            int64_t stride, int N, uint32_t *__restrict__ off) {
+                            int64_t stride, int N, int key_shift, uint32_t *__restrict__ off) {
     const int64_t seg = blockIdx.y;
     const int64_t L = seglen[seg];
     const uint32_t *K = skeys + seg * stride;
     uint32_t *o = off + seg * (int64_t)(N + 1);
     for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p <= L;
          p += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t hiK = p < L ? (int64_t)K[p] : (int64_t)N;
-        const int64_t loK = p > 0 ? (int64_t)K[p - 1] : -1;
+        const int64_t hiK = p < L ? (int64_t)(K[p] >> key_shift) : (int64_t)N;
+        const int64_t loK = p > 0 ? (int64_t)(K[p - 1] >> key_shift) : -1;
         for (int64_t j = loK + 1; j <= hiK; ++j) o[j] = (uint32_t)p;
     }
 }
@@ -305,7 +306,7 @@ cudaError_t bwd_generic(const Prob &p, const float *q, const float *k, const voi
     if (e != cudaSuccess) return e;
     const int64_t L = p.N * (int64_t)p.k;
     csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(
-        static_cast<const uint32_t *>(w.rw.keys[ob]), w.rw.seglen, L, p.N, w.off);
+        static_cast<const uint32_t *>(w.rw.keys[ob]), w.rw.seglen, L, p.N, 0, w.off);
     bwd_key_generic<V, VPL><<<blocks, 256, 0, st>>>(
         q, k, static_cast<const V *>(v), gamma, w.s, static_cast<const V *>(dout), w.gbar,
         w.rw.vals[ob], w.off, L, dk, static_cast<V *>(dv), p.S, p.N, p.H, p.dK, p.dV, p.C);
@@ -345,12 +346,16 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
                                             status, st);
         if (e != cudaSuccess) return e;
         int ob = 0;
-        e = radix_sort_idx(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st);
+        const bool packed = p.N <= 65536;
+        e = packed ? radix_sort_idx_packed(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st)
+                   : radix_sort_idx(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st);
         if (e != cudaSuccess) return e;
         const int64_t L = p.N * (int64_t)p.k;
-        csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(
-            static_cast<const uint32_t *>(w.rw.keys[ob]), w.rw.seglen, L, p.N, w.off);
-        e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, w.rw.vals[ob], w.off, L, dk, dv, st);
+        const uint32_t *sorted = static_cast<const uint32_t *>(w.rw.keys[ob]);
+        csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(sorted, w.rw.seglen, L, p.N,
+                                                              packed ? 16 : 0, w.off);
+        e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, packed ? sorted : w.rw.vals[ob],
+                              packed ? 0xffffu : 0xffffffffu, w.off, L, dk, dv, st);
         if (e != cudaSuccess) return e;
         dgamma_reduce(p, w, dgamma, st);
         return cudaGetLastError();

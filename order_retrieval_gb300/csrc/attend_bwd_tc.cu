@@ -414,7 +414,7 @@ template <int DK>
 __global__ void __launch_bounds__(THREADS, 4)
 bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
            const float *__restrict__ gamma, const __nv_bfloat16 *__restrict__ dout,
-           const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q,
+           const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q, uint32_t csr_mask,
            const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
            __nv_bfloat16 *__restrict__ dv, int N, int H, int C, int tiles_per_chunk) {
     __shared__ KSmem sm;
@@ -473,7 +473,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 const int64_t pp = p0 + h * 4 + grp;
-                inext[h] = pp < p1 ? __ldg(lst + pp) : 0xffffffffu;
+                inext[h] = pp < p1 ? (__ldg(lst + pp) & csr_mask) : 0xffffffffu;
             }
             for (int64_t p = p0; p < p1; p += 16) {
                 uint32_t ic[4];
@@ -481,7 +481,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 for (int h = 0; h < 4; ++h) {
                     ic[h] = inext[h];
                     const int64_t pp = p + 16 + h * 4 + grp;
-                    inext[h] = pp < p1 ? __ldg(lst + pp) : 0xffffffffu;
+                    inext[h] = pp < p1 ? (__ldg(lst + pp) & csr_mask) : 0xffffffffu;
                 }
                 uint4 dbuf[4];
                 QRec qrec[4];
@@ -730,14 +730,14 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
 
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
                               const void *dout, const void *rec, const uint32_t *csr_q,
-                              const uint32_t *off, int64_t csr_stride, float *dk, void *dv,
-                              cudaStream_t st) {
+                              uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
+                              float *dk, void *dv, cudaStream_t st) {
     const int tpc = (p.C + T64 - 1) / T64;
     const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
 #define ZETA_BK(D)                                                                              \
     bwd_key_tc<D><<<grid, THREADS, 0, st>>>(                                                   \
         k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout), \
-        static_cast<const QRec *>(rec), csr_q, off, csr_stride, dk,                           \
+        static_cast<const QRec *>(rec), csr_q, csr_mask, off, csr_stride, dk,                 \
         static_cast<__nv_bfloat16 *>(dv), p.N, p.H, p.C, tpc)
     switch (p.dK) {
         case 1: ZETA_BK(1); break;

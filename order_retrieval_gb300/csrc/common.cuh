@@ -84,10 +84,11 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
                                 const float *gamma, const int32_t *idx, const void *dout,
                                 float *dq, void *rec, float *dg_part, int32_t *status,
                                 cudaStream_t st);
+// csr_q holds the queries of every key's list (masked with csr_mask).
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
                               const void *dout, const void *rec, const uint32_t *csr_q,
-                              const uint32_t *off, int64_t csr_stride, float *dk, void *dv,
-                              cudaStream_t st);
+                              uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
+                              float *dk, void *dv, cudaStream_t st);
 
 size_t bwd_ws_bytes(const Prob &p);
 cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, const void *v,
@@ -121,6 +122,12 @@ cudaError_t radix_sort_codes(const K *codes, int64_t S, int64_t N, int key_bits,
 // Per-slice counts land in ws.seglen.
 cudaError_t radix_sort_idx(const int32_t *idx, int64_t S, int64_t N, int k, int C, RadixWs &ws,
                            int *out_buf, int32_t *status, cudaStream_t st);
+
+// The same transpose for N <= 65536 with each entry packed as (key << 16) |
+// query in one 32-bit word (keys only, no value array); sorted words land in
+// ws.keys[*out_buf].
+cudaError_t radix_sort_idx_packed(const int32_t *idx, int64_t S, int64_t N, int k, int C,
+                                  RadixWs &ws, int *out_buf, int32_t *status, cudaStream_t st);
 
 // Carve aligned sub-buffers out of a workspace.
 struct Carver {

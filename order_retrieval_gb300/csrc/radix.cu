@@ -17,6 +17,7 @@ namespace {
 
 template <typename K>
 struct CodesSrc {          // first pass over Z codes: value = position
+    static constexpr bool kHasVal = true;
     const K *codes;
     int64_t N;
     __device__ int64_t len(int64_t) const { return N; }
@@ -29,6 +30,7 @@ struct CodesSrc {          // first pass over Z codes: value = position
 
 template <typename K>
 struct PairsSrc {          // later passes: ping-pong buffers
+    static constexpr bool kHasVal = true;
     const K *keys;
     const uint32_t *vals;
     int64_t stride;
@@ -42,6 +44,7 @@ struct PairsSrc {          // later passes: ping-pong buffers
 };
 
 struct IdxSrc {            // window indices: key = selected key, value = query
+    static constexpr bool kHasVal = true;
     const int32_t *idx;
     int64_t N;
     int k;
@@ -55,6 +58,39 @@ struct IdxSrc {            // window indices: key = selected key, value = query
         if (static_cast<uint32_t>(j) >= cC) { set_status(st, ZETA_ERR_BOUNDS); return false; }
         key = static_cast<uint32_t>(j);
         val = static_cast<uint32_t>(i);
+        return true;
+    }
+};
+
+// Window indices packed into one word, (key << 16) | query, when N <= 2^16:
+// sorting the words on their top 16 bits is the stable transpose by key, and
+// no separate value array moves.
+struct PackedIdxSrc {
+    static constexpr bool kHasVal = false;
+    const int32_t *idx;
+    int64_t N;
+    int k;
+    int C;
+    __device__ int64_t len(int64_t) const { return N * k; }
+    __device__ bool load(int64_t seg, int64_t p, uint32_t &key, uint32_t &, int32_t *st) const {
+        const int32_t j = idx[seg * N * k + p];
+        if (j == -1) return false;
+        const uint32_t i = static_cast<uint32_t>(p) / static_cast<uint32_t>(k);
+        const uint32_t cC = i - i % static_cast<uint32_t>(C);
+        if (static_cast<uint32_t>(j) >= cC) { set_status(st, ZETA_ERR_BOUNDS); return false; }
+        key = (static_cast<uint32_t>(j) << 16) | i;
+        return true;
+    }
+};
+
+struct PackedSrc {         // later passes over packed words
+    static constexpr bool kHasVal = false;
+    const uint32_t *keys;
+    int64_t stride;
+    const uint32_t *seglen;
+    __device__ int64_t len(int64_t seg) const { return (int64_t)seglen[seg]; }
+    __device__ bool load(int64_t seg, int64_t p, uint32_t &key, uint32_t &, int32_t *) const {
+        key = keys[seg * stride + p];
         return true;
     }
 };
@@ -214,7 +250,7 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
         if (dig[r] < 256) {
             const uint32_t tp = tds[dig[r]] + wcnt[w][dig[r]] + rank[r];
             skey[tp] = key[r];
-            sval[tp] = val[r];
+            if constexpr (Src::kHasVal) sval[tp] = val[r];
         }
     }
     __syncthreads();
@@ -224,7 +260,7 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
         const int d = (int)((unsigned)(kk >> shift) & 255u);
         const int64_t dst = (int64_t)soff[d] + (t - tds[d]);
         keys_out[seg * out_stride + dst] = kk;
-        vals_out[seg * out_stride + dst] = sval[t];
+        if constexpr (Src::kHasVal) vals_out[seg * out_stride + dst] = sval[t];
     }
 }
 
@@ -298,6 +334,19 @@ cudaError_t radix_sort_idx(const int32_t *idx, int64_t S, int64_t N, int k, int 
         cur = nxt;
     }
     *out_buf = cur;
+    return cudaSuccess;
+}
+
+cudaError_t radix_sort_idx_packed(const int32_t *idx, int64_t S, int64_t N, int k, int C,
+                                  RadixWs &ws, int *out_buf, int32_t *status, cudaStream_t st) {
+    const int64_t L = N * (int64_t)k;
+    cudaError_t e = run_pass<uint32_t>(PackedIdxSrc{idx, N, k, C}, 16, S, L, ws, 0, L, ws.seglen,
+                                       status, st);
+    if (e != cudaSuccess) return e;
+    e = run_pass<uint32_t>(PackedSrc{static_cast<const uint32_t *>(ws.keys[0]), L, ws.seglen}, 24,
+                           S, L, ws, 1, L, nullptr, nullptr, st);
+    if (e != cudaSuccess) return e;
+    *out_buf = 1;
     return cudaSuccess;
 }
 

@@ -208,6 +208,15 @@ def test_backward_train_bf16_sampled():
         _check_backward_slice(run, s, bf16=True)
 
 
+def test_backward_beyond_16bit_sequence_bf16():
+    """N = 131072 (> 2^16) takes the unpacked (key, query) transpose in the
+    tensor-core backward; one slice against the oracle."""
+    w = W.TRAIN.replace(name="train_n131072", B=1, H=1, N=131072, C=512, k=16)
+    run = Run(w, backward=True)
+    assert run.status() == 0
+    _check_backward_slice(run, 0, bf16=True)
+
+
 def test_backward_clustered_bf16():
     w = W.CLUSTERED.replace(B=1)
     run = Run(w, backward=True)
