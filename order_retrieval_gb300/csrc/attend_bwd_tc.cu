@@ -17,7 +17,8 @@
 //                  32-byte record {q_i, 1/s_i, gbar_i} for the key side.
 // Key side, one CTA per 64 keys of a chunk:
 //   window part  - the queries that selected key j (a transpose of idx sorted
-//                  by query), four at a time, eight lanes per dO row:
+//                  by query), 32 at a time: one lane per listed query for the
+//                  scalar terms, eight lanes per dO row for the row work:
 //                  dv_j += a_ij dO_i and dk_j += dL/dw_ij 2 w^2/gamma^2 (q_i - k_j).
 //   own chunk    - S^T = V . dO^T on tensor cores, the element-wise terms, then
 //                  dV += P^T . dO with P^T re-packed from the accumulator
@@ -450,14 +451,22 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     const int grp = lane >> 3, sub = lane & 7;
     const uint32_t *lst = csr_q + seg * csr_stride;
     const uint32_t *ob = off + seg * (int64_t)(N + 1);
+    // Each key's list is walked 32 entries at a time.  Lane e owns entry e of a
+    // chunk (its query's record, the Cauchy weight w, a = w / s and the dk
+    // term); eight lanes read one dO row slice each, so all 32 dO rows of the
+    // chunk are requested together.  The next chunk's list positions are
+    // fetched while the current chunk is processed.
+    const int wj0 = j0 + warp * 16;
+    const int nkw = max(0, min(16, jend - wj0));
+    const uint32_t bnd = lane <= nkw ? ob[wj0 + lane] : 0u;     // list bounds of this warp
     for (int r = 0; r < 16; ++r) {
         const int row = warp * 16 + r;
-        const int j = j0 + row;
+        const int j = wj0 + r;
         float2 acc[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
         float dka[4] = {0.f, 0.f, 0.f, 0.f};
-        if (j < jend) {
+        if (r < nkw) {
             float2 v2[4];
             {
                 const uint4 raw = *reinterpret_cast<const uint4 *>(vb + (int64_t)j * DV + sub * 8);
@@ -466,62 +475,64 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 for (int e = 0; e < 4; ++e) v2[e] = bf2_to_f2(uw[e]);
             }
             const float4 kj = load_k4(kb + (int64_t)j * DK, DK);
-            // Sixteen listed queries per step (four per lane group), their list
-            // positions fetched one step ahead.
-            const int64_t p0 = ob[j], p1 = ob[j + 1];
-            uint32_t inext[4];
+            const float kjc[4] = {kj.x, kj.y, kj.z, kj.w};
+            const uint32_t p0 = __shfl_sync(kFull, bnd, r), p1 = __shfl_sync(kFull, bnd, r + 1);
+            uint32_t inext = p0 + lane < p1 ? (__ldg(lst + p0 + lane) & csr_mask) : 0xffffffffu;
+            for (uint32_t p = p0; p < p1; p += 32) {
+                const uint32_t ie = inext;
+                inext = p + 32 + lane < p1 ? (__ldg(lst + p + 32 + lane) & csr_mask) : 0xffffffffu;
+                const bool own = ie != 0xffffffffu;
+                const int nst = min(8, (int)((p1 - p + 3) >> 2));   // 4-entry steps in this chunk
+                uint4 dbuf[8];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int64_t pp = p0 + h * 4 + grp;
-                inext[h] = pp < p1 ? (__ldg(lst + pp) & csr_mask) : 0xffffffffu;
-            }
-            for (int64_t p = p0; p < p1; p += 16) {
-                uint32_t ic[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    ic[h] = inext[h];
-                    const int64_t pp = p + 16 + h * 4 + grp;
-                    inext[h] = pp < p1 ? (__ldg(lst + pp) & csr_mask) : 0xffffffffu;
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t iu = __shfl_sync(kFull, ie, u * 4 + grp);
+                    dbuf[u] = (u < nst && iu != 0xffffffffu)
+                                  ? ld_stream16(db + (int64_t)iu * DV + sub * 8)
+                                  : make_uint4(0u, 0u, 0u, 0u);
                 }
-                uint4 dbuf[4];
-                QRec qrec[4];
+                // the owner's scalars for its entry
+                float a = 0.f, s2 = 0.f, inv_s = 0.f, gb = 0.f;
+                float dqk[4] = {0.f, 0.f, 0.f, 0.f};
+                if (own) {
+                    const QRec qrc = rb_[ie];
+                    const float qc[4] = {qrc.q.x, qrc.q.y, qrc.q.z, qrc.q.w};
+                    float d2 = 0.f;
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    if (ic[h] != 0xffffffffu) {
-                        dbuf[h] = ld_stream16(db + (int64_t)ic[h] * DV + sub * 8);
-                        qrec[h] = rb_[ic[h]];
+                    for (int d = 0; d < DK; ++d) {
+                        dqk[d] = qc[d] - kjc[d];
+                        d2 = __fmaf_rn(dqk[d], dqk[d], d2);
                     }
+                    const float w = cauchy_w_fast(d2, inv_g2);
+                    inv_s = qrc.sg.x;
+                    gb = qrc.sg.y;
+                    a = w * inv_s;
+                    s2 = 2.f * w * w * inv_g2;
                 }
+                float gown = 0.f;
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const bool ok = ic[h] != 0xffffffffu;
-                    float2 d2v[4];
-                    float2 gg = make_float2(0.f, 0.f);
-                    if (ok) {
-                        const uint32_t uw[4] = {dbuf[h].x, dbuf[h].y, dbuf[h].z, dbuf[h].w};
+                for (int u = 0; u < 8; ++u) {
+                    if (u < nst) {
+                        const uint32_t uw[4] = {dbuf[u].x, dbuf[u].y, dbuf[u].z, dbuf[u].w};
+                        float2 d2v[4];
+                        float2 gg = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             d2v[e] = bf2_to_f2(uw[e]);
                             gg = fma2(d2v[e], v2[e], gg);
                         }
-                    }
-                    const float g = warp_group8_sum(gg.x + gg.y);
-                    if (ok) {
-                        const float4 qi = qrec[h].q;
-                        const float qv[4] = {qi.x, qi.y, qi.z, qi.w};
-                        const float w = cauchy_w_fast(dist2k<DK>(qv, kj), inv_g2);
-                        const float inv_s = qrec[h].sg.x;
-                        const float a = w * inv_s;
-                        const float dldw = (g - qrec[h].sg.y) * inv_s;
-                        const float coef = dldw * (2.f * w * w * inv_g2);
-                        const float2 a2 = dup2(a);
+                        const float g = warp_group8_sum(gg.x + gg.y);
+                        const float2 au = dup2(__shfl_sync(kFull, a, u * 4 + grp));
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[e] = fma2(a2, d2v[e], acc[e]);
-                        dka[0] = __fmaf_rn(coef, qi.x - kj.x, dka[0]);
-                        dka[1] = __fmaf_rn(coef, qi.y - kj.y, dka[1]);
-                        dka[2] = __fmaf_rn(coef, qi.z - kj.z, dka[2]);
-                        dka[3] = __fmaf_rn(coef, qi.w - kj.w, dka[3]);
+                        for (int e = 0; e < 4; ++e) acc[e] = fma2(au, d2v[e], acc[e]);
+                        const float gx = __shfl_sync(kFull, g, (lane & 3) * 8);
+                        if ((lane >> 2) == u) gown = gx;
                     }
+                }
+                if (own) {
+                    const float coef = (gown - gb) * inv_s * s2;
+#pragma unroll
+                    for (int d = 0; d < DK; ++d) dka[d] = __fmaf_rn(coef, dqk[d], dka[d]);
                 }
             }
 #pragma unroll
@@ -532,10 +543,9 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 acc[e].y += __shfl_xor_sync(kFull, acc[e].y, 16);
             }
 #pragma unroll
-            for (int d = 0; d < 4; ++d) {
-                dka[d] += __shfl_xor_sync(kFull, dka[d], 8);
-                dka[d] += __shfl_xor_sync(kFull, dka[d], 16);
-            }
+            for (int d = 0; d < DK; ++d)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) dka[d] += __shfl_xor_sync(kFull, dka[d], o);
         }
         if (lane < 8) {
             float4 *dst = reinterpret_cast<float4 *>(&sm.dvp[row][lane * 8]);
