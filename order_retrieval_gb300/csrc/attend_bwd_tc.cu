@@ -198,10 +198,11 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
 
     // ---------------------------------------------------- window part ---
     // A pass covers up to 64 selected keys.  Lane L owns slots L and L+32 (index,
-    // coordinates, the pair's Cauchy terms); eight lanes form g_ij for one value
-    // row (16-byte slice dot + 3 shuffles) and the owner picks it up with one
-    // shuffle.  The next query's indices are fetched while this one runs.
-    const int grp = lane >> 3, sub = lane & 7;
+    // coordinates, the pair's Cauchy terms); four lanes form g_ij for one value
+    // row (two 16-byte slices each, a 2-shuffle reduction, eight rows per warp
+    // step) and the owner picks it up with one shuffle.  The next query's
+    // indices are fetched while this one runs.
+    const int g4 = lane >> 2, s4 = lane & 3;
     const int wq0 = i0 + warp * 16;
     const int nqw = c > 0 ? max(0, min(16, iend - wq0)) : 0;
     auto load_idx = [&](int i, int t0, int (&j)[2]) {
@@ -223,12 +224,13 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
             float qi[4];
 #pragma unroll
             for (int d = 0; d < 4; ++d) qi[d] = d < DK ? qb[(int64_t)i * DK + d] : 0.f;
-            float2 do2[4];
+            float2 do2[8];                              // dO_i[16 s4 .. 16 s4 + 16)
             {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(db + (int64_t)i * DV + sub * 8);
-                const uint32_t uw[4] = {raw.x, raw.y, raw.z, raw.w};
+                const uint4 *src = reinterpret_cast<const uint4 *>(db + (int64_t)i * DV + s4 * 16);
+                const uint4 r0 = src[0], r1 = src[1];
+                const uint32_t uw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) do2[e] = bf2_to_f2(uw[e]);
+                for (int e = 0; e < 8; ++e) do2[e] = bf2_to_f2(uw[e]);
             }
             for (int t0 = 0; t0 < k; t0 += 64) {
                 int j[2] = {jn[0], jn[1]};
@@ -244,25 +246,36 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     kk[s] = j[s] >= 0 ? load_k4(kb + (int64_t)j[s] * DK, DK)
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                const int nu = min(16, (k - t0 + 3) >> 2);
+                const int nu = min(8, (k - t0 + 7) >> 3);   // 8-row steps in this pass
                 uint4 buf[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int jr = __shfl_sync(kFull, j[u >> 3], (u * 4 + grp) & 31);
-                    buf[u] = (u < nu && jr >= 0) ? ld_stream16(vb + (int64_t)jr * DV + sub * 8)
-                                                 : make_uint4(0u, 0u, 0u, 0u);
+                for (int u = 0; u < 8; ++u) {
+                    const int jr = __shfl_sync(kFull, j[u >> 2], (u * 8 + g4) & 31);
+                    const bool ok = u < nu && jr >= 0;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(vb + (int64_t)jr * DV + s4 * 16);
+                    buf[2 * u] = ok ? ld_stream16(src) : make_uint4(0u, 0u, 0u, 0u);
+                    buf[2 * u + 1] = ok ? ld_stream16(src + 1) : make_uint4(0u, 0u, 0u, 0u);
                 }
                 float gown[2] = {0.f, 0.f};
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
+                for (int u = 0; u < 8; ++u) {
                     if (u < nu) {
-                        const uint32_t uw[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
-                        float2 gg = mul2(do2[0], bf2_to_f2(uw[0]));
+                        const uint32_t uw[8] = {buf[2 * u].x, buf[2 * u].y, buf[2 * u].z,
+                                                buf[2 * u].w, buf[2 * u + 1].x, buf[2 * u + 1].y,
+                                                buf[2 * u + 1].z, buf[2 * u + 1].w};
+                        float2 ga = mul2(do2[0], bf2_to_f2(uw[0]));
+                        float2 gb2 = mul2(do2[1], bf2_to_f2(uw[1]));
 #pragma unroll
-                        for (int e = 1; e < 4; ++e) gg = fma2(do2[e], bf2_to_f2(uw[e]), gg);
-                        const float g = warp_group8_sum(gg.x + gg.y);
-                        const float gx = __shfl_sync(kFull, g, (lane & 3) * 8);
-                        if ((u & 7) == (lane >> 2)) gown[u >> 3] = gx;
+                        for (int e = 2; e < 8; e += 2) {
+                            ga = fma2(do2[e], bf2_to_f2(uw[e]), ga);
+                            gb2 = fma2(do2[e + 1], bf2_to_f2(uw[e + 1]), gb2);
+                        }
+                        float g = (ga.x + ga.y) + (gb2.x + gb2.y);
+                        g += __shfl_xor_sync(kFull, g, 1);
+                        g += __shfl_xor_sync(kFull, g, 2);
+                        // row u*8 + G is owned by lane (u*8 + G) & 31, slot u >> 2
+                        const float gx = __shfl_sync(kFull, g, (lane & 7) * 4);
+                        if ((u & 3) == (lane >> 3)) gown[u >> 2] = gx;
                     }
                 }
 #pragma unroll
