@@ -146,7 +146,11 @@ LONG = Workload("long_bf16_n1048576", 1, 8, 1048576, 3, 64, 64, 4096, 10, "bf16"
 TRAIN = Workload("train_bf16_b4_n65536", 4, 8, 65536, 3, 64, 48, 1024, 10, "bf16", 0.5,
                  "uniform", "uniform", 4)
 
-ALL = {w.name: w for w in (TINY, CLUSTERED, EFFICIENCY, LONG, TRAIN)}
+# The pages' own grid: 12 bits per coordinate, 36-bit codes (64-bit containers),
+# at the efficiency scale.
+PAGES12 = EFFICIENCY.replace(name="efficiency12_bf16_n65536", bits=12)
+
+ALL = {w.name: w for w in (TINY, CLUSTERED, EFFICIENCY, LONG, TRAIN, PAGES12)}
 
 # Locality side sweep: N=16384, C=1024, d_K in {1,2,3,8} at 21/21/10/8 bits.
 SWEEP = [LONG.replace(name=f"sweep_dk{dk}_n16384", N=16384, C=1024, d_K=dk, bits=b)

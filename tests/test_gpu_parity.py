@@ -119,11 +119,12 @@ def test_forward_clustered_bf16():
         _check_forward_slice(run, s, bf16=True)
 
 
-def test_forward_efficiency_sampled():
-    """The 65,536-token workload in the timed launch configuration: prefix
-    tables of every slice checked by property, one slice's table exactly, and
-    sampled queries of every slice against the oracle."""
-    w = W.EFFICIENCY
+@pytest.mark.parametrize("w", [W.EFFICIENCY, W.PAGES12], ids=lambda w: w.name)
+def test_forward_efficiency_sampled(w):
+    """The 65,536-token workload in the timed launch configuration (and with
+    the pages' 12-bit grid, 36-bit codes in 64-bit containers): prefix tables
+    of every slice checked by property, one slice's table exactly, and sampled
+    queries of every slice against the oracle."""
     run = Run(w)
     assert run.status() == 0
     g = run.g
