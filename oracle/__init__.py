@@ -55,6 +55,8 @@ def _load():
     lib.orc_attend_fwd.argtypes = [P, P, P, D, P, I64, I64, I, I, I, P, I64, P, P]
     lib.orc_attend_bwd.argtypes = [P, P, P, D, P, P, I64, I64, I, I, I, P, P, P, P]
     lib.orc_exact_topk.argtypes = [P, P, I64, I64, I, I, P, I64, P]
+    lib.orc_encode_axes.argtypes = [P, I64, I, I, P, P]
+    lib.orc_merge_windows.argtypes = [P, I, I, I, P]
     _lib = lib
     return lib
 
@@ -91,6 +93,59 @@ def encode(x: np.ndarray, bits: int) -> np.ndarray:
     out = np.empty(x.shape[:-1], dtype=np.uint64)
     _load().orc_encode(_p(x), out.size, d_K, bits, _p(out))
     return out
+
+
+def encode_axes(x: np.ndarray, bits: int, axes) -> np.ndarray:
+    """Codes of the coordinates taken in the order `axes` (a permutation)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    d_K = x.shape[-1]
+    ax = np.ascontiguousarray(axes, dtype=np.int32)
+    assert sorted(ax.tolist()) == list(range(d_K))
+    out = np.empty(x.shape[:-1], dtype=np.uint64)
+    _load().orc_encode_axes(_p(x), out.size, d_K, bits, _p(ax), _p(out))
+    return out
+
+
+def curve_axes(d_K: int, curves: int):
+    """Axis orders of the multi-curve variant: 1 curve = identity; 3 curves =
+    the cyclic shifts (0,1,2), (1,2,0), (2,0,1); 6 curves = all permutations in
+    the pages' order (0,1,2), (0,2,1), (1,2,0), (1,0,2), (2,0,1), (2,1,0)."""
+    if curves == 1:
+        return [list(range(d_K))]
+    assert d_K == 3, "multi-curve orders are defined for d_K = 3"
+    if curves == 3:
+        return [[0, 1, 2], [1, 2, 0], [2, 0, 1]]
+    if curves == 6:
+        return [[0, 1, 2], [0, 2, 1], [1, 2, 0], [1, 0, 2], [2, 0, 1], [2, 1, 0]]
+    raise ValueError("curves must be 1, 3 or 6")
+
+
+def merge_windows(windows: np.ndarray, k: int) -> np.ndarray:
+    """windows int32 [..., M, km] -> union rows int32 [..., k] (curve order,
+    first occurrence kept, -1 padded)."""
+    w = np.ascontiguousarray(windows, dtype=np.int32)
+    M, km = w.shape[-2], w.shape[-1]
+    lead = w.shape[:-2]
+    flat = w.reshape(-1, M * km)
+    out = np.empty((flat.shape[0], k), dtype=np.int32)
+    lib = _load()
+    for r in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[r])
+        o = out[r]
+        lib.orc_merge_windows(_p(row), M, km, k, _p(o))
+    return out.reshape(*lead, k)
+
+
+def select_multi(q, kx, C: int, k: int, bits: int, curves: int, rows=None):
+    """Multi-curve window of one slice: per curve, codes of the permuted axes,
+    a window of k // curves keys; the union row of k entries."""
+    km = k // curves
+    wins = []
+    for axes in curve_axes(q.shape[-1], curves):
+        qc = encode_axes(q, bits, axes)
+        kc = encode_axes(kx, bits, axes)
+        wins.append(select(qc[None], kc[None], C, km, rows=rows)[0])
+    return merge_windows(np.stack(wins, axis=-2), k)
 
 
 # ------------------------------------------------------------ sort/select ---

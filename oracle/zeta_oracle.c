@@ -36,7 +36,11 @@
  *     code; the window is positions [clamp(r - ceil(k/2), 0, M - k), +k) of that
  *     sorted prefix of M = c*C keys (all M, padded with -1, when M < k);
  *   - every key j of the query's own chunk with j <= i joins the attended set;
- *   - Cauchy weight w = 1 / (1 + |q - k|^2 / gamma^2), normalised over the set.
+ *   - Cauchy weight w = 1 / (1 + |q - k|^2 / gamma^2), normalised over the set;
+ *   - several curves [RB-asym]: curve m reads the coordinates in the order
+ *     axes[m]; each curve's window holds k // curves keys (same centring rule);
+ *     the union lists the windows in curve order, drops a key an earlier curve
+ *     (or slot) already gave, and pads the row to k with -1.
  *
  * Floating point is double everywhere except the quantiser, which the reading
  * above fixes to float32.  Compile with -ffp-contract=off.
@@ -303,4 +307,40 @@ void orc_exact_topk(const float *q, const float *kx, int64_t N, int64_t C, int d
         for (int s = 0; s < k; ++s) out[t * k + s] = s < M ? buf[s].idx : -1;
     }
     free(buf);
+}
+
+/* --------------------------------------------------- multiple Z curves --- */
+
+/* Codes of the coordinates read in the order axes[0..d_K) (a permutation of
+ * 0..d_K-1): the curve of the tuple (x[axes[0]], x[axes[1]], ...), OpenReview
+ * discussion, reply on the asymmetry of Z-order curves (shifted and permuted
+ * coordinate orders (K^1,K^2,K^3), (K^2,K^3,K^1), ...). */
+void orc_encode_axes(const float *x, int64_t ntok, int d_K, int bits, const int32_t *axes,
+                     uint64_t *codes)
+{
+    uint32_t u[64];
+    for (int64_t t = 0; t < ntok; ++t) {
+        for (int d = 0; d < d_K; ++d)
+            u[d] = orc_quantise(x[t * d_K + axes[d]], bits);
+        codes[t] = orc_interleave(u, d_K, bits);
+    }
+}
+
+/* Union of M per-curve windows of one query, same reply ("each mapping
+ * collects k//M tokens"): curve windows in curve order, an index already taken
+ * from an earlier curve (or earlier in the same window) is dropped, the row is
+ * filled to k with -1.  win: M rows of km entries; out: k entries. */
+void orc_merge_windows(const int32_t *win, int M, int km, int k, int32_t *out)
+{
+    int n = 0;
+    for (int m = 0; m < M; ++m)
+        for (int t = 0; t < km; ++t) {
+            int32_t j = win[m * km + t];
+            if (j < 0) continue;
+            int dup = 0;
+            for (int s = 0; s < n; ++s)
+                if (out[s] == j) { dup = 1; break; }
+            if (!dup && n < k) out[n++] = j;
+        }
+    for (; n < k; ++n) out[n] = -1;
 }
