@@ -383,6 +383,38 @@ def run_ours(args, w, rank, world):
     fwd_e_ms = sum(fwd_e) / len(fwd_e)
     att_e_ms = sum(att_e) / len(att_e)
 
+    # --- multi-curve variant (3 cyclic / 6 permuted coordinate orders) on the
+    # efficiency workload: the whole forward, and its index part
+    variants = {}
+    for curves in (3, 6):
+        pc = ZetaPlan(pe, dev, backward=False, curves=curves)
+        for _ in range(warm):
+            pc.forward(qe, ke, ve, gme)
+        tot, sel = [], []
+        for _ in range(args.steps):
+            flush.zero_()
+            e = [ev() for _ in range(3)]
+            e[0].record()
+            zb.zeta_encode_curves(pe, qe, pc.axes, pc.q_codes)
+            zb.zeta_encode_curves(pe, ke, pc.axes, pc.k_codes)
+            zb.zeta_sort_chunks(pc.p_sort, pc.k_codes, pc.prefix_codes, pc.prefix_idx,
+                                pc.sort_ws)
+            zb.zeta_select_topk_curves(pe, curves, pc.q_codes, pc.prefix_codes, pc.prefix_idx,
+                                       pc.idx)
+            e[1].record()
+            zb.zeta_attend_fwd(pe, qe, ke, ve, gme, pc.idx, pc.out, pc.rowsum, pc.status)
+            e[2].record()
+            e[2].synchronize()
+            tot.append(e[0].elapsed_time(e[2]))
+            sel.append(e[0].elapsed_time(e[1]))
+        if int(pc.status.item()) != 0:
+            raise RuntimeError(f"device status {pc.status.item()} ({curves} curves)")
+        ms = sum(tot) / len(tot)
+        variants[f"curves{curves}"] = {
+            "workload": we.name, "fwd_tokens_per_s": we.B * we.N * world / (ms * 1e-3),
+            "fwd_ms": ms, "encode_sort_select_ms": sum(sel) / len(sel)}
+        del pc
+
     if rank != 0:
         return
     peaks = {}
@@ -419,6 +451,7 @@ def run_ours(args, w, rank, world):
         "fwd_efficiency": {"workload": we.name, "tokens_per_s": we.B * we.N * world /
                            (fwd_e_ms * 1e-3), "ms": fwd_e_ms, "attend_fwd_ms": att_e_ms},
         "per_call_ms": per_call,
+        "variants": variants,
         "roofline": {"kernel": "attend_fwd_tc (efficiency workload, L2 flushed)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": None,

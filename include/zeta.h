@@ -155,6 +155,47 @@ zeta_status_t zeta_select_topk(const zeta_problem_t *p, const void *q_codes,
                                int32_t *idx, cudaStream_t stream);
 
 /*
+ * zeta_encode_curves -- codes of every token along several Z-order curves.
+ * Passage: OpenReview discussion, reply on the asymmetry of Z-order curves
+ * (the key coordinates are interleaved in several orders: the three cyclic
+ * shifts of (K^1, K^2, K^3), or all six orderings).
+ * Curve m reads coordinate axes[m][s] into slot s, slot 0 being the most
+ * significant bit of each level; with axes[m] = (0, 1, ..., d_K - 1) the code
+ * is the one zeta_encode writes.  Quantisation as for zeta_encode.
+ *   x       in : float [B, H, N, d_K]
+ *   curves  in : 1..8
+ *   axes    in : HOST int32 [curves][d_K], every row a permutation of 0..d_K-1
+ *                (read during the call only)
+ *   codes   out: code type of the problem [curves][B, H, N]
+ * Errors: ZETA_ERR_INVALID_ARG (null pointers, curves out of range, a row of
+ *         axes that is not a permutation).
+ */
+zeta_status_t zeta_encode_curves(const zeta_problem_t *p, const float *x, int32_t curves,
+                                 const int32_t *axes, void *codes, cudaStream_t stream);
+
+/*
+ * zeta_select_topk_curves -- the union of one window per curve.
+ * Passage: OpenReview discussion, reply on the asymmetry of Z-order curves
+ * (every curve collects k // curves of the k tokens).
+ * Reading of the union: with km = k // curves, curve m gives the km keys that
+ * zeta_select_topk would give with km in place of k (its own prefix table);
+ * the windows are listed in curve order, a key already listed is dropped, and
+ * the row is padded to k with -1.  Chunk-0 rows are all -1.
+ *   q_codes       in : [curves][B, H, N]  (zeta_encode_curves)
+ *   prefix_codes  in : [curves][B, H, T]  (curve m's key codes sorted by
+ *   prefix_idx    in : [curves][B, H, T]   zeta_sort_chunks; one call on the
+ *                      problem with B replaced by curves*B sorts every curve,
+ *                      as the two layouts coincide)
+ *   idx           out: int32 [B, H, N, k], for zeta_attend_fwd / _bwd
+ * Limits: 1 <= curves <= 8, k // curves >= 1, k <= 256.
+ * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED (k > 256).
+ */
+zeta_status_t zeta_select_topk_curves(const zeta_problem_t *p, int32_t curves,
+                                      const void *q_codes, const void *prefix_codes,
+                                      const int32_t *prefix_idx, int32_t *idx,
+                                      cudaStream_t stream);
+
+/*
  * zeta_attend_fwd -- Adaptive Cauchy-softmax over the selected keys.
  * Passage: OpenReview reply A2 "Discussion on its robustness" (trainable gamma,
  * Cauchy softmax), reply A3 "Justification for Euclidean Distance Claim", and

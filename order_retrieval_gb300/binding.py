@@ -83,6 +83,10 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.zeta_sort_chunks.restype = S
     L.zeta_select_topk.argtypes = [PP, P, P, P, P, P]
     L.zeta_select_topk.restype = S
+    L.zeta_encode_curves.argtypes = [PP, P, ctypes.c_int32, P, P, P]
+    L.zeta_encode_curves.restype = S
+    L.zeta_select_topk_curves.argtypes = [PP, ctypes.c_int32, P, P, P, P, P]
+    L.zeta_select_topk_curves.restype = S
     L.zeta_attend_fwd.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.zeta_attend_fwd.restype = S
     L.zeta_attend_bwd.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
@@ -206,6 +210,50 @@ def zeta_select_topk(p, q_codes, prefix_codes, prefix_idx, idx, stream=None):
     _check("zeta_select_topk",
            lib().zeta_select_topk(ctypes.byref(p), _ptr(q_codes), _ptr(prefix_codes),
                                   _ptr(prefix_idx), _ptr(idx), _stream(stream)))
+
+
+def zeta_encode_curves(p, x, axes, codes, stream=None):
+    """axes: sequence of `curves` coordinate orders (each a permutation of
+    0..d_K-1); codes: [curves * B * H * N] of the problem's code type."""
+    rows = [list(map(int, a)) for a in axes]
+    curves = len(rows)
+    S = p.B * p.H * p.N
+    _expect(x, "x", torch.float32, S * p.d_K)
+    _expect(codes, "codes", code_dtype(p), curves * S)
+    flat = [v for r in rows for v in r]
+    if any(len(r) != p.d_K for r in rows):
+        raise ValueError("every axis order needs d_K entries")
+    arr = (ctypes.c_int32 * max(1, len(flat)))(*flat)
+    _check("zeta_encode_curves",
+           lib().zeta_encode_curves(ctypes.byref(p), _ptr(x), curves, arr, _ptr(codes),
+                                    _stream(stream)))
+
+
+def zeta_select_topk_curves(p, curves, q_codes, prefix_codes, prefix_idx, idx, stream=None):
+    S = p.B * p.H
+    T = zeta_prefix_entries(p)
+    _expect(q_codes, "q_codes", code_dtype(p), curves * S * p.N)
+    _expect(prefix_codes, "prefix_codes", code_dtype(p), curves * S * T)
+    _expect(prefix_idx, "prefix_idx", torch.int32, curves * S * T)
+    _expect(idx, "idx", torch.int32, S * p.N * p.k)
+    _check("zeta_select_topk_curves",
+           lib().zeta_select_topk_curves(ctypes.byref(p), curves, _ptr(q_codes),
+                                         _ptr(prefix_codes), _ptr(prefix_idx), _ptr(idx),
+                                         _stream(stream)))
+
+
+def curve_axes(d_K: int, curves: int) -> list:
+    """The pages' coordinate orders: one curve = (0..d_K-1); three = the cyclic
+    shifts of (0, 1, 2); six = all orderings of (0, 1, 2)."""
+    if curves == 1:
+        return [list(range(d_K))]
+    if d_K != 3:
+        raise ValueError("several curves are defined for d_K = 3")
+    if curves == 3:
+        return [[0, 1, 2], [1, 2, 0], [2, 0, 1]]
+    if curves == 6:
+        return [[0, 1, 2], [0, 2, 1], [1, 2, 0], [1, 0, 2], [2, 0, 1], [2, 1, 0]]
+    raise ValueError("curves must be 1, 3 or 6")
 
 
 def zeta_attend_fwd(p, q, k, v, gamma, idx, out, rowsum, dev_status=None, stream=None):

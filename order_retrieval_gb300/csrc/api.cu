@@ -119,6 +119,43 @@ ZETA_API zeta_status_t zeta_select_topk(const zeta_problem_t *p, const void *q_c
     return from_cuda(zeta::launch_select(pr, q_codes, prefix_codes, prefix_idx, idx, stream));
 }
 
+ZETA_API zeta_status_t zeta_encode_curves(const zeta_problem_t *p, const float *x,
+                                          int32_t curves, const int32_t *axes, void *codes,
+                                          cudaStream_t stream) {
+    Prob pr;
+    zeta_status_t s = check_problem(p, &pr);
+    if (s != ZETA_OK) return s;
+    if (curves < 1 || curves > 8 || !axes) return ZETA_ERR_INVALID_ARG;
+    for (int m = 0; m < curves; ++m) {
+        unsigned seen = 0;
+        for (int d = 0; d < pr.dK; ++d) {
+            const int32_t a = axes[m * pr.dK + d];
+            if (a < 0 || a >= pr.dK || (seen >> a) & 1u) return ZETA_ERR_INVALID_ARG;
+            seen |= 1u << a;
+        }
+    }
+    if (empty(pr)) return ZETA_OK;
+    if (!x || !codes) return ZETA_ERR_INVALID_ARG;
+    return from_cuda(zeta::launch_encode_curves(pr, x, curves, axes, codes, stream));
+}
+
+ZETA_API zeta_status_t zeta_select_topk_curves(const zeta_problem_t *p, int32_t curves,
+                                               const void *q_codes, const void *prefix_codes,
+                                               const int32_t *prefix_idx, int32_t *idx,
+                                               cudaStream_t stream) {
+    Prob pr;
+    zeta_status_t s = check_problem(p, &pr);
+    if (s != ZETA_OK) return s;
+    if (curves < 1 || curves > 8 || pr.k / curves < 1) return ZETA_ERR_INVALID_ARG;
+    if (pr.k > 256) return ZETA_ERR_UNSUPPORTED;
+    if (pr.S * curves > 65535) return ZETA_ERR_UNSUPPORTED;
+    if (empty(pr)) return ZETA_OK;
+    if (!q_codes || !idx) return ZETA_ERR_INVALID_ARG;
+    if (pr.T > 0 && (!prefix_codes || !prefix_idx)) return ZETA_ERR_INVALID_ARG;
+    return from_cuda(
+        zeta::launch_select_curves(pr, curves, q_codes, prefix_codes, prefix_idx, idx, stream));
+}
+
 ZETA_API zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, const float *k,
                                        const void *v, const float *gamma, const int32_t *idx,
                                        void *out, float *rowsum, int32_t *dev_status,

@@ -66,6 +66,11 @@ cudaError_t launch_sort_chunks(const Prob &p, const void *key_codes, void *prefi
 
 cudaError_t launch_select(const Prob &p, const void *q_codes, const void *prefix_codes,
                           const int32_t *prefix_idx, int32_t *idx, cudaStream_t st);
+cudaError_t launch_encode_curves(const Prob &p, const float *x, int curves, const int32_t *axes,
+                                 void *codes, cudaStream_t st);
+cudaError_t launch_select_curves(const Prob &p, int curves, const void *q_codes,
+                                 const void *prefix_codes, const int32_t *prefix_idx,
+                                 int32_t *idx, cudaStream_t st);
 
 cudaError_t launch_attend_fwd(const Prob &p, const float *q, const float *k, const void *v,
                               const float *gamma, const int32_t *idx, void *out, float *rowsum,

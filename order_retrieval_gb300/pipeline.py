@@ -5,6 +5,12 @@ workspaces, outputs) so that repeated steps allocate nothing.  ``forward`` and
 ``backward`` enqueue the five library calls on the current stream;
 ``ZetaAttention`` wraps them as a torch.autograd.Function (selection is not
 differentiated).  All arithmetic runs in the library's CUDA kernels.
+
+With ``curves`` = 3 or 6 the plan follows the multi-curve variant (the keys
+are indexed along the cyclic shifts, or all orderings, of the three
+coordinates and every curve contributes k // curves keys): the codes and
+prefix tables gain a leading curve dimension, one sort call covers every
+curve, and the union of the windows feeds the same attend kernels.
 """
 from __future__ import annotations
 
@@ -14,8 +20,14 @@ from . import binding as zb
 
 
 class ZetaPlan:
-    def __init__(self, p: zb.zeta_problem_t, device="cuda", backward: bool = True):
+    def __init__(self, p: zb.zeta_problem_t, device="cuda", backward: bool = True,
+                 curves: int = 1):
         self.p = p
+        self.curves = curves
+        self.axes = zb.curve_axes(p.d_K, curves)
+        # Every curve's slices sort as one problem with curves*B batches.
+        self.p_sort = zb.problem(p.B * curves, p.H, p.N, p.d_K, p.d_V, p.k, p.C, p.bits,
+                                 p.v_dtype) if curves > 1 else p
         dev = torch.device(device)
         S = p.B * p.H
         N = p.N
@@ -25,12 +37,13 @@ class ZetaPlan:
         if T < 0:
             raise zb.ZetaError("zeta_prefix_entries", 1)
         self.T = T
-        self.q_codes = torch.empty(S * N, dtype=cdt, device=dev)
-        self.k_codes = torch.empty(S * N, dtype=cdt, device=dev)
-        self.prefix_codes = torch.empty(max(S * T, 1), dtype=cdt, device=dev)[: S * T]
-        self.prefix_idx = torch.empty(max(S * T, 1), dtype=torch.int32, device=dev)[: S * T]
-        self.sort_ws = torch.empty(max(zb.zeta_sort_workspace_bytes(p), 256), dtype=torch.uint8,
-                                   device=dev)
+        G = curves * S
+        self.q_codes = torch.empty(G * N, dtype=cdt, device=dev)
+        self.k_codes = torch.empty(G * N, dtype=cdt, device=dev)
+        self.prefix_codes = torch.empty(max(G * T, 1), dtype=cdt, device=dev)[: G * T]
+        self.prefix_idx = torch.empty(max(G * T, 1), dtype=torch.int32, device=dev)[: G * T]
+        self.sort_ws = torch.empty(max(zb.zeta_sort_workspace_bytes(self.p_sort), 256),
+                                   dtype=torch.uint8, device=dev)
         self.idx = torch.empty(S * N * p.k, dtype=torch.int32, device=dev)
         self.out = torch.empty(S * N * p.d_V, dtype=vdt, device=dev)
         self.rowsum = torch.empty(S * N, dtype=torch.float32, device=dev)
@@ -47,12 +60,20 @@ class ZetaPlan:
     def forward(self, q, k, v, gamma, stream=None):
         """Encode, sort, select, attend.  Returns (out, rowsum, idx) views."""
         p = self.p
-        zb.zeta_encode(p, q, self.q_codes, stream)
-        zb.zeta_encode(p, k, self.k_codes, stream)
-        zb.zeta_sort_chunks(p, self.k_codes, self.prefix_codes, self.prefix_idx, self.sort_ws,
-                            stream)
-        zb.zeta_select_topk(p, self.q_codes, self.prefix_codes, self.prefix_idx, self.idx,
-                            stream)
+        if self.curves == 1:
+            zb.zeta_encode(p, q, self.q_codes, stream)
+            zb.zeta_encode(p, k, self.k_codes, stream)
+        else:
+            zb.zeta_encode_curves(p, q, self.axes, self.q_codes, stream)
+            zb.zeta_encode_curves(p, k, self.axes, self.k_codes, stream)
+        zb.zeta_sort_chunks(self.p_sort, self.k_codes, self.prefix_codes, self.prefix_idx,
+                            self.sort_ws, stream)
+        if self.curves == 1:
+            zb.zeta_select_topk(p, self.q_codes, self.prefix_codes, self.prefix_idx, self.idx,
+                                stream)
+        else:
+            zb.zeta_select_topk_curves(p, self.curves, self.q_codes, self.prefix_codes,
+                                       self.prefix_idx, self.idx, stream)
         zb.zeta_attend_fwd(p, q, k, v, gamma, self.idx, self.out, self.rowsum, self.status,
                            stream)
         return self.out, self.rowsum, self.idx
@@ -69,12 +90,12 @@ class ZetaAttention(torch.autograd.Function):
     """out = ZETA attention(q, k, v, gamma); q, k [B,H,N,d_K] f32, v [B,H,N,d_V]."""
 
     @staticmethod
-    def forward(ctx, q, k, v, gamma, C: int, k_sel: int, bits: int):
+    def forward(ctx, q, k, v, gamma, C: int, k_sel: int, bits: int, curves: int = 1):
         B, H, N, d_K = q.shape
         d_V = v.shape[-1]
         vd = "bf16" if v.dtype == torch.bfloat16 else "f32"
         p = zb.problem(B, H, N, d_K, d_V, k_sel, C, bits, vd)
-        plan = ZetaPlan(p, q.device)
+        plan = ZetaPlan(p, q.device, curves=curves)
         q, k, v, gamma = (t.contiguous() for t in (q, k, v, gamma))
         out, _, _ = plan.forward(q, k, v, gamma)
         ctx.plan = plan
@@ -86,8 +107,8 @@ class ZetaAttention(torch.autograd.Function):
         q, k, v, gamma = ctx.saved_tensors
         dq, dk, dv, dg = ctx.plan.backward(q, k, v, gamma, dout.contiguous().to(v.dtype))
         return (dq.view_as(q).clone(), dk.view_as(k).clone(), dv.view_as(v).clone(),
-                dg.clone(), None, None, None)
+                dg.clone(), None, None, None, None)
 
 
-def zeta_attention(q, k, v, gamma, C: int, k_sel: int, bits: int = 10):
-    return ZetaAttention.apply(q, k, v, gamma, C, k_sel, bits)
+def zeta_attention(q, k, v, gamma, C: int, k_sel: int, bits: int = 10, curves: int = 1):
+    return ZetaAttention.apply(q, k, v, gamma, C, k_sel, bits, curves)

@@ -115,3 +115,32 @@ def test_empty_problems_are_no_ops(L):
         assert L.zeta_encode(P, None, None, None) == 0
         assert L.zeta_select_topk(P, None, None, None, None, None) == 0
         assert L.zeta_attend_fwd(P, None, None, None, None, None, None, None, None, None) == 0
+
+
+def test_curve_calls_check_their_arguments(L):
+    p = _prob(k=16)
+    P = ctypes.byref(p)
+    fake = ctypes.c_void_p(0x1000)
+    Ax = ctypes.c_int32 * 24
+
+    def enc(curves, rows):
+        flat = [v for r in rows for v in r]
+        return L.zeta_encode_curves(P, fake, curves, Ax(*flat), fake, None)
+
+    assert enc(0, []) == 1                                      # no curve
+    assert enc(9, [[0, 1, 2]] * 8) == 1                         # above 8 curves
+    assert enc(2, [[0, 1, 2], [0, 0, 2]]) == 1                  # repeated axis
+    assert enc(1, [[0, 1, 3]]) == 1                             # axis out of range
+    assert L.zeta_encode_curves(P, fake, 3, None, fake, None) == 1
+    assert L.zeta_encode_curves(P, None, 1, Ax(0, 1, 2), fake, None) == 1
+    assert L.zeta_select_topk_curves(P, 0, fake, fake, fake, fake, None) == 1
+    assert L.zeta_select_topk_curves(P, 17, fake, fake, fake, fake, None) == 1  # k // 17 == 0
+    assert L.zeta_select_topk_curves(P, 3, fake, fake, fake, None, None) == 1
+    big = _prob(k=512, C=512)
+    assert L.zeta_select_topk_curves(ctypes.byref(big), 3, fake, fake, fake, fake, None) == 2
+    for kw in (dict(B=0), dict(N=0)):
+        e = _prob(**kw)
+        assert L.zeta_encode_curves(ctypes.byref(e), None, 3, Ax(0, 1, 2, 1, 2, 0, 2, 0, 1),
+                                    None, None) == 0
+        assert L.zeta_select_topk_curves(ctypes.byref(e), 3, None, None, None, None, None) == 0
+    assert zb.curve_axes(3, 6)[3] == [1, 0, 2]
