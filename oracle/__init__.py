@@ -52,8 +52,8 @@ def _load():
     lib.orc_prefix.argtypes = [P, I64, I64, P, P]
     lib.orc_prefix_table.argtypes = [P, I64, I64, P, P]
     lib.orc_select.argtypes = [P, P, I64, I64, I, P, I64, P]
-    lib.orc_attend_fwd.argtypes = [P, P, P, D, P, I64, I64, I, I, I, P, I64, P, P]
-    lib.orc_attend_bwd.argtypes = [P, P, P, D, P, P, I64, I64, I, I, I, P, P, P, P]
+    lib.orc_attend_fwd.argtypes = [P, P, P, D, P, I64, I64, I, I, I, P, I64, P, P, I]
+    lib.orc_attend_bwd.argtypes = [P, P, P, D, P, P, I64, I64, I, I, I, P, P, P, P, I]
     lib.orc_exact_topk.argtypes = [P, P, I64, I64, I, I, P, I64, P]
     lib.orc_encode_axes.argtypes = [P, I64, I, I, P, P]
     lib.orc_merge_windows.argtypes = [P, I, I, I, P]
@@ -190,9 +190,14 @@ def select(q_codes: np.ndarray, key_codes: np.ndarray, C: int, k: int, rows=None
 
 # ----------------------------------------------------------------- attend ---
 
-def attend_fwd(q, k, v, gamma: float, idx, C: int, rows=None):
+CAUCHY, SOFTMAX, INV_EUCLID = 0, 1, 2     # weight kernels (see zeta_oracle.c)
+
+
+def attend_fwd(q, k, v, gamma: float, idx, C: int, rows=None, kind: int = CAUCHY):
     """One slice.  q,k [N,d_K]; v [N,d_V] (any float dtype, taken as double);
     idx int32 [R,k], one row per listed query (all N when rows is None).
+    kind: CAUCHY, SOFTMAX (of -d2/gamma^2, rowsum taken with the row's
+    smallest d2 as shift) or INV_EUCLID.
     Returns (out [R,d_V] float64, rowsum [R] float64)."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     kx = np.ascontiguousarray(k, dtype=np.float64)
@@ -206,11 +211,11 @@ def attend_fwd(q, k, v, gamma: float, idx, C: int, rows=None):
     out = np.empty((cnt, d_V), dtype=np.float64)
     rs = np.empty((cnt,), dtype=np.float64)
     _load().orc_attend_fwd(_p(q), _p(kx), _p(v), float(gamma), _p(idx), N, C, d_K, d_V, kk,
-                           _p(r) if r is not None else None, nr, _p(out), _p(rs))
+                           _p(r) if r is not None else None, nr, _p(out), _p(rs), int(kind))
     return out, rs
 
 
-def attend_bwd(q, k, v, gamma: float, idx, dout, C: int):
+def attend_bwd(q, k, v, gamma: float, idx, dout, C: int, kind: int = CAUCHY):
     """One slice, selection fixed.  Returns (dq, dk, dv, dgamma) in float64."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     kx = np.ascontiguousarray(k, dtype=np.float64)
@@ -225,7 +230,7 @@ def attend_bwd(q, k, v, gamma: float, idx, dout, C: int):
     dv = np.empty_like(v)
     dg = np.zeros(1, dtype=np.float64)
     _load().orc_attend_bwd(_p(q), _p(kx), _p(v), float(gamma), _p(idx), _p(do), N, C, d_K, d_V,
-                           kk, _p(dq), _p(dk), _p(dv), _p(dg))
+                           kk, _p(dq), _p(dk), _p(dv), _p(dg), int(kind))
     return dq, dk, dv, float(dg[0])
 
 

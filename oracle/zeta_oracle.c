@@ -37,6 +37,8 @@
  *     sorted prefix of M = c*C keys (all M, padded with -1, when M < k);
  *   - every key j of the query's own chunk with j <= i joins the attended set;
  *   - Cauchy weight w = 1 / (1 + |q - k|^2 / gamma^2), normalised over the set;
+ *     the ablation kernels (softmax of -|q - k|^2 / gamma^2, inverse Euclidean
+ *     1 / sqrt(|q - k|^2 + 1e-12)) are described at orc_w below;
  *   - several curves [RB-asym]: curve m reads the coordinates in the order
  *     axes[m]; each curve's window holds k // curves keys (same centring rule);
  *     the union lists the windows in curve order, drops a key an earlier curve
@@ -167,12 +169,57 @@ void orc_select(const uint64_t *q_codes, const uint64_t *key_codes, int64_t N,
 
 /* ------------------------------------------------------------- attend --- */
 
-/* Cauchy weight of one (query, key) pair, [RB-cauchy]. */
-static double orc_weight(const double *q, const double *kk, int d_K, double gamma)
+/* Weight kernels of the attended set, [RB-cauchy] and the ablation in reply A3
+ * "Justification for Euclidean Distance Claim" (Cauchy softmax against
+ * negative Euclidean with the usual softmax and inverse Euclidean):
+ *   kind 0  Cauchy             w = 1 / (1 + d2 / gamma^2)
+ *   kind 1  softmax of -d2/gamma^2: w = exp(-(d2 - m) / gamma^2), m the row's
+ *           smallest d2 over the attended set (a shift that leaves w / sum w
+ *           unchanged and keeps the largest weight at 1)
+ *   kind 2  inverse Euclidean  w = 1 / sqrt(d2 + eps^2), eps = 1e-6
+ * d2 = |q - k|^2.  For each kind, dw/d(d2) and dw/dgamma (m held fixed, which
+ * changes no gradient because sum_j a_ij (g_ij - gbar_i) = 0). */
+#define ORC_INV_EPS2 1e-12
+
+static double orc_d2(const double *q, const double *kk, int d_K)
 {
     double d2 = 0.0;
     for (int d = 0; d < d_K; ++d) { double e = q[d] - kk[d]; d2 += e * e; }
+    return d2;
+}
+
+static double orc_w(int kind, double d2, double m, double gamma)
+{
+    if (kind == 1) return exp(-(d2 - m) / (gamma * gamma));
+    if (kind == 2) return 1.0 / sqrt(d2 + ORC_INV_EPS2);
     return 1.0 / (1.0 + d2 / (gamma * gamma));
+}
+
+static double orc_dw_dd2(int kind, double w, double gamma)
+{
+    if (kind == 1) return -w / (gamma * gamma);
+    if (kind == 2) return -0.5 * w * w * w;
+    return -w * w / (gamma * gamma);
+}
+
+static double orc_dw_dgamma(int kind, double w, double d2, double m, double gamma)
+{
+    if (kind == 1) return w * 2.0 * (d2 - m) / (gamma * gamma * gamma);
+    if (kind == 2) return 0.0;
+    return 2.0 * w * (1.0 - w) / gamma;
+}
+
+/* Row shift m of kind 1: the smallest d2 over the set (0 for the other kinds). */
+static double orc_shift(int kind, const double *qi, const double *kx, const int64_t *set,
+                        int64_t n, int d_K)
+{
+    if (kind != 1) return 0.0;
+    double m = INFINITY;
+    for (int64_t a = 0; a < n; ++a) {
+        double d2 = orc_d2(qi, kx + set[a] * d_K, d_K);
+        if (d2 < m) m = d2;
+    }
+    return m;
 }
 
 /* Attended set of query i: its window keys (non-negative entries of idx row)
@@ -191,19 +238,20 @@ static int64_t orc_set(const int32_t *idxrow, int k, int64_t i, int64_t C, int64
  * ([nrows][k], or [N][k] when rows == NULL); out: [nrows][d_V]; rowsum: [nrows]. */
 void orc_attend_fwd(const double *q, const double *kx, const double *v, double gamma,
                     const int32_t *idx, int64_t N, int64_t C, int d_K, int d_V, int k,
-                    const int64_t *rows, int64_t nrows, double *out, double *rowsum)
+                    const int64_t *rows, int64_t nrows, double *out, double *rowsum, int kind)
 {
     int64_t cnt = rows ? nrows : N;
     int64_t *set = (int64_t *)malloc((size_t)(k + C + 1) * sizeof(int64_t));
     for (int64_t t = 0; t < cnt; ++t) {
         int64_t i = rows ? rows[t] : t;
         int64_t m = orc_set(idx + t * k, k, i, C, set);
+        double sh = orc_shift(kind, q + i * d_K, kx, set, m, d_K);
         double s = 0.0;
         double *o = out + t * d_V;
         for (int e = 0; e < d_V; ++e) o[e] = 0.0;
         for (int64_t a = 0; a < m; ++a) {
             int64_t j = set[a];
-            double w = orc_weight(q + i * d_K, kx + j * d_K, d_K, gamma);
+            double w = orc_w(kind, orc_d2(q + i * d_K, kx + j * d_K, d_K), sh, gamma);
             s += w;
             for (int e = 0; e < d_V; ++e) o[e] += w * v[j * d_V + e];
         }
@@ -216,14 +264,14 @@ void orc_attend_fwd(const double *q, const double *kx, const double *v, double g
 /* Backward for one slice with the selection held fixed.  With a_ij = w_ij / s_i,
  * g_ij = dO_i . v_j and gbar_i = dO_i . o_i:
  *   dL/dw_ij   = (g_ij - gbar_i) / s_i
- *   dw/d(d^2)  = -w^2 / gamma^2,        dw/dgamma = 2 w (1 - w) / gamma
- *   dq_i  += dL/dw_ij * (-2 w_ij^2 / gamma^2) (q_i - k_j),  dk_j gets the negation
- *   dv_j  += a_ij dO_i,                  dgamma += dL/dw_ij * 2 w_ij (1 - w_ij) / gamma
+ *   dq_i  += dL/dw_ij * dw/d(d2) * 2 (q_i - k_j),  dk_j gets the negation
+ *   dv_j  += a_ij dO_i,                  dgamma += dL/dw_ij * dw/dgamma
+ * (Cauchy: dw/d(d2) = -w^2 / gamma^2, dw/dgamma = 2 w (1 - w) / gamma.)
  * Outputs are overwritten.  dgamma is this slice's sum. */
 void orc_attend_bwd(const double *q, const double *kx, const double *v, double gamma,
                     const int32_t *idx, const double *dout, int64_t N, int64_t C,
                     int d_K, int d_V, int k,
-                    double *dq, double *dk, double *dv, double *dgamma)
+                    double *dq, double *dk, double *dv, double *dgamma, int kind)
 {
     int64_t *set = (int64_t *)malloc((size_t)(k + C + 1) * sizeof(int64_t));
     double *w = (double *)malloc((size_t)(k + C + 1) * sizeof(double));
@@ -232,16 +280,16 @@ void orc_attend_bwd(const double *q, const double *kx, const double *v, double g
     memset(dk, 0, (size_t)N * d_K * sizeof(double));
     memset(dv, 0, (size_t)N * d_V * sizeof(double));
     double dg = 0.0;
-    double g2 = gamma * gamma;
     for (int64_t i = 0; i < N; ++i) {
         int64_t m = orc_set(idx + i * k, k, i, C, set);
         const double *qi = q + i * d_K;
         const double *doi = dout + i * d_V;
+        double sh = orc_shift(kind, qi, kx, set, m, d_K);
         double s = 0.0;
         for (int e = 0; e < d_V; ++e) o[e] = 0.0;
         for (int64_t a = 0; a < m; ++a) {
             int64_t j = set[a];
-            w[a] = orc_weight(qi, kx + j * d_K, d_K, gamma);
+            w[a] = orc_w(kind, orc_d2(qi, kx + j * d_K, d_K), sh, gamma);
             s += w[a];
             for (int e = 0; e < d_V; ++e) o[e] += w[a] * v[j * d_V + e];
         }
@@ -254,7 +302,8 @@ void orc_attend_bwd(const double *q, const double *kx, const double *v, double g
             double g = 0.0;
             for (int e = 0; e < d_V; ++e) g += doi[e] * v[j * d_V + e];
             double dldw = (g - gbar) / s;
-            double coef = dldw * (-2.0 * w[a] * w[a] / g2);
+            /* d(d2)/dq_i = 2 (q_i - k_j) = -d(d2)/dk_j */
+            double coef = dldw * orc_dw_dd2(kind, w[a], gamma) * 2.0;
             for (int d = 0; d < d_K; ++d) {
                 double term = coef * (qi[d] - kj[d]);
                 dq[i * d_K + d] += term;
@@ -262,7 +311,7 @@ void orc_attend_bwd(const double *q, const double *kx, const double *v, double g
             }
             double aij = w[a] / s;
             for (int e = 0; e < d_V; ++e) dv[j * d_V + e] += aij * doi[e];
-            dg += dldw * 2.0 * w[a] * (1.0 - w[a]) / gamma;
+            dg += dldw * orc_dw_dgamma(kind, w[a], orc_d2(qi, kj, d_K), sh, gamma);
         }
     }
     *dgamma = dg;
