@@ -50,9 +50,26 @@ typedef enum {
 
 typedef enum { ZETA_F32 = 0, ZETA_BF16 = 1 } zeta_dtype_t;
 
+/* Weight kernel of the attended set, in the low two bits of
+ * zeta_problem_t.flags (d2 = |q_i - k_j|^2, a_ij = w_ij / s_i, s_i = sum_j w_ij):
+ *   ZETA_W_CAUCHY      w = 1 / (1 + d2 / gamma^2): the method's Adaptive
+ *                      Cauchy softmax (OpenReview reply A2 "Discussion on its
+ *                      robustness").
+ *   ZETA_W_SOFTMAX     w = exp(-(d2 - m_i) / gamma^2), m_i the smallest d2 of
+ *                      query i's attended set: the usual softmax of
+ *                      -d2 / gamma^2 ("negative Euclidean with traditional
+ *                      softmax", reply A3 "Justification for Euclidean
+ *                      Distance Claim"); rowsum_i is s_i with that shift.
+ *   ZETA_W_INV_EUCLID  w = 1 / sqrt(d2 + 1e-12): inverse Euclidean distance
+ *                      (same reply); gamma does not enter, dgamma is 0.
+ * The squared distance inside the softmax and the 1e-12 guard are readings:
+ * the pages name the kernels without formulas. */
+typedef enum { ZETA_W_CAUCHY = 0, ZETA_W_SOFTMAX = 1, ZETA_W_INV_EUCLID = 2 } zeta_weight_t;
+
 /* Problem statement: B batch, H heads, N tokens, d_K query/key width, d_V value
  * width, k window length, C chunk length, bits grid bits per coordinate,
- * v_dtype element type of v / out / dout / dv, flags reserved (pass 0).
+ * v_dtype element type of v / out / dout / dv, flags: bits 0-1 the weight
+ * kernel (zeta_weight_t), other bits reserved (pass 0).
  * These are the quantities the pages use to state the method: the 12-bit grid
  * and d_K = 3 (OpenReview reply A2 "Clarification of Binary Expansion and
  * Precision"), the chunk count and d_K = d_Q = 3 (reply A2 "Details about
@@ -202,7 +219,8 @@ zeta_status_t zeta_select_topk_curves(const zeta_problem_t *p, int32_t curves,
  * the atlas.scime.ai summary, "Approach".
  * The attended set of query i in chunk c is its window (non-negative entries
  * of idx row i) plus every key j of its own chunk with cC <= j <= i.  With
- * w_ij = 1 / (1 + |q_i - k_j|^2 / gamma_h^2) and s_i = sum_j w_ij:
+ * w_ij = 1 / (1 + |q_i - k_j|^2 / gamma_h^2) (or the kernel that flags
+ * selects, see zeta_weight_t) and s_i = sum_j w_ij:
  * out_i = sum_j w_ij v_j / s_i, rowsum_i = s_i.
  *   q, k    in : float [B, H, N, d_K]
  *   v       in : v_dtype [B, H, N, d_V]  (16-B aligned)
@@ -220,16 +238,19 @@ zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, const flo
                               cudaStream_t stream);
 
 /*
- * zeta_attend_bwd -- gradients through the Cauchy weights, selection fixed.
+ * zeta_attend_bwd -- gradients through the weights, selection fixed.
  * Passage: the forward/backward timings of the OpenReview replies A3/A4 (the
  * method is trained end to end) and the forward definition above.
  * With a_ij = w_ij / s_i, g_ij = dO_i . v_j and gbar_i = sum_j a_ij g_ij
  * (= dO_i . out_i for the exact output):
  *   dL/dw_ij = (g_ij - gbar_i) / s_i
- *   dq_i     = sum_j dL/dw_ij * (-2 w_ij^2 / gamma^2) (q_i - k_j)
- *   dk_j     = sum_i dL/dw_ij * ( 2 w_ij^2 / gamma^2) (q_i - k_j)
+ *   dq_i     = sum_j dL/dw_ij * 2 (dw/dd2)_ij (q_i - k_j)
+ *   dk_j     = -sum_i dL/dw_ij * 2 (dw/dd2)_ij (q_i - k_j)
  *   dv_j     = sum_i a_ij dO_i
- *   dgamma_h = sum_{b,i,j} dL/dw_ij * 2 w_ij (1 - w_ij) / gamma_h
+ *   dgamma_h = sum_{b,i,j} dL/dw_ij * (dw/dgamma)_ij
+ * with, per weight kernel, dw/dd2 = -w^2/gamma^2 and dw/dgamma =
+ * 2 w (1 - w) / gamma (Cauchy); -w/gamma^2 and 2 w (d2 - m_i) / gamma^3
+ * (softmax); -w^3/2 and 0 (inverse Euclidean).
  * s_i and gbar_i are recomputed from q, k, v and idx (one pass over each
  * query's set), so the forward's rounded output is not needed.
  *   q, k, v, gamma, idx  in : as for zeta_attend_fwd

@@ -19,6 +19,10 @@ from . import build as _build
 ZETA_F32 = 0
 ZETA_BF16 = 1
 
+# Weight kernels (low bits of zeta_problem_t.flags).
+ZETA_W_CAUCHY, ZETA_W_SOFTMAX, ZETA_W_INV_EUCLID = 0, 1, 2
+WEIGHTS = {"cauchy": ZETA_W_CAUCHY, "softmax": ZETA_W_SOFTMAX, "inv_euclid": ZETA_W_INV_EUCLID}
+
 STATUS = {
     0: "ZETA_OK", 1: "ZETA_ERR_INVALID_ARG", 2: "ZETA_ERR_UNSUPPORTED", 3: "ZETA_ERR_WORKSPACE",
     4: "ZETA_ERR_CUDA", 5: "ZETA_ERR_DEVICE_TIMEOUT", 6: "ZETA_ERR_BOUNDS",
@@ -40,14 +44,16 @@ class zeta_problem_t(ctypes.Structure):
                 ("flags", ctypes.c_uint32)]
 
 
-def problem(B, H, N, d_K, d_V, k, C, bits, v_dtype="bf16", flags=0) -> zeta_problem_t:
+def problem(B, H, N, d_K, d_V, k, C, bits, v_dtype="bf16", flags=0,
+            weight="cauchy") -> zeta_problem_t:
+    """flags: raw flag bits; weight: 'cauchy', 'softmax' or 'inv_euclid' (ORed in)."""
     vd = {"f32": ZETA_F32, "bf16": ZETA_BF16, ZETA_F32: ZETA_F32, ZETA_BF16: ZETA_BF16}[v_dtype]
-    return zeta_problem_t(B, H, N, d_K, d_V, k, C, bits, vd, flags)
+    return zeta_problem_t(B, H, N, d_K, d_V, k, C, bits, vd, flags | WEIGHTS[weight])
 
 
-def problem_of(w) -> zeta_problem_t:
+def problem_of(w, weight="cauchy") -> zeta_problem_t:
     """Problem struct of a workloads.Workload."""
-    return problem(w.B, w.H, w.N, w.d_K, w.d_V, w.k, w.C, w.bits, w.v_dtype)
+    return problem(w.B, w.H, w.N, w.d_K, w.d_V, w.k, w.C, w.bits, w.v_dtype, weight=weight)
 
 
 _lib = None

@@ -22,7 +22,7 @@ zeta_status_t check_problem(const zeta_problem_t *pp, Prob *out) {
     if (p.N % p.C != 0) return ZETA_ERR_INVALID_ARG;
     if (p.k > p.C) return ZETA_ERR_INVALID_ARG;
     if (p.v_dtype != ZETA_F32 && p.v_dtype != ZETA_BF16) return ZETA_ERR_INVALID_ARG;
-    if (p.flags != 0) return ZETA_ERR_UNSUPPORTED;
+    if ((p.flags & ~3u) != 0 || (p.flags & 3u) == 3u) return ZETA_ERR_UNSUPPORTED;
     const int64_t S = (int64_t)p.B * p.H;
     if (S > 65535) return ZETA_ERR_UNSUPPORTED;            // slices ride on gridDim.y
     if ((int64_t)p.N * p.k > INT32_MAX) return ZETA_ERR_UNSUPPORTED;
@@ -33,6 +33,7 @@ zeta_status_t check_problem(const zeta_problem_t *pp, Prob *out) {
     r.n = p.N / p.C;
     r.T = (int64_t)p.C * r.n * (r.n - 1) / 2;
     r.code64 = p.d_K * p.bits > 32;
+    r.wk = (int)(p.flags & 3u);
     *out = r;
     return ZETA_OK;
 }

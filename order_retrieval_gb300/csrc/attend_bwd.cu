@@ -8,7 +8,9 @@
 //
 // With a_ij = w_ij / s_i, g_ij = dO_i . v_j, gbar_i = sum_j a_ij g_ij:
 //   dL/dw_ij = (g_ij - gbar_i) / s_i,   dw/d(d^2) = -w^2 / gamma^2,
-//   dw/dgamma = 2 w (1 - w) / gamma.
+//   dw/dgamma = 2 w (1 - w) / gamma  (Cauchy; the other weight kernels swap in
+//   their own dw/d(d^2) and dw/dgamma, common.cuh, and the softmax first finds
+//   its shift, the smallest d^2 of the set, which the key side reads back).
 // Query side (one warp per query): s_i, gbar_i, dq_i and the query's share
 // of dgamma.  Key side (one warp per key): dv_j and dk_j, reducing over the
 // queries that selected j.  Those are found through a transpose of idx built
@@ -47,21 +49,21 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 // ---------------------------------------------------------- query side ---
-// One pass over the attended set of query i.  With c_ij = -2 w^2 / gamma^2 and
-// e_ij = 2 w (1 - w) / gamma, and dL/dw_ij = (g_ij - gbar_i) / s_i:
+// One pass over the attended set of query i.  With c_ij = 2 dw/d(d^2) and
+// e_ij = dw/dgamma, and dL/dw_ij = (g_ij - gbar_i) / s_i:
 //   s      = sum w,          G  = sum w g        -> gbar = G / s
 //   A_d    = sum g c (q-k)_d, Bd = sum c (q-k)_d -> dq_d  = (A_d - gbar Bd) / s
 //   E1     = sum g e,        E2 = sum e          -> dgamma_i = (E1 - gbar E2) / s
 // so gbar is exact (from the values themselves, not the rounded output).
 
-template <typename V, int VPL>
+template <typename V, int VPL, int WK>
 __global__ void __launch_bounds__(256)
 bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
                   const V *__restrict__ v, const float *__restrict__ gamma,
                   const int32_t *__restrict__ idx, const V *__restrict__ dout,
                   float *__restrict__ dq, float *__restrict__ s_out, float *__restrict__ gbar_out,
-                  float *__restrict__ dg_part, int32_t *status, int64_t S, int N, int H, int dK,
-                  int dV, int k, int C) {
+                  float *__restrict__ m_out, float *__restrict__ dg_part, int32_t *status,
+                  int64_t S, int N, int H, int dK, int dV, int k, int C) {
     __shared__ float sdo[8][kMaxDV];
     const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
     if (gw >= S * N) return;
@@ -84,12 +86,26 @@ bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
 #pragma unroll
     for (int d = 0; d < kMaxDK; ++d) A[d] = Bd[d] = 0.f;
     float sw = 0.f, G = 0.f, E1 = 0.f, E2 = 0.f;
+    const int32_t *irow = idx + row * (int64_t)k;
+    float m = 0.f;                                 // softmax shift: min d2 of the set
+    if constexpr (WK == kWSoftmax) {
+        float mn = INFINITY;
+        for (int t = lane; t < k; t += 32) {
+            const int j = irow[t];
+            if (j >= 0 && j < cC) mn = fminf(mn, dist2b(qi, kb + (int64_t)j * dK, dK));
+        }
+        for (int j = cC + lane; j <= i; j += 32)
+            mn = fminf(mn, dist2b(qi, kb + (int64_t)j * dK, dK));
+        for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+        m = mn;
+    }
     auto visit = [&](int j) {
         const float *kj = kb + (int64_t)j * dK;
-        const float w = cauchy_w(dist2b(qi, kj, dK), inv_g2);
+        const float d2 = dist2b(qi, kj, dK);
+        const float w = weight_of<WK>(d2, m, inv_g2);
         const float gij = dot_row<V>(sdo[wib], vb + (int64_t)j * dV, dV);
-        const float c = -2.f * w * w * inv_g2;
-        const float e = 2.f * w * (1.f - w) * inv_g;
+        const float c = -2.f * neg_dw_dd2<WK>(w, inv_g2);
+        const float e = dw_dgamma<WK>(w, d2, m, inv_g2, inv_g);
         sw += w;
         G = __fmaf_rn(w, gij, G);
         E1 = __fmaf_rn(gij, e, E1);
@@ -102,7 +118,6 @@ bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
                 Bd[d] += t;
             }
     };
-    const int32_t *irow = idx + row * (int64_t)k;
     for (int t = lane; t < k; t += 32) {
         int j = irow[t];
         if (j == -1) continue;
@@ -125,6 +140,7 @@ bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
         for (int d = 0; d < dK; ++d) dq[row * dK + d] = (A[d] - gb * Bd[d]) * inv_s;
         s_out[row] = sw;
         gbar_out[row] = gb;
+        m_out[row] = m;
         dg_part[row] = (E1 - gb * E2) * inv_s;
     }
 }
@@ -147,12 +163,13 @@ __global__ void csr_offsets(const uint32_t *__restrict__ skeys, const uint32_t *
     }
 }
 
-template <typename V, int VPL>
+template <typename V, int VPL, int WK>
 __global__ void __launch_bounds__(256)
 bwd_key_generic(const float *__restrict__ q, const float *__restrict__ kx,
                 const V *__restrict__ v, const float *__restrict__ gamma,
                 const float *__restrict__ rowsum, const V *__restrict__ dout,
-                const float *__restrict__ gbar, const uint32_t *__restrict__ csr_q,
+                const float *__restrict__ gbar, const float *__restrict__ shift,
+                const uint32_t *__restrict__ csr_q,
                 const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
                 V *__restrict__ dv, int64_t S, int N, int H, int dK, int dV, int C) {
     __shared__ float sv[8][kMaxDV];
@@ -184,12 +201,12 @@ bwd_key_generic(const float *__restrict__ q, const float *__restrict__ kx,
         float a = 0.f;
         if (i >= 0) {
             const float *qi = qb + (int64_t)i * dK;
-            const float w = cauchy_w(dist2b(qi, kj, dK), inv_g2);
+            const float w = weight_of<WK>(dist2b(qi, kj, dK), shift[seg * N + i], inv_g2);
             const float inv_s = __frcp_rn(rs[i]);
             a = w * inv_s;
             const float gij = dot_row<V>(sv[wib], dob + (int64_t)i * dV, dV);
             const float dldw = (gij - gbb[i]) * inv_s;
-            const float coef = dldw * (2.f * w * w * inv_g2);
+            const float coef = dldw * (2.f * neg_dw_dd2<WK>(w, inv_g2));
 #pragma unroll
             for (int d = 0; d < kMaxDK; ++d)
                 if (d < dK) dka[d] = __fmaf_rn(coef, qi[d] - kj[d], dka[d]);
@@ -257,6 +274,7 @@ __global__ void dgamma_heads(const double *__restrict__ slice_sum, int B, int H,
 struct BwdWs {
     float *s;
     float *gbar;
+    float *m;
     float *dgp;
     void *rec;
     double *slice_sum;
@@ -271,6 +289,7 @@ BwdWs carve_bwd(const Prob &p, void *base, size_t *bytes) {
     const int64_t L = p.N * (int64_t)p.k;
     w.s = cv.take<float>(rows);
     w.gbar = cv.take<float>(rows);
+    w.m = cv.take<float>(rows);
     w.dgp = cv.take<float>(rows);
     w.rec = cv.take<char>(bwd_tc_rec_bytes(p));
     w.slice_sum = cv.take<double>(p.S);
@@ -290,7 +309,7 @@ void dgamma_reduce(const Prob &p, const BwdWs &w, float *dgamma, cudaStream_t st
     dgamma_heads<<<(unsigned)((p.H + 127) / 128), 128, 0, st>>>(w.slice_sum, p.B, p.H, dgamma);
 }
 
-template <typename V, int VPL>
+template <typename V, int VPL, int WK>
 cudaError_t bwd_generic(const Prob &p, const float *q, const float *k, const void *v,
                         const float *gamma, const int32_t *idx, const void *dout, float *dq,
                         float *dk, void *dv, float *dgamma, void *ws, int32_t *status,
@@ -298,17 +317,17 @@ cudaError_t bwd_generic(const Prob &p, const float *q, const float *k, const voi
     BwdWs w = carve_bwd(p, ws, nullptr);
     const int64_t warps = p.S * p.N;
     const unsigned blocks = (unsigned)((warps + 7) / 8);
-    bwd_query_generic<V, VPL><<<blocks, 256, 0, st>>>(
+    bwd_query_generic<V, VPL, WK><<<blocks, 256, 0, st>>>(
         q, k, static_cast<const V *>(v), gamma, idx, static_cast<const V *>(dout), dq, w.s,
-        w.gbar, w.dgp, status, p.S, p.N, p.H, p.dK, p.dV, p.k, p.C);
+        w.gbar, w.m, w.dgp, status, p.S, p.N, p.H, p.dK, p.dV, p.k, p.C);
     int ob = 0;
     cudaError_t e = radix_sort_idx(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st);
     if (e != cudaSuccess) return e;
     const int64_t L = p.N * (int64_t)p.k;
     csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(
         static_cast<const uint32_t *>(w.rw.keys[ob]), w.rw.seglen, L, p.N, 0, w.off);
-    bwd_key_generic<V, VPL><<<blocks, 256, 0, st>>>(
-        q, k, static_cast<const V *>(v), gamma, w.s, static_cast<const V *>(dout), w.gbar,
+    bwd_key_generic<V, VPL, WK><<<blocks, 256, 0, st>>>(
+        q, k, static_cast<const V *>(v), gamma, w.s, static_cast<const V *>(dout), w.gbar, w.m,
         w.rw.vals[ob], w.off, L, dk, static_cast<V *>(dv), p.S, p.N, p.H, p.dK, p.dV, p.C);
     dgamma_reduce(p, w, dgamma, st);
     return cudaGetLastError();
@@ -319,11 +338,24 @@ cudaError_t bwd_dispatch(const Prob &p, const float *q, const float *k, const vo
                          const float *gamma, const int32_t *idx, const void *dout, float *dq,
                          float *dk, void *dv, float *dgamma, void *ws, int32_t *status,
                          cudaStream_t st) {
-#define ZETA_BWD(VPL) \
-    return bwd_generic<V, VPL>(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, ws, status, st)
-    if (p.dV <= 32) ZETA_BWD(1);
-    if (p.dV <= 64) ZETA_BWD(2);
-    if (p.dV <= 128) ZETA_BWD(4);
+#define ZETA_BWD(VPL)                                                                        \
+    if (p.wk == kWSoftmax)                                                                   \
+        return bwd_generic<V, VPL, kWSoftmax>(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, \
+                                              ws, status, st);                               \
+    if (p.wk == kWInvEuclid)                                                                 \
+        return bwd_generic<V, VPL, kWInvEuclid>(p, q, k, v, gamma, idx, dout, dq, dk, dv,     \
+                                                dgamma, ws, status, st);                     \
+    return bwd_generic<V, VPL, kWCauchy>(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, ws, \
+                                         status, st)
+    if (p.dV <= 32) {
+        ZETA_BWD(1);
+    }
+    if (p.dV <= 64) {
+        ZETA_BWD(2);
+    }
+    if (p.dV <= 128) {
+        ZETA_BWD(4);
+    }
     ZETA_BWD(8);
 #undef ZETA_BWD
 }

@@ -725,7 +725,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
 }  // namespace
 
 bool attend_bwd_tc_supported(const Prob &p) {
-    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4;
+    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4 && p.wk == kWCauchy;
 }
 
 size_t bwd_tc_rec_bytes(const Prob &p) { return sizeof(QRec) * (size_t)(p.S * p.N); }

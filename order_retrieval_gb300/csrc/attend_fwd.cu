@@ -10,8 +10,9 @@
 // plus every own-chunk key j with cC <= j <= i.
 //   w_ij = 1 / (1 + |q_i - k_j|^2 / gamma_h^2),  s_i = sum_j w_ij,
 //   out_i = sum_j w_ij v_j / s_i,                rowsum_i = s_i.
-// Weights lie in (0, 1], so no running maximum is needed and partial sums of
-// the window part and the own-chunk part simply add.
+// Other weight kernels (flags): softmax of -d2 / gamma^2 and inverse Euclidean
+// (reply A3 "Justification for Euclidean Distance Claim"); the softmax takes
+// its shift, the smallest d2 of the set, in a first pass over the keys.
 //
 // Generic path: one warp per query, one key per lane for the weights, then the
 // warp walks the 32 keys with lanes spread over the value columns.  Any d_V up
@@ -60,7 +61,7 @@ __device__ __forceinline__ float dist2(const float *qi, const float *kj, int dK)
     return d2;
 }
 
-template <typename V, int VPL>
+template <typename V, int VPL, int WK>
 __global__ void __launch_bounds__(256)
 attend_fwd_generic(const float *__restrict__ q, const float *__restrict__ kx,
                    const V *__restrict__ v, const float *__restrict__ gamma,
@@ -83,6 +84,17 @@ attend_fwd_generic(const float *__restrict__ q, const float *__restrict__ kx,
     FwdAcc<V, VPL> a;
     a.zero();
     const int32_t *irow = idx + (seg * N + i) * (int64_t)k;
+    float m = 0.f;                                 // softmax shift: min d2 of the set
+    if constexpr (WK == kWSoftmax) {
+        float mn = INFINITY;
+        for (int t = lane; t < k; t += 32) {
+            const int j = irow[t];
+            if (j >= 0 && j < cC) mn = fminf(mn, dist2(qi, kb + (int64_t)j * dK, dK));
+        }
+        for (int j = cC + lane; j <= i; j += 32) mn = fminf(mn, dist2(qi, kb + (int64_t)j * dK, dK));
+        for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+        m = mn;
+    }
     for (int t0 = 0; t0 < k; t0 += 32) {
         const int t = t0 + lane;
         int j = -1;
@@ -93,12 +105,14 @@ attend_fwd_generic(const float *__restrict__ q, const float *__restrict__ kx,
                 j = -1;
             }
         }
-        const float w = j >= 0 ? cauchy_w(dist2(qi, kb + (int64_t)j * dK, dK), inv_g2) : 0.f;
+        const float w = j >= 0 ? weight_of<WK>(dist2(qi, kb + (int64_t)j * dK, dK), m, inv_g2)
+                               : 0.f;
         a.add32(w, j, vb, dV, lane);
     }
     for (int j0 = cC; j0 <= i; j0 += 32) {
         const int j = j0 + lane <= i ? j0 + lane : -1;
-        const float w = j >= 0 ? cauchy_w(dist2(qi, kb + (int64_t)j * dK, dK), inv_g2) : 0.f;
+        const float w = j >= 0 ? weight_of<WK>(dist2(qi, kb + (int64_t)j * dK, dK), m, inv_g2)
+                               : 0.f;
         a.add32(w, j, vb, dV, lane);
     }
     float s = a.s;
@@ -118,9 +132,14 @@ cudaError_t fwd_generic(const Prob &p, const float *q, const float *k, const voi
                         int32_t *status, cudaStream_t st) {
     const int64_t warps = p.S * p.N;
     const int64_t blocks = (warps + 7) / 8;
-    attend_fwd_generic<V, VPL><<<(unsigned)blocks, 256, 0, st>>>(
-        q, k, static_cast<const V *>(v), gamma, idx, static_cast<V *>(out), rowsum, status, p.S,
-        p.N, p.H, p.dK, p.dV, p.k, p.C);
+#define ZETA_FWD_G(WK)                                                                        \
+    attend_fwd_generic<V, VPL, WK><<<(unsigned)blocks, 256, 0, st>>>(                         \
+        q, k, static_cast<const V *>(v), gamma, idx, static_cast<V *>(out), rowsum, status, p.S, \
+        p.N, p.H, p.dK, p.dV, p.k, p.C)
+    if (p.wk == kWSoftmax) ZETA_FWD_G(kWSoftmax);
+    else if (p.wk == kWInvEuclid) ZETA_FWD_G(kWInvEuclid);
+    else ZETA_FWD_G(kWCauchy);
+#undef ZETA_FWD_G
     return cudaGetLastError();
 }
 

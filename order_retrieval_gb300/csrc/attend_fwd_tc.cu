@@ -322,7 +322,7 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
 }  // namespace
 
 bool attend_fwd_tc_supported(const Prob &p) {
-    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4;
+    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4 && p.wk == kWCauchy;
 }
 
 cudaError_t launch_attend_fwd_tc(const Prob &p, const float *q, const float *k, const void *v,

@@ -26,6 +26,7 @@ struct Prob {
     int64_t n;        // chunks N / C
     int64_t T;        // prefix entries per slice
     int code64;       // 1 when d_K*bits > 32
+    int wk;           // weight kernel (kWCauchy, kWSoftmax, kWInvEuclid)
 };
 
 // Record the first device-side error in an optional status word.
@@ -53,6 +54,39 @@ template <> struct VT<__nv_bfloat16> {
 // reciprocal.
 __device__ __forceinline__ float cauchy_w(float d2, float inv_g2) {
     return __frcp_rn(__fmaf_rn(d2, inv_g2, 1.0f));
+}
+
+// Weight kernels of the attended set (the low bits of zeta_problem_t.flags):
+// the Cauchy softmax of the method, and the two kernels it is compared with in
+// the OpenReview discussion, reply A3 "Justification for Euclidean Distance
+// Claim": softmax of -d2 / gamma^2 (weights exp((m - d2) / gamma^2) with a
+// per-query shift m = the smallest d2 of the attended set, which leaves the
+// normalised weights unchanged) and inverse Euclidean 1 / sqrt(d2 + 1e-12).
+constexpr int kWCauchy = 0, kWSoftmax = 1, kWInvEuclid = 2;
+constexpr float kInvEps2 = 1e-12f;
+
+template <int WK>
+__device__ __forceinline__ float weight_of(float d2, float m, float inv_g2) {
+    if constexpr (WK == kWSoftmax) return expf((m - d2) * inv_g2);
+    else if constexpr (WK == kWInvEuclid) return __frsqrt_rn(d2 + kInvEps2);
+    else return cauchy_w(d2, inv_g2);
+}
+
+// -dw/d(d2) as a function of the weight.
+template <int WK>
+__device__ __forceinline__ float neg_dw_dd2(float w, float inv_g2) {
+    if constexpr (WK == kWSoftmax) return w * inv_g2;
+    else if constexpr (WK == kWInvEuclid) return 0.5f * w * w * w;
+    else return w * w * inv_g2;
+}
+
+// dw/dgamma (for the softmax with the shift held fixed; the shift's own
+// derivative cancels in the normalised weights).
+template <int WK>
+__device__ __forceinline__ float dw_dgamma(float w, float d2, float m, float inv_g2, float inv_g) {
+    if constexpr (WK == kWSoftmax) return 2.f * w * (d2 - m) * inv_g2 * inv_g;
+    else if constexpr (WK == kWInvEuclid) return 0.f;
+    else return 2.f * w * (1.f - w) * inv_g;
 }
 
 // ----------------------------------------------------------- launchers ---

@@ -27,7 +27,7 @@ class ZetaPlan:
         self.axes = zb.curve_axes(p.d_K, curves)
         # Every curve's slices sort as one problem with curves*B batches.
         self.p_sort = zb.problem(p.B * curves, p.H, p.N, p.d_K, p.d_V, p.k, p.C, p.bits,
-                                 p.v_dtype) if curves > 1 else p
+                                 p.v_dtype, flags=p.flags) if curves > 1 else p
         dev = torch.device(device)
         S = p.B * p.H
         N = p.N
@@ -90,11 +90,12 @@ class ZetaAttention(torch.autograd.Function):
     """out = ZETA attention(q, k, v, gamma); q, k [B,H,N,d_K] f32, v [B,H,N,d_V]."""
 
     @staticmethod
-    def forward(ctx, q, k, v, gamma, C: int, k_sel: int, bits: int, curves: int = 1):
+    def forward(ctx, q, k, v, gamma, C: int, k_sel: int, bits: int, curves: int = 1,
+                weight: str = "cauchy"):
         B, H, N, d_K = q.shape
         d_V = v.shape[-1]
         vd = "bf16" if v.dtype == torch.bfloat16 else "f32"
-        p = zb.problem(B, H, N, d_K, d_V, k_sel, C, bits, vd)
+        p = zb.problem(B, H, N, d_K, d_V, k_sel, C, bits, vd, weight=weight)
         plan = ZetaPlan(p, q.device, curves=curves)
         q, k, v, gamma = (t.contiguous() for t in (q, k, v, gamma))
         out, _, _ = plan.forward(q, k, v, gamma)
@@ -107,8 +108,11 @@ class ZetaAttention(torch.autograd.Function):
         q, k, v, gamma = ctx.saved_tensors
         dq, dk, dv, dg = ctx.plan.backward(q, k, v, gamma, dout.contiguous().to(v.dtype))
         return (dq.view_as(q).clone(), dk.view_as(k).clone(), dv.view_as(v).clone(),
-                dg.clone(), None, None, None, None)
+                dg.clone(), None, None, None, None, None)
 
 
-def zeta_attention(q, k, v, gamma, C: int, k_sel: int, bits: int = 10, curves: int = 1):
-    return ZetaAttention.apply(q, k, v, gamma, C, k_sel, bits, curves)
+def zeta_attention(q, k, v, gamma, C: int, k_sel: int, bits: int = 10, curves: int = 1,
+                   weight: str = "cauchy"):
+    """weight: 'cauchy' (the method), 'softmax' (of -|q-k|^2/gamma^2) or
+    'inv_euclid' (1/|q-k|); see zeta_weight_t in include/zeta.h."""
+    return ZetaAttention.apply(q, k, v, gamma, C, k_sel, bits, curves, weight)

@@ -30,10 +30,10 @@ def codes_np(t):
 class Run:
     """Device tensors and results of one forward (and optional backward)."""
 
-    def __init__(self, w, g=None, backward=False, dout=None):
+    def __init__(self, w, g=None, backward=False, dout=None, weight="cauchy"):
         self.w = w
         self.g = g if g is not None else W.generate(w, with_dout=backward)
-        self.p = zb.problem_of(w)
+        self.p = zb.problem_of(w, weight=weight)
         S, N = w.B * w.H, w.N
         self.q = torch.from_numpy(self.g["q"]).cuda().reshape(-1)
         self.k = torch.from_numpy(self.g["k"]).cuda().reshape(-1)

@@ -52,7 +52,8 @@ BAD = [
     dict(d_K=8, bits=9),          # 72-bit code
     dict(B=-1), dict(v_dtype=7),
 ]
-UNSUP = [dict(d_K=9, bits=7), dict(bits=25, d_K=2), dict(d_V=512), dict(flags=1)]
+UNSUP = [dict(d_K=9, bits=7), dict(bits=25, d_K=2), dict(d_V=512), dict(flags=3),
+         dict(flags=4)]
 
 
 def _prob(**kw):
@@ -106,6 +107,13 @@ def test_null_pointers_and_workspace(L):
     # Too many chunks for the prefix builder.
     many = _prob(N=4096, C=2, k=2)
     assert L.zeta_sort_chunks(ctypes.byref(many), fake, fake, fake, fake, 1 << 40, None) == 2
+
+
+def test_weight_kernels_are_accepted(L):
+    for wk in ("cauchy", "softmax", "inv_euclid"):
+        p = zb.problem(1, 2, 1024, 3, 32, 16, 128, 10, "f32", weight=wk)
+        assert L.zeta_prefix_entries(ctypes.byref(p)) > 0
+        assert zb.zeta_bwd_workspace_bytes(p) > 0
 
 
 def test_empty_problems_are_no_ops(L):
