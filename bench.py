@@ -415,6 +415,42 @@ def run_ours(args, w, rank, world):
             "fwd_ms": ms, "encode_sort_select_ms": sum(sel) / len(sel)}
         del pc
 
+    # --- alternative weight kernels (softmax of -d2/gamma^2, inverse Euclidean)
+    # on the timed workload: the whole step, captured and timed like the main one
+    for weight in ("softmax", "inv_euclid"):
+        pw = zb.problem_of(wr, weight=weight)
+        pln = ZetaPlan(pw, dev)
+        with torch.cuda.stream(side):
+            for _ in range(warm):
+                pln.forward(q, k, v, gamma)
+                pln.backward(q, k, v, gamma, dout)
+        torch.cuda.current_stream().wait_stream(side)
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph):
+            pln.forward(q, k, v, gamma)
+            pln.backward(q, k, v, gamma, dout)
+        fgph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fgph):
+            pln.forward(q, k, v, gamma)
+        tms, fms = [], []
+        for it in range(warm + args.steps):
+            for gr, lst in ((gph, tms), (fgph, fms)):
+                flush.zero_()
+                a, b = ev(), ev()
+                a.record()
+                gr.replay()
+                b.record()
+                b.synchronize()
+                if it >= warm:
+                    lst.append(a.elapsed_time(b))
+        if int(pln.status.item()) != 0:
+            raise RuntimeError(f"device status {pln.status.item()} ({weight})")
+        sms, fmean = sum(tms) / len(tms), sum(fms) / len(fms)
+        variants[weight] = {"workload": wr.name, "tokens_per_s": tokens / (sms * 1e-3),
+                            "ms_per_step": sms, "fwd_tokens_per_s": tokens / (fmean * 1e-3),
+                            "fwd_ms": fmean}
+        del pln, gph, fgph
+
     if rank != 0:
         return
     peaks = {}

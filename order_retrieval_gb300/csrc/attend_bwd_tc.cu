@@ -23,6 +23,11 @@
 //   own chunk    - S^T = V . dO^T on tensor cores, the element-wise terms, then
 //                  dV += P^T . dO with P^T re-packed from the accumulator
 //                  fragments (their layout is the A-fragment layout).
+// Other weight kernels (flags; reply A3 "Justification for Euclidean Distance
+// Claim") swap in their w, dw/d(d^2) and dw/dgamma.  The softmax keeps a running
+// shift m per query on the query side (the sums are moved onto a lower shift
+// when it appears, exactly: sum g e and sum e also pick up the shift change),
+// and records the final m with 1/s and gbar for the key side.
 #include <type_traits>
 
 #include "mma.cuh"
@@ -34,7 +39,8 @@ constexpr int T64 = 64;           // rows per CTA tile (queries or keys)
 constexpr int DV = 64;
 constexpr int THREADS = 128;
 
-// Per-query record for the key side: q (padded to 4), then {1/s, gbar, 0, 0}.
+// Per-query record for the key side: q (padded to 4), then {1/s, gbar, m, 0}
+// (m: the softmax shift; 0 for the other weight kernels).
 struct __align__(16) QRec {
     float4 q;
     float4 sg;
@@ -107,20 +113,31 @@ struct __align__(16) QSmem {
     __nv_bfloat16 v[2][T64 * DV];
     float4 kt[2][T64];
     float part[T64][12];
+    float mpart[T64];             // softmax: the window part's shift per query
 };
 
 // Accumulators of one query row: x[0] = sum w, x[1] = sum w g, x[2] = sum g e,
 // x[3] = sum e, x[4..7] = sum g c (q-k), x[8..11] = sum c (q-k).
+// With the softmax, e = 2 w (d2 - m) / gamma^3 depends on the shift m: moving
+// the sums from shift m to m' = m + dm multiplies every term by
+// sc = exp(dm / gamma^2) and subtracts dm 2/gamma^3 w from each e.
 struct QAcc {
     float x[12];
     __device__ void zero() {
 #pragma unroll
         for (int y = 0; y < 12; ++y) x[y] = 0.f;
     }
-    __device__ void add(float w, float g, const float (&qi)[4], float4 kk, float inv_g2,
-                        float inv_g) {
-        const float c = -2.f * w * w * inv_g2;
-        const float e = 2.f * w * (1.f - w) * inv_g;
+    __device__ void rebase(float dm, float sc, float k2) {
+        x[2] -= dm * k2 * x[1];
+        x[3] -= dm * k2 * x[0];
+#pragma unroll
+        for (int y = 0; y < 12; ++y) x[y] *= sc;
+    }
+    template <int WK>
+    __device__ void add(float w, float d2, float m, float g, const float (&qi)[4], float4 kk,
+                        float inv_g2, float inv_g) {
+        const float c = -2.f * neg_dw_dd2<WK>(w, inv_g2);
+        const float e = dw_dgamma<WK>(w, d2, m, inv_g2, inv_g);
         x[0] += w;
         x[1] = __fmaf_rn(w, g, x[1]);
         x[2] = __fmaf_rn(g, e, x[2]);
@@ -143,10 +160,27 @@ struct QAcc2 {
 #pragma unroll
         for (int y = 0; y < 12; ++y) x[y] = make_float2(0.f, 0.f);
     }
-    template <int DK>
-    __device__ void add(float2 w, float2 g, const float2 (&dq)[4], float2 m2ig2, float2 two_ig) {
-        const float2 c = mul2(mul2(w, w), m2ig2);                 // -2 w^2 / gamma^2
-        const float2 e = mul2(mul2(w, sub2(dup2(1.f), w)), two_ig); // 2 w (1 - w) / gamma
+    __device__ void rebase(float2 dm, float2 sc, float2 k2) {
+        x[2] = sub2(x[2], mul2(mul2(dm, k2), x[1]));
+        x[3] = sub2(x[3], mul2(mul2(dm, k2), x[0]));
+#pragma unroll
+        for (int y = 0; y < 12; ++y) x[y] = mul2(x[y], sc);
+    }
+    // m2ig2 = -2/gamma^2, two_ig = 2/gamma, k2 = 2/gamma^3; d2, m only for the softmax.
+    template <int DK, int WK>
+    __device__ void add(float2 w, float2 d2, float2 m, float2 g, const float2 (&dq)[4],
+                        float2 m2ig2, float2 two_ig, float2 k2) {
+        float2 c, e;
+        if constexpr (WK == kWSoftmax) {
+            c = mul2(w, m2ig2);                                   // -2 w / gamma^2
+            e = mul2(mul2(w, sub2(d2, m)), k2);                   // 2 w (d2 - m) / gamma^3
+        } else if constexpr (WK == kWInvEuclid) {
+            c = mul2(mul2(w, w), mul2(w, dup2(-1.f)));            // -w^3
+            e = make_float2(0.f, 0.f);
+        } else {
+            c = mul2(mul2(w, w), m2ig2);                          // -2 w^2 / gamma^2
+            e = mul2(mul2(w, sub2(dup2(1.f), w)), two_ig);        // 2 w (1 - w) / gamma
+        }
         x[0] = add2(x[0], w);
         x[1] = fma2(w, g, x[1]);
         x[2] = fma2(g, e, x[2]);
@@ -160,7 +194,7 @@ struct QAcc2 {
     }
 };
 
-template <int DK>
+template <int DK, int WK>
 __global__ void __launch_bounds__(THREADS, 4)
 bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
              const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
@@ -215,10 +249,12 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
     };
     int jn[2] = {-1, -1};
     if (nqw > 0) load_idx(wq0, 0, jn);
+    const float k2 = 2.f * inv_g2 * inv_g;
     for (int r = 0; r < 16; ++r) {
         const int row = warp * 16 + r;
         QAcc acc;
         acc.zero();
+        float mrun = INFINITY;                     // softmax shift of this query
         if (r < nqw) {
             const int i = wq0 + r;
             float qi[4];
@@ -278,11 +314,24 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
                         if ((u & 3) == (lane >> 3)) gown[u >> 2] = gx;
                     }
                 }
+                float d2v[2];
+#pragma unroll
+                for (int s = 0; s < 2; ++s) d2v[s] = j[s] >= 0 ? dist2k<DK>(qi, kk[s]) : INFINITY;
+                if constexpr (WK == kWSoftmax) {
+                    float pm = fminf(d2v[0], d2v[1]);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) pm = fminf(pm, __shfl_xor_sync(kFull, pm, o));
+                    const float mn = fminf(mrun, pm);
+                    if (mn != mrun) {                    // uniform across the warp
+                        if (mrun != INFINITY) acc.rebase(mn - mrun, shift_scale(mn, mrun, inv_g2), k2);
+                        mrun = mn;
+                    }
+                }
 #pragma unroll
                 for (int s = 0; s < 2; ++s)
                     if (j[s] >= 0)
-                        acc.add(cauchy_w_fast(dist2k<DK>(qi, kk[s]), inv_g2), gown[s], qi, kk[s],
-                                inv_g2, inv_g);
+                        acc.add<WK>(weight_fast<WK>(d2v[s], mrun, inv_g2), d2v[s], mrun, gown[s],
+                                    qi, kk[s], inv_g2, inv_g);
             }
         }
         float tv[16];
@@ -290,7 +339,9 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
         for (int y = 0; y < 16; ++y) tv[y] = y < 12 ? acc.x[y] : 0.f;
         const float tot = warp_transpose_sum16(tv, lane);      // value (lane >> 1)
         if (!(lane & 1) && (lane >> 1) < 12) sm.part[row][lane >> 1] = tot;
+        if (lane == 0) sm.mpart[row] = mrun;
     }
+    __syncwarp();
 
     // ------------------------------------------------- own-chunk part ---
     const int g8 = lane >> 2, tig = lane & 3;
@@ -309,10 +360,47 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
 #pragma unroll
     for (int d = 0; d < 4; ++d) qab[d] = make_float2(qa[d], qbv[d]);
     const float2 ig2 = dup2(inv_g2), m2ig2 = dup2(-2.f * inv_g2), two_ig = dup2(2.f * inv_g);
+    const float2 k2v = dup2(k2);
     QAcc2 lab;
     lab.zero();
     uint32_t afr[4][4];
+    const int rowa_l = warp * 16 + g8;
+    float2 mab = make_float2(sm.mpart[rowa_l], sm.mpart[rowa_l + 8]);   // softmax shifts
     auto tile = [&](const float4 *Ks, uint32_t vbase, int key0, auto masked) {
+        if constexpr (WK == kWSoftmax) {           // move the shift to this tile's minimum
+            float2 tmin = make_float2(INFINITY, INFINITY);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int kl = nt * 8 + 2 * tig + e;
+                    const float4 kv = Ks[kl];
+                    const float kc[4] = {kv.x, kv.y, kv.z, kv.w};
+                    float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int d = 0; d < DK; ++d) {
+                        const float2 t = sub2(qab[d], dup2(kc[d]));
+                        d2 = fma2(t, t, d2);
+                    }
+                    if (decltype(masked)::value) {
+                        const int key = key0 + kl;
+                        d2.x = key <= lim_a ? d2.x : INFINITY;
+                        d2.y = key <= lim_b ? d2.y : INFINITY;
+                    }
+                    tmin = make_float2(fminf(tmin.x, d2.x), fminf(tmin.y, d2.y));
+                }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                tmin.x = fminf(tmin.x, __shfl_xor_sync(kFull, tmin.x, o));
+                tmin.y = fminf(tmin.y, __shfl_xor_sync(kFull, tmin.y, o));
+            }
+            const float2 mn = make_float2(fminf(mab.x, tmin.x), fminf(mab.y, tmin.y));
+            const float2 dm = make_float2(mab.x == INFINITY ? 0.f : mn.x - mab.x,
+                                          mab.y == INFINITY ? 0.f : mn.y - mab.y);
+            lab.rebase(dm, make_float2(shift_scale(mn.x, mab.x, inv_g2),
+                                       shift_scale(mn.y, mab.y, inv_g2)), k2v);
+            mab = mn;
+        }
         float s[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -343,13 +431,14 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     dq[d] = sub2(qab[d], dup2(kc[d]));
                     d2 = fma2(dq[d], dq[d], d2);
                 }
-                float2 w = cauchy_w2(d2, ig2);
+                float2 w = weight_fast2<WK>(d2, mab, ig2);
                 if (decltype(masked)::value) {
                     const int key = key0 + kl;
                     w.x = key <= lim_a ? w.x : 0.f;
                     w.y = key <= lim_b ? w.y : 0.f;
                 }
-                lab.add<DK>(w, make_float2(s[nt][e], s[nt][2 + e]), dq, m2ig2, two_ig);
+                lab.add<DK, WK>(w, d2, mab, make_float2(s[nt][e], s[nt][2 + e]), dq, m2ig2, two_ig,
+                                k2v);
             }
     };
     for (int kt = 0; kt < nkt; ++kt) {
@@ -396,10 +485,17 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
         const int rloc = warp * 16 + g8 + tig * 8;
         const int i = i0 + rloc;
         if (i < iend) {
-            const float *pw = sm.part[rloc];
+            QAcc wpart;                            // the window part, on the final shift
+#pragma unroll
+            for (int y = 0; y < 12; ++y) wpart.x[y] = sm.part[rloc][y];
+            const float mfin = tig == 0 ? mab.x : mab.y;
+            if constexpr (WK == kWSoftmax) {
+                const float mw = sm.mpart[rloc];
+                if (mw != INFINITY) wpart.rebase(mfin - mw, shift_scale(mfin, mw, inv_g2), k2);
+            }
             float t[12];
 #pragma unroll
-            for (int y = 0; y < 12; ++y) t[y] = (tig == 0 ? la.x[y] : lb.x[y]) + pw[y];
+            for (int y = 0; y < 12; ++y) t[y] = (tig == 0 ? la.x[y] : lb.x[y]) + wpart.x[y];
             const float inv_s = __frcp_rn(t[0]);
             const float gb = t[1] * inv_s;
             const int64_t gi = seg * N + i;
@@ -408,7 +504,7 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
             const float *qq = tig == 0 ? qa : qbv;
             QRec rcd;
             rcd.q = make_float4(qq[0], qq[1], qq[2], qq[3]);
-            rcd.sg = make_float4(inv_s, gb, 0.f, 0.f);
+            rcd.sg = make_float4(inv_s, gb, WK == kWSoftmax ? mfin : 0.f, 0.f);
             rec[gi] = rcd;
         }
     }
@@ -424,7 +520,7 @@ struct __align__(16) KSmem {
     float dkp[T64][4];
 };
 
-template <int DK>
+template <int DK, int WK>
 __global__ void __launch_bounds__(THREADS, 4)
 bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
            const float *__restrict__ gamma, const __nv_bfloat16 *__restrict__ dout,
@@ -516,11 +612,11 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                         dqk[d] = qc[d] - kjc[d];
                         d2 = __fmaf_rn(dqk[d], dqk[d], d2);
                     }
-                    const float w = cauchy_w_fast(d2, inv_g2);
+                    const float w = weight_fast<WK>(d2, qrc.sg.z, inv_g2);
                     inv_s = qrc.sg.x;
                     gb = qrc.sg.y;
                     a = w * inv_s;
-                    s2 = 2.f * w * w * inv_g2;
+                    s2 = 2.f * neg_dw_dd2<WK>(w, inv_g2);
                 }
                 float gown = 0.f;
 #pragma unroll
@@ -633,6 +729,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                     const QRec qrc = qt_rec[ql];
                     const float qc[4] = {qrc.q.x, qrc.q.y, qrc.q.z, qrc.q.w};
                     const float2 inv_s = dup2(qrc.sg.x), gb = dup2(qrc.sg.y);
+                    const float2 mq = dup2(qrc.sg.z);
                     float2 dqk[4];
                     float2 d2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -640,7 +737,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                         dqk[d] = sub2(dup2(qc[d]), kab[d]);
                         d2 = fma2(dqk[d], dqk[d], d2);
                     }
-                    float2 w = cauchy_w2(d2, ig2);
+                    float2 w = weight_fast2<WK>(d2, mq, ig2);
                     if (decltype(masked)::value) {
                         const int i = iq0 + ql;
                         w.x = (i >= first_a && i < cend) ? w.x : 0.f;
@@ -648,7 +745,11 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                     }
                     const float2 aw = mul2(w, inv_s);
                     const float2 dldw = mul2(sub2(make_float2(s[nt][e], s[nt][2 + e]), gb), inv_s);
-                    const float2 coef = mul2(dldw, mul2(mul2(w, w), two_ig2));
+                    float2 ndw;                    // 2 (-dw/d(d^2))
+                    if constexpr (WK == kWSoftmax) ndw = mul2(w, two_ig2);
+                    else if constexpr (WK == kWInvEuclid) ndw = mul2(mul2(w, w), w);
+                    else ndw = mul2(mul2(w, w), two_ig2);
+                    const float2 coef = mul2(dldw, ndw);
 #pragma unroll
                     for (int d = 0; d < DK; ++d) dkab[d] = fma2(coef, dqk[d], dkab[d]);
                     pa_[hh * 4 + e] = aw.x;
@@ -725,19 +826,17 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
 }  // namespace
 
 bool attend_bwd_tc_supported(const Prob &p) {
-    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4 && p.wk == kWCauchy;
+    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4;
 }
 
 size_t bwd_tc_rec_bytes(const Prob &p) { return sizeof(QRec) * (size_t)(p.S * p.N); }
 
-cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, const void *v,
-                                const float *gamma, const int32_t *idx, const void *dout,
-                                float *dq, void *rec, float *dg_part, int32_t *status,
-                                cudaStream_t st) {
-    const int tpc = (p.C + T64 - 1) / T64;
-    const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
+template <int WK>
+void bwd_query_tc_dk(const Prob &p, dim3 grid, int tpc, const float *q, const float *k,
+                     const void *v, const float *gamma, const int32_t *idx, const void *dout,
+                     float *dq, void *rec, float *dg_part, int32_t *status, cudaStream_t st) {
 #define ZETA_BQ(D)                                                                              \
-    bwd_query_tc<D><<<grid, THREADS, 0, st>>>(                                                 \
+    bwd_query_tc<D, WK><<<grid, THREADS, 0, st>>>(                                             \
         q, k, static_cast<const __nv_bfloat16 *>(v), gamma, idx,                              \
         static_cast<const __nv_bfloat16 *>(dout), dq, static_cast<QRec *>(rec), dg_part, status, \
         p.N, p.H, p.k, p.C, tpc)
@@ -748,17 +847,15 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
         default: ZETA_BQ(4); break;
     }
 #undef ZETA_BQ
-    return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
-                              const void *dout, const void *rec, const uint32_t *csr_q,
-                              uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
-                              float *dk, void *dv, cudaStream_t st) {
-    const int tpc = (p.C + T64 - 1) / T64;
-    const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
+template <int WK>
+void bwd_key_tc_dk(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
+                   const float *gamma, const void *dout, const void *rec, const uint32_t *csr_q,
+                   uint32_t csr_mask, const uint32_t *off, int64_t csr_stride, float *dk, void *dv,
+                   cudaStream_t st) {
 #define ZETA_BK(D)                                                                              \
-    bwd_key_tc<D><<<grid, THREADS, 0, st>>>(                                                   \
+    bwd_key_tc<D, WK><<<grid, THREADS, 0, st>>>(                                               \
         k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout), \
         static_cast<const QRec *>(rec), csr_q, csr_mask, off, csr_stride, dk,                 \
         static_cast<__nv_bfloat16 *>(dv), p.N, p.H, p.C, tpc)
@@ -769,6 +866,41 @@ cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, cons
         default: ZETA_BK(4); break;
     }
 #undef ZETA_BK
+}
+
+cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, const void *v,
+                                const float *gamma, const int32_t *idx, const void *dout,
+                                float *dq, void *rec, float *dg_part, int32_t *status,
+                                cudaStream_t st) {
+    const int tpc = (p.C + T64 - 1) / T64;
+    const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
+    if (p.wk == kWSoftmax)
+        bwd_query_tc_dk<kWSoftmax>(p, grid, tpc, q, k, v, gamma, idx, dout, dq, rec, dg_part,
+                                   status, st);
+    else if (p.wk == kWInvEuclid)
+        bwd_query_tc_dk<kWInvEuclid>(p, grid, tpc, q, k, v, gamma, idx, dout, dq, rec, dg_part,
+                                     status, st);
+    else
+        bwd_query_tc_dk<kWCauchy>(p, grid, tpc, q, k, v, gamma, idx, dout, dq, rec, dg_part,
+                                  status, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
+                              const void *dout, const void *rec, const uint32_t *csr_q,
+                              uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
+                              float *dk, void *dv, cudaStream_t st) {
+    const int tpc = (p.C + T64 - 1) / T64;
+    const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
+    if (p.wk == kWSoftmax)
+        bwd_key_tc_dk<kWSoftmax>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
+                                 csr_stride, dk, dv, st);
+    else if (p.wk == kWInvEuclid)
+        bwd_key_tc_dk<kWInvEuclid>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
+                                   csr_stride, dk, dv, st);
+    else
+        bwd_key_tc_dk<kWCauchy>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
+                                csr_stride, dk, dv, st);
     return cudaGetLastError();
 }
 

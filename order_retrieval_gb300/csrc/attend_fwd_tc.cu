@@ -19,7 +19,13 @@
 //    straight into mma A fragments (bf16), B fragments come from ldmatrix.trans,
 //    and mma.sync m16n8k16 accumulates in float32 registers.  Row sums of P are
 //    kept in float32 from the unrounded weights.
-//  * The two partial sums simply add (weights are in (0, 1], no rescaling).
+//  * The two partial sums simply add (Cauchy weights are in (0, 1], no
+//    rescaling).  The other weight kernels (flags; reply A3 "Justification for
+//    Euclidean Distance Claim") reuse everything: inverse Euclidean swaps the
+//    weight; the softmax keeps a running shift (the smallest d2 seen) per query,
+//    rescales its sums when the shift moves (per 64-key pass in the window, per
+//    key tile in the own chunk, which starts from the window's shift) and
+//    brings the window sums onto the final shift in the epilogue.
 #include <type_traits>
 
 #include "mma.cuh"
@@ -38,6 +44,7 @@ struct __align__(16) FwdSmem {
     float4 kt[2][TK];
     float win[TQ][WPAD];
     float swin[TQ];
+    float mwin[TQ];               // softmax: the window's shift per query
 };
 
 template <int DK>
@@ -88,7 +95,7 @@ __device__ __forceinline__ void load_tile(FwdSmem &sm, int b, const float *kb,
     }
 }
 
-template <int DK>
+template <int DK, int WK>
 __global__ void __launch_bounds__(THREADS, 4)
 attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
               const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
@@ -138,6 +145,7 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
         float sw = 0.f;
+        float mrun = INFINITY;                     // softmax shift of this query
         if (r < nqw) {
             const int i = wq0 + r;
             float qi[4];
@@ -169,10 +177,26 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     buf[u] = (u < nu && jr >= 0) ? ld_stream16(vb + (int64_t)jr * DV + sub * 8)
                                                  : make_uint4(0u, 0u, 0u, 0u);
                 }
+                float d2v[2];
+#pragma unroll
+                for (int s = 0; s < 2; ++s) d2v[s] = j[s] >= 0 ? dist2k<DK>(qi, kk[s]) : INFINITY;
+                if constexpr (WK == kWSoftmax) {
+                    float pm = fminf(d2v[0], d2v[1]);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) pm = fminf(pm, __shfl_xor_sync(kFull, pm, o));
+                    const float mn = fminf(mrun, pm);
+                    if (mn != mrun) {                    // uniform across the warp
+                        const float sc = shift_scale(mn, mrun, inv_g2);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[e] = mul2(acc[e], dup2(sc));
+                        sw *= sc;
+                        mrun = mn;
+                    }
+                }
                 float w[2];
 #pragma unroll
                 for (int s = 0; s < 2; ++s) {
-                    w[s] = j[s] >= 0 ? cauchy_w_fast(dist2k<DK>(qi, kk[s]), inv_g2) : 0.f;
+                    w[s] = j[s] >= 0 ? weight_fast<WK>(d2v[s], mrun, inv_g2) : 0.f;
                     sw += w[s];
                 }
 #pragma unroll
@@ -198,8 +222,12 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
             dst[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
             dst[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
         }
-        if (lane == 0) sm.swin[row] = sw;
+        if (lane == 0) {
+            sm.swin[row] = sw;
+            sm.mwin[row] = mrun;
+        }
     }
+    __syncwarp();
 
     // --------------------------------------------------- own-chunk part ---
     const int g = lane >> 2, tig = lane & 3;
@@ -216,6 +244,8 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
 #pragma unroll
     for (int d = 0; d < 4; ++d) qab[d] = make_float2(qa[d], qbv[d]);
     const float2 ig2 = dup2(inv_g2);
+    const int rowa = warp * 16 + g, rowb = rowa + 8;
+    float2 mab = make_float2(sm.mwin[rowa], sm.mwin[rowb]);   // softmax shifts of rows a, b
     float acc[8][4];
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt)
@@ -226,8 +256,54 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     const int warp_last = min(warp_first + 15, iend - 1);
     const bool warp_rows_full = warp_first + 15 < iend;
 
+    // Squared distances of rows (a, b) to key kl of the tile.
+    auto d2ab = [&](const float4 *Ks, int kl) {
+        const float4 kv = Ks[kl];
+        const float kc[4] = {kv.x, kv.y, kv.z, kv.w};
+        float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int d = 0; d < DK; ++d) {
+            const float2 e = sub2(qab[d], dup2(kc[d]));
+            d2 = fma2(e, e, d2);
+        }
+        return d2;
+    };
+
     // One 64-key tile: weights of rows (a, b) against 16 keys per k-step, packed.
     auto tile = [&](const float4 *Ks, uint32_t vbase, int key0, auto masked) {
+        if constexpr (WK == kWSoftmax) {           // move the shift to this tile's minimum
+            float2 tmin = make_float2(INFINITY, INFINITY);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int kl = ks * 16 + 2 * tig + (h & 1) + (h >> 1) * 8;
+                    float2 d2 = d2ab(Ks, kl);
+                    if (decltype(masked)::value) {
+                        const int key = key0 + kl;
+                        d2.x = key <= lim_a ? d2.x : INFINITY;
+                        d2.y = key <= lim_b ? d2.y : INFINITY;
+                    }
+                    tmin = make_float2(fminf(tmin.x, d2.x), fminf(tmin.y, d2.y));
+                }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                tmin.x = fminf(tmin.x, __shfl_xor_sync(kFull, tmin.x, o));
+                tmin.y = fminf(tmin.y, __shfl_xor_sync(kFull, tmin.y, o));
+            }
+            const float2 mn = make_float2(fminf(mab.x, tmin.x), fminf(mab.y, tmin.y));
+            const float sa_ = shift_scale(mn.x, mab.x, inv_g2);
+            const float sb_ = shift_scale(mn.y, mab.y, inv_g2);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                acc[nt][0] *= sa_;
+                acc[nt][1] *= sa_;
+                acc[nt][2] *= sb_;
+                acc[nt][3] *= sb_;
+            }
+            sab = mul2(sab, make_float2(sa_, sb_));
+            mab = mn;
+        }
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
             const int kk0 = ks * 16 + 2 * tig;
@@ -235,15 +311,7 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
 #pragma unroll
             for (int h = 0; h < 4; ++h) {              // keys kk0, kk0+1, kk0+8, kk0+9
                 const int kl = kk0 + (h & 1) + (h >> 1) * 8;
-                const float4 kv = Ks[kl];
-                const float kc[4] = {kv.x, kv.y, kv.z, kv.w};
-                float2 d2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int d = 0; d < DK; ++d) {
-                    const float2 e = sub2(qab[d], dup2(kc[d]));
-                    d2 = fma2(e, e, d2);
-                }
-                float2 w = cauchy_w2(d2, ig2);
+                float2 w = weight_fast2<WK>(d2ab(Ks, kl), mab, ig2);
                 if (decltype(masked)::value) {
                     const int key = key0 + kl;
                     w.x = key <= lim_a ? w.x : 0.f;
@@ -293,22 +361,27 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     sa += __shfl_xor_sync(kFull, sa, 2);
     sb += __shfl_xor_sync(kFull, sb, 1);
     sb += __shfl_xor_sync(kFull, sb, 2);
-    const int rowa = warp * 16 + g, rowb = rowa + 8;
-    const float ta = sa + sm.swin[rowa], tb = sb + sm.swin[rowb];
+    // Window sums onto the final shift (softmax; a factor of 1 otherwise).
+    float fa = 1.f, fb = 1.f;
+    if constexpr (WK == kWSoftmax) {
+        fa = shift_scale(mab.x, sm.mwin[rowa], inv_g2);
+        fb = shift_scale(mab.y, sm.mwin[rowb], inv_g2);
+    }
+    const float ta = sa + sm.swin[rowa] * fa, tb = sb + sm.swin[rowb] * fb;
     const float ia = ra < iend ? __frcp_rn(ta) : 0.f;
     const float ib = rb < iend ? __frcp_rn(tb) : 0.f;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
         const int col = nt * 8 + 2 * tig;
         if (ra < iend) {
-            const float o0 = (acc[nt][0] + sm.win[rowa][col]) * ia;
-            const float o1 = (acc[nt][1] + sm.win[rowa][col + 1]) * ia;
+            const float o0 = __fmaf_rn(sm.win[rowa][col], fa, acc[nt][0]) * ia;
+            const float o1 = __fmaf_rn(sm.win[rowa][col + 1], fa, acc[nt][1]) * ia;
             *reinterpret_cast<__nv_bfloat162 *>(out + (seg * N + ra) * (int64_t)DV + col) =
                 __floats2bfloat162_rn(o0, o1);
         }
         if (rb < iend) {
-            const float o0 = (acc[nt][2] + sm.win[rowb][col]) * ib;
-            const float o1 = (acc[nt][3] + sm.win[rowb][col + 1]) * ib;
+            const float o0 = __fmaf_rn(sm.win[rowb][col], fb, acc[nt][2]) * ib;
+            const float o1 = __fmaf_rn(sm.win[rowb][col + 1], fb, acc[nt][3]) * ib;
             *reinterpret_cast<__nv_bfloat162 *>(out + (seg * N + rb) * (int64_t)DV + col) =
                 __floats2bfloat162_rn(o0, o1);
         }
@@ -322,7 +395,7 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
 }  // namespace
 
 bool attend_fwd_tc_supported(const Prob &p) {
-    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4 && p.wk == kWCauchy;
+    return p.vdt == ZETA_BF16 && p.dV == DV && p.dK <= 4;
 }
 
 cudaError_t launch_attend_fwd_tc(const Prob &p, const float *q, const float *k, const void *v,
@@ -332,15 +405,24 @@ cudaError_t launch_attend_fwd_tc(const Prob &p, const float *q, const float *k, 
     const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
     const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(v);
     __nv_bfloat16 *ob = static_cast<__nv_bfloat16 *>(out);
-#define ZETA_FWD_TC(D)                                                                        \
-    attend_fwd_tc<D><<<grid, THREADS, 0, st>>>(q, k, vb, gamma, idx, ob, rowsum, status, p.N, \
-                                               p.H, p.k, p.C, tpc)
-    switch (p.dK) {
-        case 1: ZETA_FWD_TC(1); break;
-        case 2: ZETA_FWD_TC(2); break;
-        case 3: ZETA_FWD_TC(3); break;
-        default: ZETA_FWD_TC(4); break;
+#define ZETA_FWD_TC(D, WK)                                                                    \
+    attend_fwd_tc<D, WK><<<grid, THREADS, 0, st>>>(q, k, vb, gamma, idx, ob, rowsum, status,   \
+                                                   p.N, p.H, p.k, p.C, tpc)
+#define ZETA_FWD_TC_D(WK)                        \
+    switch (p.dK) {                              \
+        case 1: ZETA_FWD_TC(1, WK); break;       \
+        case 2: ZETA_FWD_TC(2, WK); break;       \
+        case 3: ZETA_FWD_TC(3, WK); break;       \
+        default: ZETA_FWD_TC(4, WK); break;      \
     }
+    if (p.wk == kWSoftmax) {
+        ZETA_FWD_TC_D(kWSoftmax);
+    } else if (p.wk == kWInvEuclid) {
+        ZETA_FWD_TC_D(kWInvEuclid);
+    } else {
+        ZETA_FWD_TC_D(kWCauchy);
+    }
+#undef ZETA_FWD_TC_D
 #undef ZETA_FWD_TC
     return cudaGetLastError();
 }

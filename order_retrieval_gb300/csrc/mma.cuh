@@ -196,6 +196,35 @@ __device__ __forceinline__ float2 cauchy_w2(float2 d2, float2 inv_g2) {
     return make_float2(__fdividef(1.0f, t.x), __fdividef(1.0f, t.y));
 }
 
+// Weight kernels (common.cuh) with fast intrinsics, for weights that feed sums:
+// the Cauchy reciprocal by __fdividef, the softmax exponential by __expf
+// (m = the query's current shift), inverse Euclidean by rsqrtf.
+template <int WK>
+__device__ __forceinline__ float weight_fast(float d2, float m, float inv_g2) {
+    if constexpr (WK == kWSoftmax) return __expf((m - d2) * inv_g2);
+    else if constexpr (WK == kWInvEuclid) return rsqrtf(d2 + kInvEps2);
+    else return cauchy_w_fast(d2, inv_g2);
+}
+
+template <int WK>
+__device__ __forceinline__ float2 weight_fast2(float2 d2, float2 m, float2 inv_g2) {
+    if constexpr (WK == kWSoftmax) {
+        const float2 t = mul2(sub2(m, d2), inv_g2);
+        return make_float2(__expf(t.x), __expf(t.y));
+    } else if constexpr (WK == kWInvEuclid) {
+        const float2 t = add2(d2, dup2(kInvEps2));
+        return make_float2(rsqrtf(t.x), rsqrtf(t.y));
+    } else {
+        return cauchy_w2(d2, inv_g2);
+    }
+}
+
+// Factor that moves sums taken with shift m_old onto shift m_new <= m_old
+// (exactly 1 when the shift did not move, 0 when nothing was summed yet).
+__device__ __forceinline__ float shift_scale(float m_new, float m_old, float inv_g2) {
+    return m_new == m_old ? 1.f : __expf((m_new - m_old) * inv_g2);
+}
+
 // Two bf16 (one 32-bit word) -> float2, exactly.
 __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
