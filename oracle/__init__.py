@@ -56,6 +56,7 @@ def _load():
     lib.orc_attend_bwd.argtypes = [P, P, P, D, P, P, I64, I64, I, I, I, P, P, P, P, I]
     lib.orc_exact_topk.argtypes = [P, P, I64, I64, I, I, P, I64, P]
     lib.orc_encode_axes.argtypes = [P, I64, I, I, P, P]
+    lib.orc_project.argtypes = [P, I64, I, I, I, I, P, P, P, P, P]
     lib.orc_merge_windows.argtypes = [P, I, I, I, P]
     _lib = lib
     return lib
@@ -146,6 +147,22 @@ def select_multi(q, kx, C: int, k: int, bits: int, curves: int, rows=None):
         kc = encode_axes(kx, bits, axes)
         wins.append(select(qc[None], kc[None], C, km, rows=rows)[0])
     return merge_windows(np.stack(wins, axis=-2), k)
+
+
+def project(x, W1, b1, W2, b2):
+    """Two-layer projection (see orc_project).  x [M, D]; W1 [H*F, D]; b1 [H*F];
+    W2 [H, d_K, F]; b2 [H, d_K]; all taken as float64.  Returns [M, H, d_K]."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    W1 = np.ascontiguousarray(W1, dtype=np.float64)
+    b1 = np.ascontiguousarray(b1, dtype=np.float64)
+    W2 = np.ascontiguousarray(W2, dtype=np.float64)
+    b2 = np.ascontiguousarray(b2, dtype=np.float64)
+    M, D = x.shape
+    H, d_K, F = W2.shape
+    assert W1.shape == (H * F, D) and b1.shape == (H * F,) and b2.shape == (H, d_K)
+    out = np.empty((M, H, d_K), dtype=np.float64)
+    _load().orc_project(_p(x), M, D, H, F, d_K, _p(W1), _p(b1), _p(W2), _p(b2), _p(out))
+    return out
 
 
 # ------------------------------------------------------------ sort/select ---

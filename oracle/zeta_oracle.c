@@ -393,3 +393,38 @@ void orc_merge_windows(const int32_t *win, int M, int km, int k, int32_t *out)
         }
     for (; n < k; ++n) out[n] = -1;
 }
+
+/* ------------------------------------------------------------ projection --- */
+
+/* Two-layer projection of one token onto the d_K key (or query) coordinates of
+ * every head, OpenReview discussion, reply A "LLMs impact the selection of
+ * d_K" (a two-layer neural network projects the input into keys):
+ *   h_f   = max(0, sum_e W1[hd*F + f][e] x[e] + b1[hd*F + f])     f < F
+ *   y_c   = tanh(sum_f W2[hd][c][f] h_f + b2[hd][c])               c < d_K
+ * tanh lands the coordinates in (-1, 1), the range the quantiser reads.
+ * x: [M][D]; W1: [H*F][D]; b1: [H*F]; W2: [H][d_K][F]; b2: [H][d_K];
+ * out: [M][H][d_K]. */
+void orc_project(const double *x, int64_t M, int D, int H, int F, int d_K,
+                 const double *W1, const double *b1, const double *W2, const double *b2,
+                 double *out)
+{
+    double *h = (double *)malloc((size_t)F * sizeof(double));
+    for (int64_t t = 0; t < M; ++t) {
+        const double *xt = x + t * D;
+        for (int hd = 0; hd < H; ++hd) {
+            for (int f = 0; f < F; ++f) {
+                const double *w = W1 + ((int64_t)hd * F + f) * D;
+                double z = b1[hd * F + f];
+                for (int e = 0; e < D; ++e) z += w[e] * xt[e];
+                h[f] = z > 0.0 ? z : 0.0;
+            }
+            for (int c = 0; c < d_K; ++c) {
+                const double *w = W2 + ((int64_t)hd * d_K + c) * F;
+                double y = b2[hd * d_K + c];
+                for (int f = 0; f < F; ++f) y += w[f] * h[f];
+                out[(t * H + hd) * d_K + c] = tanh(y);
+            }
+        }
+    }
+    free(h);
+}

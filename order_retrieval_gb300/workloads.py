@@ -161,6 +161,38 @@ SWEEP = [LONG.replace(name=f"sweep_dk{dk}_n16384", N=16384, C=1024, d_K=dk, bits
 FD = TRAIN.replace(name="fd_n256", B=1, H=2, N=256, C=128)
 
 
+# Two-layer projection front end: token features of width D = H * d_V feed a
+# per-head Linear(D -> F), ReLU, Linear(F -> d_K), tanh, for queries and keys.
+@dataclasses.dataclass(frozen=True)
+class Projection:
+    name: str
+    base: Workload        # B, H, N, d_K, bits (and the attention that follows)
+    D: int
+    F: int
+    seed: int
+
+
+PROJ = Projection("proj_train_b4_n65536_d512", TRAIN, 512, 64, 5)
+PROJ_SMALL = Projection("proj_small", TRAIN.replace(B=1, H=4, N=1024, C=128), 128, 64, 6)
+
+
+def generate_projection(pj: Projection) -> dict:
+    """Draw x [B, N, D] ~ N(0, 1); per projection (query, key): W1 [H*F, D] ~
+    N(0, 1/D), b1 [H*F] ~ N(0, 0.1^2), W2 [H, d_K, F] ~ N(0, 2/F), b2 [H, d_K] ~
+    N(0, 0.1^2).  x and W1 are bf16 bit patterns (int16), stacked [2, ...] for
+    (query, key); biases and W2 float32."""
+    w = pj.base
+    st = SplitMix64(pj.seed)
+    x = st.normal_f64(w.B * w.N * pj.D).astype(np.float32).reshape(w.B, w.N, pj.D)
+    HF = w.H * pj.F
+    W1 = (st.normal_f64(2 * HF * pj.D) / np.sqrt(pj.D)).astype(np.float32).reshape(2, HF, pj.D)
+    b1 = (0.1 * st.normal_f64(2 * HF)).astype(np.float32).reshape(2, HF)
+    W2 = (st.normal_f64(2 * w.H * w.d_K * pj.F) * np.sqrt(2.0 / pj.F)).astype(np.float32)
+    W2 = W2.reshape(2, w.H, w.d_K, pj.F)
+    b2 = (0.1 * st.normal_f64(2 * w.H * w.d_K)).astype(np.float32).reshape(2, w.H, w.d_K)
+    return {"x": f32_to_bf16_bits(x), "W1": f32_to_bf16_bits(W1), "b1": b1, "W2": W2, "b2": b2}
+
+
 def _points(st: SplitMix64, w: Workload, count: int, centres: Optional[np.ndarray]) -> np.ndarray:
     if w.dist == "uniform":
         return st.uniform_pm1_f32(count * w.d_K).reshape(count, w.d_K)
