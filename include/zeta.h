@@ -212,6 +212,42 @@ zeta_status_t zeta_select_topk_curves(const zeta_problem_t *p, int32_t curves,
                                       const int32_t *prefix_idx, int32_t *idx,
                                       cudaStream_t stream);
 
+/* Widths of the projection front end: D input features per token, F hidden
+ * units per head. */
+typedef struct {
+    int32_t D, F;
+} zeta_proj_t;
+
+/*
+ * zeta_project_encode -- queries and keys from token features, with their codes.
+ * Passage: OpenReview reply A "LLMs impact the selection of d_K" (a two-layer
+ * neural network projects the input into the keys) and reply A2
+ * "Clarification of Binary Expansion and Precision" (the codes).
+ * Reading: per head hd, and separately for queries (projection 0) and keys
+ * (projection 1):
+ *   h_f = max(0, W1[hd*F + f] . x_t + b1[hd*F + f]),  y_c = tanh(W2[hd][c] . h + b2[hd][c])
+ * (tanh puts the coordinates in (-1, 1), the quantiser's range); y is written
+ * out and encoded exactly as zeta_encode would encode it.
+ *   x        in : bf16 [B, N, D]           (16-B aligned)
+ *   w1       in : bf16 [2, H*F, D]         (16-B aligned; rows are hidden units)
+ *   b1       in : float [2, H*F]
+ *   w2       in : float [2, H, d_K, F]
+ *   b2       in : float [2, H, d_K]
+ *   q, k     out: float [B, H, N, d_K]
+ *   q_codes, k_codes  out: code type of the problem [B, H, N]
+ *   dev_status  optional int32 device word (ZETA_ERR_DEVICE_TIMEOUT if a
+ *               bounded wait of the kernel gave up)
+ * Limits: F = 64, D a multiple of 64, H a multiple of 4, d_K <= 4, B*N < 2^31.
+ * The first layer runs on the tensor cores with bf16 inputs and float32
+ * accumulation; the rest in float32.
+ * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED (outside the limits).
+ */
+zeta_status_t zeta_project_encode(const zeta_problem_t *p, const zeta_proj_t *pj,
+                                  const void *x, const void *w1, const float *b1,
+                                  const float *w2, const float *b2, float *q, float *k,
+                                  void *q_codes, void *k_codes, int32_t *dev_status,
+                                  cudaStream_t stream);
+
 /*
  * zeta_attend_fwd -- Adaptive Cauchy-softmax over the selected keys.
  * Passage: OpenReview reply A2 "Discussion on its robustness" (trainable gamma,

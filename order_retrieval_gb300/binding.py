@@ -44,6 +44,10 @@ class zeta_problem_t(ctypes.Structure):
                 ("flags", ctypes.c_uint32)]
 
 
+class zeta_proj_t(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int32), ("F", ctypes.c_int32)]
+
+
 def problem(B, H, N, d_K, d_V, k, C, bits, v_dtype="bf16", flags=0,
             weight="cauchy") -> zeta_problem_t:
     """flags: raw flag bits; weight: 'cauchy', 'softmax' or 'inv_euclid' (ORed in)."""
@@ -93,6 +97,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.zeta_encode_curves.restype = S
     L.zeta_select_topk_curves.argtypes = [PP, ctypes.c_int32, P, P, P, P, P]
     L.zeta_select_topk_curves.restype = S
+    L.zeta_project_encode.argtypes = [PP, ctypes.POINTER(zeta_proj_t)] + [P] * 11
+    L.zeta_project_encode.restype = S
     L.zeta_attend_fwd.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.zeta_attend_fwd.restype = S
     L.zeta_attend_bwd.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
@@ -246,6 +252,29 @@ def zeta_select_topk_curves(p, curves, q_codes, prefix_codes, prefix_idx, idx, s
            lib().zeta_select_topk_curves(ctypes.byref(p), curves, _ptr(q_codes),
                                          _ptr(prefix_codes), _ptr(prefix_idx), _ptr(idx),
                                          _stream(stream)))
+
+
+def zeta_project_encode(p, D, F, x, w1, b1, w2, b2, q, k, q_codes, k_codes, dev_status=None,
+                        stream=None):
+    """x bf16 [B,N,D]; w1 bf16 [2,H*F,D]; b1 f32 [2,H*F]; w2 f32 [2,H,d_K,F];
+    b2 f32 [2,H,d_K]; q, k f32 [B,H,N,d_K]; q_codes, k_codes [B,H,N]."""
+    S = p.B * p.H * p.N
+    _expect(x, "x", torch.bfloat16, p.B * p.N * D)
+    _expect(w1, "w1", torch.bfloat16, 2 * p.H * F * D)
+    _expect(b1, "b1", torch.float32, 2 * p.H * F)
+    _expect(w2, "w2", torch.float32, 2 * p.H * p.d_K * F)
+    _expect(b2, "b2", torch.float32, 2 * p.H * p.d_K)
+    for t, n in ((q, "q"), (k, "k")):
+        _expect(t, n, torch.float32, S * p.d_K)
+    for t, n in ((q_codes, "q_codes"), (k_codes, "k_codes")):
+        _expect(t, n, code_dtype(p), S)
+    _expect(dev_status, "dev_status", torch.int32, 1)
+    pj = zeta_proj_t(D, F)
+    _check("zeta_project_encode",
+           lib().zeta_project_encode(ctypes.byref(p), ctypes.byref(pj), _ptr(x), _ptr(w1),
+                                     _ptr(b1), _ptr(w2), _ptr(b2), _ptr(q), _ptr(k),
+                                     _ptr(q_codes), _ptr(k_codes), _ptr(dev_status),
+                                     _stream(stream)))
 
 
 def curve_axes(d_K: int, curves: int) -> list:

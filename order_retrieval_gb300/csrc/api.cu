@@ -157,6 +157,24 @@ ZETA_API zeta_status_t zeta_select_topk_curves(const zeta_problem_t *p, int32_t 
         zeta::launch_select_curves(pr, curves, q_codes, prefix_codes, prefix_idx, idx, stream));
 }
 
+ZETA_API zeta_status_t zeta_project_encode(const zeta_problem_t *p, const zeta_proj_t *pj,
+                                           const void *x, const void *w1, const float *b1,
+                                           const float *w2, const float *b2, float *q, float *k,
+                                           void *q_codes, void *k_codes, int32_t *dev_status,
+                                           cudaStream_t stream) {
+    Prob pr;
+    zeta_status_t s = check_problem(p, &pr);
+    if (s != ZETA_OK) return s;
+    if (!pj || pj->D < 1 || pj->F < 1) return ZETA_ERR_INVALID_ARG;
+    if (empty(pr)) return ZETA_OK;
+    if (!x || !w1 || !b1 || !w2 || !b2 || !q || !k || !q_codes || !k_codes)
+        return ZETA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w1)) return ZETA_ERR_INVALID_ARG;
+    if (!zeta::project_tc_supported(pr, pj->D, pj->F)) return ZETA_ERR_UNSUPPORTED;
+    return from_cuda(zeta::launch_project_tc(pr, pj->D, x, w1, b1, w2, b2, q, k, q_codes,
+                                             k_codes, dev_status, stream));
+}
+
 ZETA_API zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, const float *k,
                                        const void *v, const float *gamma, const int32_t *idx,
                                        void *out, float *rowsum, int32_t *dev_status,

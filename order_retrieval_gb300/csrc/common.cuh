@@ -106,6 +106,13 @@ cudaError_t launch_select_curves(const Prob &p, int curves, const void *q_codes,
                                  const void *prefix_codes, const int32_t *prefix_idx,
                                  int32_t *idx, cudaStream_t st);
 
+// Two-layer projection + encode on tcgen05 (F = 64, D % 64 == 0, H % 4 == 0).
+bool project_tc_supported(const Prob &p, int D, int F);
+cudaError_t launch_project_tc(const Prob &p, int D, const void *x, const void *w1,
+                              const float *b1, const float *w2, const float *b2, float *q,
+                              float *k, void *q_codes, void *k_codes, int32_t *status,
+                              cudaStream_t st);
+
 cudaError_t launch_attend_fwd(const Prob &p, const float *q, const float *k, const void *v,
                               const float *gamma, const int32_t *idx, void *out, float *rowsum,
                               int32_t *status, cudaStream_t st);

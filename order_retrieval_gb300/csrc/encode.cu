@@ -10,42 +10,10 @@
 // One thread per token.  The work is a few integer operations per 4*d_K bytes
 // read, so the kernel runs at copy speed; bit spreading for d_K = 2 and 3 uses
 // the usual shift-and-mask ("magic number") dilation, other widths a bit loop.
-#include "common.cuh"
+#include "zorder.cuh"
 
 namespace zeta {
 namespace {
-
-// Grid cell of one coordinate.  Float32, no contraction: (x + 1) rounded once,
-// then an exact power-of-two scale.
-__device__ __forceinline__ uint32_t quantise(float x, float scale, float umax) {
-    float t = __fmul_rn(__fadd_rn(x, 1.0f), scale);
-    float f = floorf(t);
-    f = fmaxf(f, 0.0f);      // also maps NaN to 0
-    f = fminf(f, umax);
-    return static_cast<uint32_t>(f);
-}
-
-// Spread the low 21 bits of x so that bit j moves to bit 3j.
-__device__ __forceinline__ uint64_t dilate3(uint64_t x) {
-    x &= 0x1fffffull;
-    x = (x | (x << 32)) & 0x001f00000000ffffull;
-    x = (x | (x << 16)) & 0x001f0000ff0000ffull;
-    x = (x | (x << 8)) & 0x100f00f00f00f00full;
-    x = (x | (x << 4)) & 0x10c30c30c30c30c3ull;
-    x = (x | (x << 2)) & 0x1249249249249249ull;
-    return x;
-}
-
-// Spread the low 32 bits of x so that bit j moves to bit 2j.
-__device__ __forceinline__ uint64_t dilate2(uint64_t x) {
-    x &= 0xffffffffull;
-    x = (x | (x << 16)) & 0x0000ffff0000ffffull;
-    x = (x | (x << 8)) & 0x00ff00ff00ff00ffull;
-    x = (x | (x << 4)) & 0x0f0f0f0f0f0f0f0full;
-    x = (x | (x << 2)) & 0x3333333333333333ull;
-    x = (x | (x << 1)) & 0x5555555555555555ull;
-    return x;
-}
 
 template <typename CodeT>
 __global__ void encode_kernel(const float *__restrict__ x, CodeT *__restrict__ codes,

@@ -152,3 +152,25 @@ def test_curve_calls_check_their_arguments(L):
                                     None, None) == 0
         assert L.zeta_select_topk_curves(ctypes.byref(e), 3, None, None, None, None, None) == 0
     assert zb.curve_axes(3, 6)[3] == [1, 0, 2]
+
+
+def test_project_encode_checks_its_arguments(L):
+    p = _prob(H=8)
+    P = ctypes.byref(p)
+    fake = ctypes.c_void_p(0x1000)
+    ok = zb.zeta_proj_t(512, 64)
+    args = [fake] * 11
+    assert L.zeta_project_encode(P, None, *args) == 1                        # no widths
+    assert L.zeta_project_encode(P, ctypes.byref(zb.zeta_proj_t(0, 64)), *args) == 1
+    assert L.zeta_project_encode(P, ctypes.byref(ok), None, *args[1:]) == 1  # null x
+    odd = [ctypes.c_void_p(0x1008)] + args[1:]
+    assert L.zeta_project_encode(P, ctypes.byref(ok), *odd) == 1             # x not 16-B aligned
+    for pj in (zb.zeta_proj_t(512, 32), zb.zeta_proj_t(500, 64)):             # F != 64, D % 64
+        assert L.zeta_project_encode(P, ctypes.byref(pj), *args) == 2
+    p6 = _prob(H=6)
+    assert L.zeta_project_encode(ctypes.byref(p6), ctypes.byref(ok), *args) == 2   # H % 4
+    e = _prob(B=0)
+    assert L.zeta_project_encode(ctypes.byref(e), ctypes.byref(ok), *([None] * 11)) == 0
+    # the binding's marshalling matches the C signature (empty problem: no launch)
+    pe = zb.problem(0, 8, 1024, 3, 64, 16, 128, 10, "bf16")
+    zb.zeta_project_encode(pe, 512, 64, *([None] * 9), stream=0)

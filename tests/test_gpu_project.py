@@ -1,0 +1,89 @@
+"""GPU parity of the projection front end fused with the encode (two-layer
+network per head, OpenReview discussion of "ZETA: Leveraging Z-order Curves
+for Efficient Top-k Attention", reply A "LLMs impact the selection of d_K").
+
+Coordinates are compared with the oracle's double-precision projection of the
+same bf16 inputs; the codes are compared bit for bit with the oracle's encode
+of the coordinates the device produced (the quantiser's decision is taken on
+the same float32 value on both sides)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from order_retrieval_gb300 import binding as zb
+from order_retrieval_gb300 import workloads as W
+
+from gpu_util import codes_np
+
+pytestmark = [
+    pytest.mark.gpu,
+    pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU"),
+]
+
+# First layer: bf16 products are exact in float32, so the device result differs
+# from the double-precision one by float32 accumulation (D terms of size ~1/sqrt(D))
+# and a few float32 operations after it; 2e-5 absolute covers D = 512 with room.
+COORD_ATOL = 2e-5
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).cuda()
+
+
+def run_projection(pj, g, bits=None):
+    w = pj.base if bits is None else pj.base.replace(bits=bits)
+    p = zb.problem_of(w)
+    S = w.B * w.H * w.N
+    x, w1 = _bf16(g["x"]).reshape(-1), _bf16(g["W1"]).reshape(-1)
+    b1, w2, b2 = (torch.from_numpy(g[n]).cuda().reshape(-1) for n in ("b1", "W2", "b2"))
+    q = torch.empty(S * w.d_K, dtype=torch.float32, device="cuda")
+    k = torch.empty_like(q)
+    qc = torch.empty(S, dtype=zb.code_dtype(p), device="cuda")
+    kc = torch.empty_like(qc)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    zb.zeta_project_encode(p, pj.D, pj.F, x, w1, b1, w2, b2, q, k, qc, kc, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    shape = (w.B, w.H, w.N, w.d_K)
+    return (w, q.cpu().numpy().reshape(shape), k.cpu().numpy().reshape(shape),
+            codes_np(qc).reshape(shape[:3]), codes_np(kc).reshape(shape[:3]))
+
+
+def _check(pj, g, w, q, k, qc, kc, tokens):
+    x = W.bf16_bits_to_f32(g["x"]).astype(np.float64)
+    for pr, (y, codes) in enumerate(((q, qc), (k, kc))):
+        W1 = W.bf16_bits_to_f32(g["W1"][pr]).astype(np.float64)
+        for b in range(w.B):
+            ref = oracle.project(x[b][tokens], W1, g["b1"][pr], g["W2"][pr], g["b2"][pr])
+            got = y[b][:, tokens].transpose(1, 0, 2)                 # [T, H, d_K]
+            err = np.abs(got - ref).max()
+            assert err <= COORD_ATOL, f"projection {pr}: max err {err:.3e}"
+            want = oracle.encode(got, w.bits)                          # [T, H]
+            assert np.array_equal(codes[b][:, tokens].T, want)
+
+
+@pytest.mark.parametrize("bits", [10, 12])
+def test_small_projection_all_tokens(bits):
+    pj = W.PROJ_SMALL
+    g = W.generate_projection(pj)
+    w, q, k, qc, kc = run_projection(pj, g, bits)
+    _check(pj, g, w, q, k, qc, kc, np.arange(w.N))
+
+
+def test_ragged_token_count():
+    """B*N not a multiple of the 128-token tile: the tail rows are masked."""
+    pj = W.Projection("proj_ragged", W.TRAIN.replace(B=3, H=8, N=200, C=40, k=8), 192, 64, 7)
+    g = W.generate_projection(pj)
+    w, q, k, qc, kc = run_projection(pj, g)
+    _check(pj, g, w, q, k, qc, kc, np.arange(w.N))
+
+
+def test_training_scale_sampled():
+    """B=4, H=8, N=65536, D=512 (the training workload's tokens): sampled tokens."""
+    pj = W.PROJ
+    g = W.generate_projection(pj)
+    w, q, k, qc, kc = run_projection(pj, g)
+    rng = np.random.default_rng(9)
+    tokens = np.sort(np.concatenate([rng.choice(w.N, 60, replace=False), [0, 127, 128, w.N - 1]]))
+    _check(pj, g, w, q, k, qc, kc, tokens)
