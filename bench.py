@@ -415,6 +415,55 @@ def run_ours(args, w, rank, world):
             "fwd_ms": ms, "encode_sort_select_ms": sum(sel) / len(sel)}
         del pc
 
+    # --- projection front end fused with the encode (tcgen05), the training
+    # workload's tokens with D = 512 features: the kernel alone, then the whole
+    # forward from features (project, sort, select, attend)
+    pj = W.PROJ
+    gp = W.generate_projection(pj)
+    pp = zb.problem_of(pj.base)
+
+    def bf16_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).reshape(-1).to(dev)
+
+    xp, w1p = bf16_dev(gp["x"]), bf16_dev(gp["W1"])
+    b1p, w2p, b2p = (torch.from_numpy(gp[n]).reshape(-1).to(dev) for n in ("b1", "W2", "b2"))
+    plan_p = ZetaPlan(pp, dev, backward=False)
+    qp = torch.empty(pp.B * pp.H * pp.N * pp.d_K, dtype=torch.float32, device=dev)
+    kp = torch.empty_like(qp)
+
+    def project():
+        zb.zeta_project_encode(pp, pj.D, pj.F, xp, w1p, b1p, w2p, b2p, qp, kp, plan_p.q_codes,
+                               plan_p.k_codes, plan_p.status)
+
+    for _ in range(warm):
+        project()
+    pr_ms, pf_ms = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        e = [ev() for _ in range(3)]
+        e[0].record()
+        project()
+        e[1].record()
+        zb.zeta_sort_chunks(pp, plan_p.k_codes, plan_p.prefix_codes, plan_p.prefix_idx,
+                            plan_p.sort_ws)
+        zb.zeta_select_topk(pp, plan_p.q_codes, plan_p.prefix_codes, plan_p.prefix_idx,
+                            plan_p.idx)
+        zb.zeta_attend_fwd(pp, qp, kp, v, gamma, plan_p.idx, plan_p.out, plan_p.rowsum,
+                           plan_p.status)
+        e[2].record()
+        e[2].synchronize()
+        pr_ms.append(e[0].elapsed_time(e[1]))
+        pf_ms.append(e[0].elapsed_time(e[2]))
+    if int(plan_p.status.item()) != 0:
+        raise RuntimeError(f"device status {plan_p.status.item()} (projection)")
+    proj_ms = sum(pr_ms) / len(pr_ms)
+    proj_flop = 2.0 * pp.B * pp.N * pj.D * (2 * pp.H * pj.F)
+    variants["projection"] = {
+        "workload": pj.name, "kernel_ms": proj_ms, "tflops": proj_flop / (proj_ms * 1e-3) / 1e12,
+        "fwd_from_features_tokens_per_s": tokens / (sum(pf_ms) / len(pf_ms) * 1e-3),
+        "fwd_from_features_ms": sum(pf_ms) / len(pf_ms)}
+    del plan_p
+
     # --- alternative weight kernels (softmax of -d2/gamma^2, inverse Euclidean)
     # on the timed workload: the whole step, captured and timed like the main one
     for weight in ("softmax", "inv_euclid"):
@@ -492,6 +541,13 @@ def run_ours(args, w, rank, world):
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": None,
                      "algorithmic_bytes": fb, "peak_source": peak_src},
+        "roofline_projection": {
+            "kernel": "project_encode_tc (tcgen05, B=4 N=65536 D=512 F=64, L2 flushed)",
+            "bound": "tensor", "achieved": variants["projection"]["tflops"],
+            "peak": peaks.get("bf16_tflops", 1900.0), "unit": "TFLOP/s",
+            "frac": variants["projection"]["tflops"] / peaks.get("bf16_tflops", 1900.0),
+            "peak_source": "measured (cuBLAS bf16 burst)" if "bf16_tflops" in peaks
+                           else "fallback"},
         "roofline_train": {
             "attend_fwd": {"achieved": fbt / (per_call["attend_fwd"] * 1e-3) / 1e9,
                            "frac": fbt / (per_call["attend_fwd"] * 1e-3) / 1e9 / hbm_peak,

@@ -10,18 +10,27 @@
 //   y_c = tanh(W2[hd][c] . h + b2[hd][c]),             c < d_K
 // then y is written out and quantised into the token's Morton code.
 //
-// One CTA computes 128 tokens x 256 hidden units (four heads of F = 64) of one
-// projection: the first layer is a K = D contraction on tcgen05.mma (M = 128,
-// N = 256, K = 16 per instruction, bf16 in, f32 accumulator in 256 TMEM
-// columns).  x and W1 tiles of 64 K-elements (128 bytes, the 128-byte swizzle
-// row) are brought by 2-D TMA loads into a three-stage ring; one thread waits
-// for a stage, issues its four MMAs and commits them to the stage's "empty"
-// barrier, then refills the stage of the previous step.  The epilogue runs on
-// all four warps: each thread owns one token (one TMEM lane), reads its 64
-// accumulators of a head with tcgen05.ld, applies bias and ReLU, the 64 -> d_K
-// second layer from shared memory, tanh, and the quantiser + bit interleave.
-// Every wait is bounded; a wait that gives up records ZETA_ERR_DEVICE_TIMEOUT,
-// drains the loads in flight (again bounded) and frees the TMEM before exiting.
+// Work unit: 128 tokens x 256 hidden units (four heads of F = 64) of one
+// projection; the first layer is a K = D contraction on tcgen05.mma (M = 128,
+// N = 256, K = 16 per instruction, bf16 in, f32 accumulator in TMEM).  The
+// kernel is persistent (one CTA per SM walking the units, the four units of a
+// token tile next to each other so the x tile is reused from L2) and
+// warp-specialised:
+//   warp 0    TMA producer: x and W1 tiles of 64 K-elements (128 bytes, the
+//             128-byte swizzle row) into a three-stage ring;
+//   warp 1    MMA issuer (one thread) and owner of the TMEM allocation: two
+//             256-column accumulators, so a unit's MMAs run while the previous
+//             unit's epilogue drains the other accumulator;
+//   warps 2-5 epilogue: each thread owns one token (one TMEM lane), reads its
+//             64 accumulators of a head with tcgen05.ld, applies bias and ReLU,
+//             the 64 -> d_K second layer (weights staged in shared memory),
+//             tanh, and the quantiser + bit interleave.
+// Hand-offs are mbarriers: full/empty per ring stage (TMA -> MMA -> TMA), and
+// full/empty per accumulator (MMA commit -> epilogue -> MMA).  Every wait is
+// bounded; a wait that gives up records ZETA_ERR_DEVICE_TIMEOUT and raises an
+// abort flag that ends every role's loop; the producer then waits (bounded)
+// for its loads in flight and the MMA thread for its MMAs before the TMEM is
+// freed.
 #include <cudaTypedefs.h>
 
 #include "tc05.cuh"
@@ -30,69 +39,93 @@
 namespace zeta {
 namespace {
 
-constexpr int BM = 128;                   // tokens per CTA
-constexpr int BN = 256;                   // hidden units per CTA
+constexpr int BM = 128;                   // tokens per unit
+constexpr int BN = 256;                   // hidden units per unit
 constexpr int BK = 64;                    // K elements per stage (128 bytes of bf16)
 constexpr int FH = 64;                    // hidden units per head
-constexpr int HPC = BN / FH;              // heads per CTA
+constexpr int HPC = BN / FH;              // heads per unit
 constexpr int STAGES = 3;
-constexpr int PTHREADS = 128;
+constexpr int PTHREADS = 192;             // producer, MMA, four epilogue warps
+constexpr int MAX_H = 16;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = BN * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;    // two accumulators
 
 struct ProjHead {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
-    uint64_t done;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
     uint32_t tmem_base;
-    int32_t err;
-    float b1[BN];
-    float w2[HPC][4][FH];
-    float b2[HPC][4];
+    int32_t abort;
 };
 
-constexpr size_t kProjSmem = 1024 + STAGES * STAGE_BYTES + sizeof(ProjHead);
+// Second-layer parameters of both projections, staged once per CTA.
+struct ProjParams {
+    float b1[2][MAX_H * FH];
+    float w2[2][MAX_H][4][FH];            // d_K padded to 4 with zeros
+    float b2[2][MAX_H][4];
+};
 
-template <typename CodeT>
+constexpr size_t kProjSmem = 1024 + STAGES * STAGE_BYTES + sizeof(ProjHead) + sizeof(ProjParams);
+
+__device__ __forceinline__ bool aborted(const ProjHead &sh) {
+    return *reinterpret_cast<const volatile int32_t *>(&sh.abort) != 0;
+}
+
+__device__ __forceinline__ bool wait_or_abort(ProjHead &sh, uint64_t *bar, uint32_t parity,
+                                              int32_t *status) {
+    if (mbar_wait_bounded(bar, parity)) return true;
+    *reinterpret_cast<volatile int32_t *>(&sh.abort) = 1;
+    set_status(status, ZETA_ERR_DEVICE_TIMEOUT);
+    return false;
+}
+
+template <typename CodeT, int DK>
 __global__ void __launch_bounds__(PTHREADS, 1)
 project_encode_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                   const float *__restrict__ b1, const float *__restrict__ w2,
                   const float *__restrict__ b2, float *__restrict__ qo, float *__restrict__ ko,
-                  CodeT *__restrict__ qc, CodeT *__restrict__ kc, int64_t M, int N, int H, int dK,
-                  int D, int bits, int32_t *status) {
+                  CodeT *__restrict__ qc, CodeT *__restrict__ kc, int64_t M, int N, int H, int D,
+                  int bits, int32_t *status) {
     extern __shared__ unsigned char dsm[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(dsm) + 1023) & ~uintptr_t(1023));
     ProjHead &sh = *reinterpret_cast<ProjHead *>(base + STAGES * STAGE_BYTES);
+    ProjParams &pp = *reinterpret_cast<ProjParams *>(base + STAGES * STAGE_BYTES +
+                                                    sizeof(ProjHead));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t m0 = (int64_t)blockIdx.x * BM;
-    const int ct = blockIdx.y;
-    const int tiles_per_proj = H * FH / BN;
-    const int pr = ct / tiles_per_proj;               // 0: queries, 1: keys
-    const int h0 = (ct % tiles_per_proj) * HPC;
+    const int n_ct = 2 * H * FH / BN;                 // units per token tile
+    const int64_t n_mt = (M + BM - 1) / BM;
+    const int64_t units = n_mt * n_ct;
     const int KB = D / BK;
 
-    for (int t = tid; t < BN; t += PTHREADS) sh.b1[t] = b1[((int64_t)pr * H + h0) * FH + t];
-    for (int t = tid; t < HPC * 4 * FH; t += PTHREADS) {
-        const int hh = t / (4 * FH), c = (t / FH) & 3, f = t % FH;
-        sh.w2[hh][c][f] = c < dK ? w2[(((int64_t)pr * H + h0 + hh) * dK + c) * FH + f] : 0.f;
+    for (int t = tid; t < 2 * H * FH; t += PTHREADS) pp.b1[t / (H * FH)][t % (H * FH)] = b1[t];
+    for (int t = tid; t < 2 * H * 4 * FH; t += PTHREADS) {
+        const int pr = t / (H * 4 * FH), hd = (t / (4 * FH)) % H, c = (t / FH) & 3, f = t % FH;
+        pp.w2[pr][hd][c][f] = c < DK ? w2[(((int64_t)pr * H + hd) * DK + c) * FH + f] : 0.f;
     }
-    if (tid < HPC * 4) {
-        const int hh = tid >> 2, c = tid & 3;
-        sh.b2[hh][c] = c < dK ? b2[((int64_t)pr * H + h0 + hh) * dK + c] : 0.f;
+    for (int t = tid; t < 2 * H * 4; t += PTHREADS) {
+        const int pr = t / (H * 4), hd = (t / 4) % H, c = t & 3;
+        pp.b2[pr][hd][c] = c < DK ? b2[((int64_t)pr * H + hd) * DK + c] : 0.f;
     }
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&sh.full[s], 1);
             mbar_init(&sh.empty[s], 1);
         }
-        mbar_init(&sh.done, 1);
-        sh.err = 0;
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sh.acc_full[a], 1);
+            mbar_init(&sh.acc_empty[a], 4);           // one arrive per epilogue warp
+        }
+        mbar_init(&sh.drain, 1);
+        sh.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {
-        tmem_alloc(&sh.tmem_base, BN);
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
     tc05_fence_before();
@@ -100,114 +133,139 @@ project_encode_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constan
     tc05_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
-    // ------------------------------------------------ producer + MMA issue ---
-    if (tid == 0) {
-        auto load = [&](int kb) {
-            const int s = kb % STAGES;
-            unsigned char *sa = base + s * STAGE_BYTES;
-            mbar_arrive_expect_tx(&sh.full[s], STAGE_BYTES);
-            tma_load_2d(sa, &xmap, kb * BK, (int)m0, &sh.full[s]);
-            tma_load_2d(sa + A_BYTES, &wmap, kb * BK, ct * BN, &sh.full[s]);
-        };
-        const int pre = KB < STAGES ? KB : STAGES;
-        for (int kb = 0; kb < pre; ++kb) load(kb);
-        int issued = pre, consumed = 0;
-        bool ok = true;
-        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % STAGES;
-            if (!mbar_wait_bounded(&sh.full[s], (uint32_t)(kb / STAGES) & 1u)) {
-                ok = false;
-                break;
-            }
-            consumed = kb + 1;
-            tc05_fence_after();
-            const uint32_t sa = smem_u32(base + s * STAGE_BYTES);
-            const uint64_t ad = sdesc_k128(sa), bd = sdesc_k128(sa + A_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)   // 32 bytes of K per instruction
-                umma_bf16(tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0);
-            umma_commit(&sh.empty[s]);
-            const int kp = kb - 1;                  // refill the previous step's stage
-            if (kp >= 0 && kp + STAGES < KB) {
-                if (!mbar_wait_bounded(&sh.empty[kp % STAGES], (uint32_t)(kp / STAGES) & 1u)) {
-                    ok = false;
-                    break;
+    if (warp == 0) {
+        // ------------------------------------------------------ producer ---
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t u = blockIdx.x; u < units && !aborted(sh); u += gridDim.x) {
+                const int mt = (int)(u / n_ct), ct = (int)(u % n_ct);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    if (!wait_or_abort(sh, &sh.empty[s], ((it / STAGES) & 1u) ^ 1u, status)) break;
+                    unsigned char *sa = base + s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&sh.full[s], STAGE_BYTES);
+                    tma_load_2d(sa, &xmap, kb * BK, mt * BM, &sh.full[s]);
+                    tma_load_2d(sa + A_BYTES, &wmap, kb * BK, ct * BN, &sh.full[s]);
                 }
-                load(kp + STAGES);
-                issued = kp + STAGES + 1;
+            }
+            if (aborted(sh)) {
+                // the last load into each stage completes after all earlier ones
+                for (uint32_t s = 0; s < STAGES; ++s) {
+                    if (it <= s) continue;
+                    const uint32_t last = it - 1 - ((it - 1 + STAGES - s) % STAGES);
+                    mbar_wait_bounded(&sh.full[s], (last / STAGES) & 1u);
+                }
             }
         }
-        if (ok) {
-            umma_commit(&sh.done);
-        } else {
-            sh.err = 1;
-            set_status(status, ZETA_ERR_DEVICE_TIMEOUT);
-            for (int kb = consumed; kb < issued; ++kb)      // loads still in flight
-                mbar_wait_bounded(&sh.full[kb % STAGES], (uint32_t)(kb / STAGES) & 1u);
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA ---
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            uint32_t it = 0, lt = 0;
+            bool issued = false;
+            for (int64_t u = blockIdx.x; u < units && !aborted(sh); u += gridDim.x, ++lt) {
+                const uint32_t a = lt & 1u;
+                if (!wait_or_abort(sh, &sh.acc_empty[a], ((lt >> 1) & 1u) ^ 1u, status)) break;
+                tc05_fence_after();
+                const uint32_t dt = tmem + a * BN;
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    if (!wait_or_abort(sh, &sh.full[s], (it / STAGES) & 1u, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc05_fence_after();
+                    const uint32_t sa = smem_u32(base + s * STAGE_BYTES);
+                    const uint64_t ad = sdesc_k128(sa), bd = sdesc_k128(sa + A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)   // 32 bytes of K per instruction
+                        umma_bf16(dt, ad + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0);
+                    issued = true;
+                    umma_commit(&sh.empty[s]);
+                }
+                if (!ok) break;
+                umma_commit(&sh.acc_full[a]);
+            }
+            if (issued && aborted(sh)) {
+                umma_commit(&sh.drain);
+                mbar_wait_bounded(&sh.drain, 0);
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue ---
+        const int quarter = warp & 3;                     // TMEM lanes 32*quarter ..
+        const int row = quarter * 32 + lane;
+        const float scale = __int_as_float((126 + bits) << 23);   // 2^(bits-1)
+        const float umax = static_cast<float>((1u << bits) - 1u);
+        uint32_t lt = 0;
+        for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
+            if (__any_sync(kFull, aborted(sh))) break;
+            const uint32_t a = lt & 1u;
+            const bool ok = wait_or_abort(sh, &sh.acc_full[a], (lt >> 1) & 1u, status);
+            if (!__all_sync(kFull, ok)) break;
+            tc05_fence_after();
+            const int mt = (int)(u / n_ct), ct = (int)(u % n_ct);
+            const int pr = ct / (n_ct / 2);               // 0: queries, 1: keys
+            const int h0 = (ct % (n_ct / 2)) * HPC;
+            const int64_t m = (int64_t)mt * BM + row;
+            const bool valid = m < M;
+            const int64_t bsl = valid ? m / N : 0;
+            const int n = valid ? (int)(m % N) : 0;
+            float *outp = pr == 0 ? qo : ko;
+            CodeT *codep = pr == 0 ? qc : kc;
+            for (int hh = 0; hh < HPC; ++hh) {
+                const int hd = h0 + hh;
+                uint32_t r0[32], r1[32];
+                const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + a * BN +
+                                       (uint32_t)(hh * FH);
+                tmem_ld32(taddr, r0);
+                tmem_ld32(taddr + 32, r1);
+                tmem_ld_wait();
+                float y[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) y[c] = pp.b2[pr][hd][c];
+                const float *bb = pp.b1[pr] + hd * FH;
+#pragma unroll
+                for (int f = 0; f < FH; ++f) {
+                    const float acc = __uint_as_float(f < 32 ? r0[f] : r1[f - 32]);
+                    const float hv = fmaxf(acc + bb[f], 0.f);
+#pragma unroll
+                    for (int c = 0; c < DK; ++c) y[c] = __fmaf_rn(pp.w2[pr][hd][c][f], hv, y[c]);
+                }
+                if (valid) {
+                    const int64_t tok = (bsl * H + hd) * (int64_t)N + n;
+                    uint32_t ucell[4];
+#pragma unroll
+                    for (int c = 0; c < DK; ++c) {
+                        const float yc = tanhf(y[c]);
+                        outp[tok * DK + c] = yc;
+                        ucell[c] = quantise(yc, scale, umax);
+                    }
+                    uint64_t code = 0;
+                    if constexpr (DK == 3) {
+                        code = morton3(ucell[0], ucell[1], ucell[2]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < DK; ++c)
+                            for (int j = 0; j < bits; ++j)
+                                code |= static_cast<uint64_t>((ucell[c] >> j) & 1u)
+                                        << (j * DK + DK - 1 - c);
+                    }
+                    codep[tok] = static_cast<CodeT>(code);
+                }
+            }
+            tc05_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.acc_empty[a]);
         }
     }
     __syncwarp();
-    __syncthreads();
-
-    // --------------------------------------------------------- epilogue ---
-    bool good = sh.err == 0;
-    if (good && !mbar_wait_bounded(&sh.done, 0)) {
-        good = false;
-        set_status(status, ZETA_ERR_DEVICE_TIMEOUT);
-    }
-    tc05_fence_after();
-    good = __all_sync(kFull, good);
-    if (good) {
-        const int row = warp * 32 + lane;                  // this thread's TMEM lane
-        const int64_t m = m0 + row;
-        const bool valid = m < M;
-        const int64_t bsl = valid ? m / N : 0;
-        const int n = valid ? (int)(m % N) : 0;
-        float *outp = pr == 0 ? qo : ko;
-        CodeT *codep = pr == 0 ? qc : kc;
-        const float scale = __int_as_float((126 + bits) << 23);   // 2^(bits-1)
-        const float umax = static_cast<float>((1u << bits) - 1u);
-        for (int hh = 0; hh < HPC; ++hh) {
-            float y[4] = {sh.b2[hh][0], sh.b2[hh][1], sh.b2[hh][2], sh.b2[hh][3]};
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(hh * FH + half * 32), r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int f = half * 32 + j;
-                    const float hv = fmaxf(__uint_as_float(r[j]) + sh.b1[hh * FH + f], 0.f);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) y[c] = __fmaf_rn(sh.w2[hh][c][f], hv, y[c]);
-                }
-            }
-            if (valid) {
-                const int64_t tok = (bsl * H + h0 + hh) * (int64_t)N + n;
-                uint32_t u[4];
-                for (int c = 0; c < dK; ++c) {
-                    const float yc = tanhf(y[c]);
-                    outp[tok * dK + c] = yc;
-                    u[c] = quantise(yc, scale, umax);
-                }
-                uint64_t code = 0;
-                if (dK == 3) {
-                    code = morton3(u[0], u[1], u[2]);
-                } else {
-                    for (int c = 0; c < dK; ++c)
-                        for (int j = 0; j < bits; ++j)
-                            code |= static_cast<uint64_t>((u[c] >> j) & 1u) << (j * dK + dK - 1 - c);
-                }
-                codep[tok] = static_cast<CodeT>(code);
-            }
-        }
-    }
     tc05_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         tc05_fence_after();
-        tmem_dealloc(tmem, BN);
+        tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -237,11 +295,50 @@ bool bf16_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <typename CodeT, int DK>
+cudaError_t launch_proj(const Prob &p, int D, const CUtensorMap &xmap, const CUtensorMap &wmap,
+                        const float *b1, const float *w2, const float *b2, float *q, float *k,
+                        void *q_codes, void *k_codes, int32_t *status, cudaStream_t st) {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(project_encode_tc<CodeT, DK>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kProjSmem);
+        if (e != cudaSuccess) {
+            sms = 0;
+            return e;
+        }
+    }
+    const int64_t M = (int64_t)p.B * p.N;
+    const int64_t units = (M + BM - 1) / BM * (2 * p.H * FH / BN);
+    const unsigned grid = (unsigned)(units < sms ? units : sms);
+    project_encode_tc<CodeT, DK><<<grid, PTHREADS, kProjSmem, st>>>(
+        xmap, wmap, b1, w2, b2, q, k, static_cast<CodeT *>(q_codes), static_cast<CodeT *>(k_codes),
+        M, p.N, p.H, D, p.bits, status);
+    return cudaGetLastError();
+}
+
+template <typename CodeT>
+cudaError_t launch_proj_dk(const Prob &p, int D, const CUtensorMap &xmap,
+                           const CUtensorMap &wmap, const float *b1, const float *w2,
+                           const float *b2, float *q, float *k, void *qc, void *kc,
+                           int32_t *status, cudaStream_t st) {
+    switch (p.dK) {
+        case 1: return launch_proj<CodeT, 1>(p, D, xmap, wmap, b1, w2, b2, q, k, qc, kc, status, st);
+        case 2: return launch_proj<CodeT, 2>(p, D, xmap, wmap, b1, w2, b2, q, k, qc, kc, status, st);
+        case 3: return launch_proj<CodeT, 3>(p, D, xmap, wmap, b1, w2, b2, q, k, qc, kc, status, st);
+        default: return launch_proj<CodeT, 4>(p, D, xmap, wmap, b1, w2, b2, q, k, qc, kc, status, st);
+    }
+}
+
 }  // namespace
 
 bool project_tc_supported(const Prob &p, int D, int F) {
-    return F == FH && D >= BK && D % BK == 0 && (p.H * FH) % BN == 0 && p.dK <= 4 &&
-           p.S * (int64_t)p.N <= INT32_MAX && tensor_map_encoder() != nullptr;
+    return F == FH && D >= BK && D % BK == 0 && (p.H * FH) % BN == 0 && p.H <= MAX_H &&
+           p.dK <= 4 && p.S * (int64_t)p.N <= INT32_MAX && tensor_map_encoder() != nullptr;
 }
 
 cudaError_t launch_project_tc(const Prob &p, int D, const void *x, const void *w1,
@@ -252,33 +349,11 @@ cudaError_t launch_project_tc(const Prob &p, int D, const void *x, const void *w
     CUtensorMap xmap, wmap;
     if (!bf16_map(&xmap, x, M, D, BM) || !bf16_map(&wmap, w1, 2LL * p.H * FH, D, BN))
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)(2 * p.H * FH / BN));
-    if (p.code64) {
-        static bool attr64 = false;
-        if (!attr64) {
-            cudaError_t e = cudaFuncSetAttribute(project_encode_tc<uint64_t>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)kProjSmem);
-            if (e != cudaSuccess) return e;
-            attr64 = true;
-        }
-        project_encode_tc<uint64_t><<<grid, PTHREADS, kProjSmem, st>>>(
-            xmap, wmap, b1, w2, b2, q, k, static_cast<uint64_t *>(q_codes),
-            static_cast<uint64_t *>(k_codes), M, p.N, p.H, p.dK, D, p.bits, status);
-    } else {
-        static bool attr32 = false;
-        if (!attr32) {
-            cudaError_t e = cudaFuncSetAttribute(project_encode_tc<uint32_t>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)kProjSmem);
-            if (e != cudaSuccess) return e;
-            attr32 = true;
-        }
-        project_encode_tc<uint32_t><<<grid, PTHREADS, kProjSmem, st>>>(
-            xmap, wmap, b1, w2, b2, q, k, static_cast<uint32_t *>(q_codes),
-            static_cast<uint32_t *>(k_codes), M, p.N, p.H, p.dK, D, p.bits, status);
-    }
-    return cudaGetLastError();
+    if (p.code64)
+        return launch_proj_dk<uint64_t>(p, D, xmap, wmap, b1, w2, b2, q, k, q_codes, k_codes,
+                                        status, st);
+    return launch_proj_dk<uint32_t>(p, D, xmap, wmap, b1, w2, b2, q, k, q_codes, k_codes, status,
+                                    st);
 }
 
 }  // namespace zeta

@@ -80,6 +80,11 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
 
+// Plain arrive (count 1) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // 2-D TMA tile load (box given by the tensor map) at element coordinates
 // (x inner, y outer); completion counted on `bar`.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y,

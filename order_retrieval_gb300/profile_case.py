@@ -1,10 +1,12 @@
 """Run whole ZETA steps on one workload, for profilers (ncu) and quick timing.
 
   python -m order_retrieval_gb300.profile_case [--workload NAME] [--B B] \
-      [--steps K] [--warmup W] [--fwd-only]
+      [--steps K] [--warmup W] [--fwd-only] [--projection]
 
 Each step enqueues encode (q, k), sort, select, attend forward and (unless
---fwd-only) attend backward through the C ABI, then synchronises.  Prints the
+--fwd-only) attend backward through the C ABI, then synchronises.  With
+--projection a step is the fused two-layer projection + encode alone on the
+projection workload (B=4, N=65536, D=512 unless --B is given).  Prints the
 mean step time measured with CUDA events.
 """
 from __future__ import annotations
@@ -26,7 +28,10 @@ def main():
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--projection", action="store_true")
     a = ap.parse_args()
+    if a.projection:
+        return projection(a)
     w = W.ALL[a.workload]
     if a.B is not None:
         w = w.replace(B=a.B)
@@ -62,6 +67,47 @@ def main():
     if int(plan.status.item()) != 0:
         raise SystemExit(f"device status {plan.status.item()}")
     print(f"{w.name} B={w.B} step_ms={sum(ts) / len(ts):.3f}")
+
+
+def projection(a):
+    pj = W.PROJ
+    if a.B is not None:
+        pj = W.Projection(pj.name, pj.base.replace(B=a.B), pj.D, pj.F, pj.seed)
+    w = pj.base
+    g = W.generate_projection(pj)
+    p = zb.problem_of(w)
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).view(torch.bfloat16).reshape(-1).cuda()
+
+    x, w1 = bf(g["x"]), bf(g["W1"])
+    b1, w2, b2 = (torch.from_numpy(g[n]).reshape(-1).cuda() for n in ("b1", "W2", "b2"))
+    S = w.B * w.H * w.N
+    q = torch.empty(S * w.d_K, dtype=torch.float32, device="cuda")
+    k = torch.empty_like(q)
+    qc = torch.empty(S, dtype=zb.code_dtype(p), device="cuda")
+    kc = torch.empty_like(qc)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def step():
+        zb.zeta_project_encode(p, pj.D, pj.F, x, w1, b1, w2, b2, q, k, qc, kc, st)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(a.steps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        step()
+        e.record()
+        torch.cuda.synchronize()
+        ts.append(s.elapsed_time(e))
+    if int(st.item()) != 0:
+        raise SystemExit(f"device status {st.item()}")
+    flop = 2.0 * w.B * w.N * pj.D * 2 * w.H * pj.F
+    ms = sum(ts) / len(ts)
+    print(f"{pj.name} B={w.B} kernel_ms={ms:.4f} tflops={flop / ms / 1e9:.1f}")
 
 
 if __name__ == "__main__":
