@@ -237,7 +237,7 @@ typedef struct {
  *   q_codes, k_codes  out: code type of the problem [B, H, N]
  *   dev_status  optional int32 device word (ZETA_ERR_DEVICE_TIMEOUT if a
  *               bounded wait of the kernel gave up)
- * Limits: F = 64, D a multiple of 64, H a multiple of 4, d_K <= 4, B*N < 2^31.
+ * Limits: F = 64, D a multiple of 64, H = 4 or 8, d_K <= 4, B*N < 2^31.
  * The first layer runs on the tensor cores with bf16 inputs and float32
  * accumulation; the rest in float32.
  * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED (outside the limits).

@@ -17,14 +17,16 @@
 // token tile next to each other so the x tile is reused from L2) and
 // warp-specialised:
 //   warp 0    TMA producer: x and W1 tiles of 64 K-elements (128 bytes, the
-//             128-byte swizzle row) into a three-stage ring;
+//             128-byte swizzle row) into a four-stage ring;
 //   warp 1    MMA issuer (one thread) and owner of the TMEM allocation: two
 //             256-column accumulators, so a unit's MMAs run while the previous
 //             unit's epilogue drains the other accumulator;
-//   warps 2-5 epilogue: each thread owns one token (one TMEM lane), reads its
-//             64 accumulators of a head with tcgen05.ld, applies bias and ReLU,
-//             the 64 -> d_K second layer (weights staged in shared memory),
-//             tanh, and the quantiser + bit interleave.
+//   warps 2-9 epilogue: two warps per TMEM lane quarter, each taking two of
+//             the unit's four heads; a thread owns one token (one TMEM lane),
+//             reads its 64 accumulators of a head with tcgen05.ld, applies bias
+//             and ReLU, the 64 -> d_K second layer (weights staged in shared
+//             memory, packed f32x2 FMAs), tanh, and the quantiser + bit
+//             interleave.
 // Hand-offs are mbarriers: full/empty per ring stage (TMA -> MMA -> TMA), and
 // full/empty per accumulator (MMA commit -> epilogue -> MMA).  Every wait is
 // bounded; a wait that gives up records ZETA_ERR_DEVICE_TIMEOUT and raises an
@@ -44,9 +46,10 @@ constexpr int BN = 256;                   // hidden units per unit
 constexpr int BK = 64;                    // K elements per stage (128 bytes of bf16)
 constexpr int FH = 64;                    // hidden units per head
 constexpr int HPC = BN / FH;              // heads per unit
-constexpr int STAGES = 3;
-constexpr int PTHREADS = 192;             // producer, MMA, four epilogue warps
-constexpr int MAX_H = 16;
+constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 8;
+constexpr int PTHREADS = 64 + 32 * EPI_WARPS;   // producer, MMA, epilogue warps
+constexpr int MAX_H = 8;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = BN * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -65,8 +68,8 @@ struct ProjHead {
 // Second-layer parameters of both projections, staged once per CTA.
 struct ProjParams {
     float b1[2][MAX_H * FH];
-    float w2[2][MAX_H][4][FH];            // d_K padded to 4 with zeros
-    float b2[2][MAX_H][4];
+    float4 w2[2][MAX_H][FH];              // (W2[0][f], .. W2[3][f]), d_K padded with zeros
+    float4 b2[2][MAX_H];
 };
 
 constexpr size_t kProjSmem = 1024 + STAGES * STAGE_BYTES + sizeof(ProjHead) + sizeof(ProjParams);
@@ -105,11 +108,13 @@ project_encode_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constan
     for (int t = tid; t < 2 * H * FH; t += PTHREADS) pp.b1[t / (H * FH)][t % (H * FH)] = b1[t];
     for (int t = tid; t < 2 * H * 4 * FH; t += PTHREADS) {
         const int pr = t / (H * 4 * FH), hd = (t / (4 * FH)) % H, c = (t / FH) & 3, f = t % FH;
-        pp.w2[pr][hd][c][f] = c < DK ? w2[(((int64_t)pr * H + hd) * DK + c) * FH + f] : 0.f;
+        reinterpret_cast<float *>(&pp.w2[pr][hd][f])[c] =
+            c < DK ? w2[(((int64_t)pr * H + hd) * DK + c) * FH + f] : 0.f;
     }
     for (int t = tid; t < 2 * H * 4; t += PTHREADS) {
         const int pr = t / (H * 4), hd = (t / 4) % H, c = t & 3;
-        pp.b2[pr][hd][c] = c < DK ? b2[((int64_t)pr * H + hd) * DK + c] : 0.f;
+        reinterpret_cast<float *>(&pp.b2[pr][hd])[c] =
+            c < DK ? b2[((int64_t)pr * H + hd) * DK + c] : 0.f;
     }
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -118,7 +123,7 @@ project_encode_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constan
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sh.acc_full[a], 1);
-            mbar_init(&sh.acc_empty[a], 4);           // one arrive per epilogue warp
+            mbar_init(&sh.acc_empty[a], EPI_WARPS);   // one arrive per epilogue warp
         }
         mbar_init(&sh.drain, 1);
         sh.abort = 0;
@@ -195,6 +200,7 @@ project_encode_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constan
     } else {
         // ---------------------------------------------------- epilogue ---
         const int quarter = warp & 3;                     // TMEM lanes 32*quarter ..
+        const int hhalf = (warp - 2) >> 2;                // heads 2*hhalf, 2*hhalf + 1
         const int row = quarter * 32 + lane;
         const float scale = __int_as_float((126 + bits) << 23);   // 2^(bits-1)
         const float umax = static_cast<float>((1u << bits) - 1u);
@@ -214,7 +220,8 @@ project_encode_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constan
             const int n = valid ? (int)(m % N) : 0;
             float *outp = pr == 0 ? qo : ko;
             CodeT *codep = pr == 0 ? qc : kc;
-            for (int hh = 0; hh < HPC; ++hh) {
+            for (int hq = 0; hq < HPC / 2; ++hq) {
+                const int hh = hhalf * (HPC / 2) + hq;
                 const int hd = h0 + hh;
                 uint32_t r0[32], r1[32];
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + a * BN +
@@ -222,17 +229,25 @@ project_encode_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constan
                 tmem_ld32(taddr, r0);
                 tmem_ld32(taddr + 32, r1);
                 tmem_ld_wait();
-                float y[4];
+                const float4 bz = pp.b2[pr][hd];
+                float2 y01 = make_float2(bz.x, bz.y), y23 = make_float2(bz.z, bz.w);
+                const float4 *bb = reinterpret_cast<const float4 *>(pp.b1[pr] + hd * FH);
+                const float4 *ww = pp.w2[pr][hd];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) y[c] = pp.b2[pr][hd][c];
-                const float *bb = pp.b1[pr] + hd * FH;
+                for (int f4 = 0; f4 < FH / 4; ++f4) {
+                    const float4 b4 = bb[f4];
+                    const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-                for (int f = 0; f < FH; ++f) {
-                    const float acc = __uint_as_float(f < 32 ? r0[f] : r1[f - 32]);
-                    const float hv = fmaxf(acc + bb[f], 0.f);
-#pragma unroll
-                    for (int c = 0; c < DK; ++c) y[c] = __fmaf_rn(pp.w2[pr][hd][c][f], hv, y[c]);
+                    for (int e = 0; e < 4; ++e) {
+                        const int f = f4 * 4 + e;
+                        const float acc = __uint_as_float(f < 32 ? r0[f] : r1[f - 32]);
+                        const float2 hv = dup2(fmaxf(acc + bv[e], 0.f));
+                        const float4 w = ww[f];
+                        y01 = fma2(make_float2(w.x, w.y), hv, y01);
+                        if constexpr (DK > 2) y23 = fma2(make_float2(w.z, w.w), hv, y23);
+                    }
                 }
+                const float y[4] = {y01.x, y01.y, y23.x, y23.y};
                 if (valid) {
                     const int64_t tok = (bsl * H + hd) * (int64_t)N + n;
                     uint32_t ucell[4];
