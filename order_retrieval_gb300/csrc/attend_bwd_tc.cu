@@ -232,9 +232,14 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
 
     // ---------------------------------------------------- window part ---
     // A pass covers up to 64 selected keys.  Lane L owns slots L and L+32 (index,
-    // coordinates, the pair's Cauchy terms); four lanes form g_ij for one value
-    // row (two 16-byte slices each, a 2-shuffle reduction, eight rows per warp
-    // step) and the owner picks it up with one shuffle.  The next query's
+    // coordinates, the pair's weight terms).  The dot products g_ij = dO_i . v_j
+    // run on the tensor cores: for 16 selected keys, G = V_J . dO_i is one
+    // m16n8k16 mma per 16 dimensions, A the gathered value rows and dO_i in
+    // column 0 of B.  A dot product does not depend on the order of the
+    // dimensions, so each lane's two 16-byte slices of a row (slices 2t, 2t+1
+    // for t = lane % 4) serve as its A fragments directly, with dO_i's slices
+    // of the same numbers in B: no unpacking, no shuffle reductions.  The
+    // owner picks g up from the lane holding column 0.  The next query's
     // indices are fetched while this one runs.
     const int g4 = lane >> 2, s4 = lane & 3;
     const int wq0 = i0 + warp * 16;
@@ -260,13 +265,11 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
             float qi[4];
 #pragma unroll
             for (int d = 0; d < 4; ++d) qi[d] = d < DK ? qb[(int64_t)i * DK + d] : 0.f;
-            float2 do2[8];                              // dO_i[16 s4 .. 16 s4 + 16)
-            {
+            uint4 doa = make_uint4(0u, 0u, 0u, 0u), dob = doa;   // B column 0: lanes 0..3
+            if (g4 == 0) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(db + (int64_t)i * DV + s4 * 16);
-                const uint4 r0 = src[0], r1 = src[1];
-                const uint32_t uw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) do2[e] = bf2_to_f2(uw[e]);
+                doa = src[0];
+                dob = src[1];
             }
             for (int t0 = 0; t0 < k; t0 += 64) {
                 int j[2] = {jn[0], jn[1]};
@@ -282,36 +285,52 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     kk[s] = j[s] >= 0 ? load_k4(kb + (int64_t)j[s] * DK, DK)
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                const int nu = min(8, (k - t0 + 7) >> 3);   // 8-row steps in this pass
-                uint4 buf[16];
+                const int nmt = min(4, (k - t0 + 15) >> 4);  // 16-key tiles in this pass
+                uint4 buf[4][4];                    // rows g, g+8 of tile mt: slices 2t, 2t+1
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int jr = __shfl_sync(kFull, j[u >> 2], (u * 8 + g4) & 31);
-                    const bool ok = u < nu && jr >= 0;
-                    const uint4 *src = reinterpret_cast<const uint4 *>(vb + (int64_t)jr * DV + s4 * 16);
-                    buf[2 * u] = ok ? ld_stream16(src) : make_uint4(0u, 0u, 0u, 0u);
-                    buf[2 * u + 1] = ok ? ld_stream16(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+                for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int slot = 16 * mt + 8 * h + g4;
+                        const int jr = __shfl_sync(kFull, j[mt >> 1], slot & 31);
+                        const bool ok = mt < nmt && jr >= 0;
+                        const uint4 *src =
+                            reinterpret_cast<const uint4 *>(vb + (int64_t)jr * DV + s4 * 16);
+                        buf[mt][2 * h] = ok ? ld_stream16(src) : make_uint4(0u, 0u, 0u, 0u);
+                        buf[mt][2 * h + 1] = ok ? ld_stream16(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
-                float gown[2] = {0.f, 0.f};
+                float cg[4][4];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (u < nu) {
-                        const uint32_t uw[8] = {buf[2 * u].x, buf[2 * u].y, buf[2 * u].z,
-                                                buf[2 * u].w, buf[2 * u + 1].x, buf[2 * u + 1].y,
-                                                buf[2 * u + 1].z, buf[2 * u + 1].w};
-                        float2 ga = mul2(do2[0], bf2_to_f2(uw[0]));
-                        float2 gb2 = mul2(do2[1], bf2_to_f2(uw[1]));
+                for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-                        for (int e = 2; e < 8; e += 2) {
-                            ga = fma2(do2[e], bf2_to_f2(uw[e]), ga);
-                            gb2 = fma2(do2[e + 1], bf2_to_f2(uw[e + 1]), gb2);
+                    for (int e = 0; e < 4; ++e) cg[mt][e] = 0.f;
+                    if (mt < nmt) {
+                        const uint32_t ra0[4] = {buf[mt][0].x, buf[mt][0].y, buf[mt][0].z, buf[mt][0].w};
+                        const uint32_t ra1[4] = {buf[mt][1].x, buf[mt][1].y, buf[mt][1].z, buf[mt][1].w};
+                        const uint32_t rb0[4] = {buf[mt][2].x, buf[mt][2].y, buf[mt][2].z, buf[mt][2].w};
+                        const uint32_t rb1[4] = {buf[mt][3].x, buf[mt][3].y, buf[mt][3].z, buf[mt][3].w};
+                        const uint32_t d0[4] = {doa.x, doa.y, doa.z, doa.w};
+                        const uint32_t d1[4] = {dob.x, dob.y, dob.z, dob.w};
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t af[4] = {ra0[ks], rb0[ks], ra1[ks], rb1[ks]};
+                            mma16816(cg[mt], af, d0[ks], d1[ks]);
                         }
-                        float g = (ga.x + ga.y) + (gb2.x + gb2.y);
-                        g += __shfl_xor_sync(kFull, g, 1);
-                        g += __shfl_xor_sync(kFull, g, 2);
-                        // row u*8 + G is owned by lane (u*8 + G) & 31, slot u >> 2
-                        const float gx = __shfl_sync(kFull, g, (lane & 7) * 4);
-                        if ((u & 3) == (lane >> 3)) gown[u >> 2] = gx;
+                    }
+                }
+                // slot L: tile L >> 4, row half (L >> 3) & 1, row L & 7 -> lane 4 (L & 7)
+                float gown[2] = {0.f, 0.f};
+                const int srcl = (lane & 7) * 4;
+                const bool hi = (lane >> 3) & 1, up = lane >> 4;
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    if (2 * sl < nmt) {
+                        const float x0 = __shfl_sync(kFull, cg[2 * sl][0], srcl);
+                        const float x1 = __shfl_sync(kFull, cg[2 * sl][2], srcl);
+                        const float x2 = __shfl_sync(kFull, cg[2 * sl + 1][0], srcl);
+                        const float x3 = __shfl_sync(kFull, cg[2 * sl + 1][2], srcl);
+                        gown[sl] = up ? (hi ? x3 : x2) : (hi ? x1 : x0);
                     }
                 }
                 float d2v[2];
