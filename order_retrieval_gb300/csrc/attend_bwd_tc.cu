@@ -576,31 +576,34 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     cp_async_commit();
 
     // ---------------------------------------------------- window part ---
-    const int grp = lane >> 3, sub = lane & 7;
     const uint32_t *lst = csr_q + seg * csr_stride;
     const uint32_t *ob = off + seg * (int64_t)(N + 1);
     // Each key's list is walked 32 entries at a time.  Lane e owns entry e of a
-    // chunk (its query's record, the Cauchy weight w, a = w / s and the dk
-    // term); eight lanes read one dO row slice each, so all 32 dO rows of the
-    // chunk are requested together.  The next chunk's list positions are
-    // fetched while the current chunk is processed.
+    // chunk (its query's record, the weight w, a = w / s and the dk term).  The
+    // dO rows of a chunk are loaded as two 16-entry tiles, lane (g, t) taking
+    // 16-byte slices 2t, 2t+1 of rows g and g+8: these serve in place as the A
+    // fragments of G = dO_rows . v_j on the tensor cores (v_j in column 0 of B;
+    // the order of the dimensions does not matter for a dot product), and the
+    // same registers feed dv_j += a dO on the CUDA cores, each lane covering
+    // dimensions 16t .. 16t+15 of its two rows.  The next chunk's list
+    // positions are fetched while the current chunk is processed.
     const int wj0 = j0 + warp * 16;
     const int nkw = max(0, min(16, jend - wj0));
     const uint32_t bnd = lane <= nkw ? ob[wj0 + lane] : 0u;     // list bounds of this warp
+    const int g4 = lane >> 2, s4 = lane & 3;
     for (int r = 0; r < 16; ++r) {
         const int row = warp * 16 + r;
         const int j = wj0 + r;
-        float2 acc[4];
+        float2 acc[8];                                         // dims 16 s4 .. 16 s4 + 15
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
+        for (int e = 0; e < 8; ++e) acc[e] = make_float2(0.f, 0.f);
         float dka[4] = {0.f, 0.f, 0.f, 0.f};
         if (r < nkw) {
-            float2 v2[4];
-            {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(vb + (int64_t)j * DV + sub * 8);
-                const uint32_t uw[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) v2[e] = bf2_to_f2(uw[e]);
+            uint4 vja = make_uint4(0u, 0u, 0u, 0u), vjb = vja;   // B column 0: lanes 0..3
+            if (g4 == 0) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(vb + (int64_t)j * DV + s4 * 16);
+                vja = src[0];
+                vjb = src[1];
             }
             const float4 kj = load_k4(kb + (int64_t)j * DK, DK);
             const float kjc[4] = {kj.x, kj.y, kj.z, kj.w};
@@ -610,14 +613,19 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 const uint32_t ie = inext;
                 inext = p + 32 + lane < p1 ? (__ldg(lst + p + 32 + lane) & csr_mask) : 0xffffffffu;
                 const bool own = ie != 0xffffffffu;
-                const int nst = min(8, (int)((p1 - p + 3) >> 2));   // 4-entry steps in this chunk
-                uint4 dbuf[8];
+                const int nmt = min(2, (int)((p1 - p + 15) >> 4));   // 16-entry tiles
+                uint4 dbuf[2][4];                    // rows g, g+8 of tile mt: slices 2t, 2t+1
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint32_t iu = __shfl_sync(kFull, ie, u * 4 + grp);
-                    dbuf[u] = (u < nst && iu != 0xffffffffu)
-                                  ? ld_stream16(db + (int64_t)iu * DV + sub * 8)
-                                  : make_uint4(0u, 0u, 0u, 0u);
+                for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t iu = __shfl_sync(kFull, ie, 16 * mt + 8 * h + g4);
+                        const bool ok = mt < nmt && iu != 0xffffffffu;
+                        const uint4 *src =
+                            reinterpret_cast<const uint4 *>(db + (int64_t)iu * DV + s4 * 16);
+                        dbuf[mt][2 * h] = ok ? ld_stream16(src) : make_uint4(0u, 0u, 0u, 0u);
+                        dbuf[mt][2 * h + 1] = ok ? ld_stream16(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 // the owner's scalars for its entry
                 float a = 0.f, s2 = 0.f, inv_s = 0.f, gb = 0.f;
@@ -637,26 +645,42 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                     a = w * inv_s;
                     s2 = 2.f * neg_dw_dd2<WK>(w, inv_g2);
                 }
-                float gown = 0.f;
+                float cg[2][4];
+                const uint32_t v0[4] = {vja.x, vja.y, vja.z, vja.w};
+                const uint32_t v1[4] = {vjb.x, vjb.y, vjb.z, vjb.w};
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (u < nst) {
-                        const uint32_t uw[4] = {dbuf[u].x, dbuf[u].y, dbuf[u].z, dbuf[u].w};
-                        float2 d2v[4];
-                        float2 gg = make_float2(0.f, 0.f);
+                for (int mt = 0; mt < 2; ++mt) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            d2v[e] = bf2_to_f2(uw[e]);
-                            gg = fma2(d2v[e], v2[e], gg);
+                    for (int e = 0; e < 4; ++e) cg[mt][e] = 0.f;
+                    if (mt < nmt) {
+                        const uint32_t ra0[4] = {dbuf[mt][0].x, dbuf[mt][0].y, dbuf[mt][0].z, dbuf[mt][0].w};
+                        const uint32_t ra1[4] = {dbuf[mt][1].x, dbuf[mt][1].y, dbuf[mt][1].z, dbuf[mt][1].w};
+                        const uint32_t rb0[4] = {dbuf[mt][2].x, dbuf[mt][2].y, dbuf[mt][2].z, dbuf[mt][2].w};
+                        const uint32_t rb1[4] = {dbuf[mt][3].x, dbuf[mt][3].y, dbuf[mt][3].z, dbuf[mt][3].w};
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t af[4] = {ra0[ks], rb0[ks], ra1[ks], rb1[ks]};
+                            mma16816(cg[mt], af, v0[ks], v1[ks]);
                         }
-                        const float g = warp_group8_sum(gg.x + gg.y);
-                        const float2 au = dup2(__shfl_sync(kFull, a, u * 4 + grp));
+                        // dv_j += a_e dO_e for this lane's rows g and g+8
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[e] = fma2(au, d2v[e], acc[e]);
-                        const float gx = __shfl_sync(kFull, g, (lane & 3) * 8);
-                        if ((lane >> 2) == u) gown = gx;
+                        for (int h = 0; h < 2; ++h) {
+                            const float2 ah = dup2(__shfl_sync(kFull, a, 16 * mt + 8 * h + g4));
+                            const uint4 q0 = dbuf[mt][2 * h], q1 = dbuf[mt][2 * h + 1];
+                            const uint32_t uw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = fma2(ah, bf2_to_f2(uw[e]), acc[e]);
+                        }
                     }
                 }
+                // entry L: tile L >> 4, row half (L >> 3) & 1, row L & 7 -> lane 4 (L & 7)
+                const int srcl = (lane & 7) * 4;
+                const float x0 = __shfl_sync(kFull, cg[0][0], srcl);
+                const float x1 = __shfl_sync(kFull, cg[0][2], srcl);
+                const float x2 = __shfl_sync(kFull, cg[1][0], srcl);
+                const float x3 = __shfl_sync(kFull, cg[1][2], srcl);
+                const float gown = (lane >> 4) ? (((lane >> 3) & 1) ? x3 : x2)
+                                               : (((lane >> 3) & 1) ? x1 : x0);
                 if (own) {
                     const float coef = (gown - gb) * inv_s * s2;
 #pragma unroll
@@ -664,21 +688,23 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[e].x += __shfl_xor_sync(kFull, acc[e].x, 8);
-                acc[e].y += __shfl_xor_sync(kFull, acc[e].y, 8);
-                acc[e].x += __shfl_xor_sync(kFull, acc[e].x, 16);
-                acc[e].y += __shfl_xor_sync(kFull, acc[e].y, 16);
+            for (int e = 0; e < 8; ++e) {
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    acc[e].x += __shfl_xor_sync(kFull, acc[e].x, o);
+                    acc[e].y += __shfl_xor_sync(kFull, acc[e].y, o);
+                }
             }
 #pragma unroll
             for (int d = 0; d < DK; ++d)
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) dka[d] += __shfl_xor_sync(kFull, dka[d], o);
         }
-        if (lane < 8) {
-            float4 *dst = reinterpret_cast<float4 *>(&sm.dvp[row][lane * 8]);
-            dst[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-            dst[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+        if (g4 == 0) {                                         // lanes 0..3: 16 dims each
+            float4 *dst = reinterpret_cast<float4 *>(&sm.dvp[row][s4 * 16]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[e] = make_float4(acc[2 * e].x, acc[2 * e].y, acc[2 * e + 1].x, acc[2 * e + 1].y);
         }
         if (lane == 0) *reinterpret_cast<float4 *>(sm.dkp[row]) =
             make_float4(dka[0], dka[1], dka[2], dka[3]);
