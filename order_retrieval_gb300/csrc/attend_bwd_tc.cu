@@ -583,9 +583,11 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     // dO rows of a chunk are loaded as two 16-entry tiles, lane (g, t) taking
     // 16-byte slices 2t, 2t+1 of rows g and g+8: these serve in place as the A
     // fragments of G = dO_rows . v_j on the tensor cores (v_j in column 0 of B;
-    // the order of the dimensions does not matter for a dot product), and the
-    // same registers feed dv_j += a dO on the CUDA cores, each lane covering
-    // dimensions 16t .. 16t+15 of its two rows.  The next chunk's list
+    // the order of the dimensions does not matter for a dot product).  The
+    // same registers, transposed 8x8 block by block with movmatrix, are the A
+    // fragments of dv_j += dO^T a (16 dimensions per mma, a rounded to bf16 in
+    // column 0 of B, as the own-chunk P is), so dv_j accumulates in the mma's
+    // column-0 registers across the whole list.  The next chunk's list
     // positions are fetched while the current chunk is processed.
     const int wj0 = j0 + warp * 16;
     const int nkw = max(0, min(16, jend - wj0));
@@ -594,9 +596,11 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     for (int r = 0; r < 16; ++r) {
         const int row = warp * 16 + r;
         const int j = wj0 + r;
-        float2 acc[8];                                         // dims 16 s4 .. 16 s4 + 15
+        float cdv[4][4];            // dv_j: column 0 of four 16-dimension mma tiles
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = make_float2(0.f, 0.f);
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cdv[c][e] = 0.f;
         float dka[4] = {0.f, 0.f, 0.f, 0.f};
         if (r < nkw) {
             uint4 vja = make_uint4(0u, 0u, 0u, 0u), vjb = vja;   // B column 0: lanes 0..3
@@ -662,14 +666,18 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                             const uint32_t af[4] = {ra0[ks], rb0[ks], ra1[ks], rb1[ks]};
                             mma16816(cg[mt], af, v0[ks], v1[ks]);
                         }
-                        // dv_j += a_e dO_e for this lane's rows g and g+8
+                        // dv_j += dO^T a: entries 2t, 2t+1 (+8) of the tile in B column 0
+                        const float e0 = __shfl_sync(kFull, a, 16 * mt + 2 * s4);
+                        const float e1 = __shfl_sync(kFull, a, 16 * mt + 2 * s4 + 1);
+                        const float e2 = __shfl_sync(kFull, a, 16 * mt + 2 * s4 + 8);
+                        const float e3 = __shfl_sync(kFull, a, 16 * mt + 2 * s4 + 9);
+                        const uint32_t ba = g4 == 0 ? pack_bf16(e0, e1) : 0u;
+                        const uint32_t bb = g4 == 0 ? pack_bf16(e2, e3) : 0u;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const float2 ah = dup2(__shfl_sync(kFull, a, 16 * mt + 8 * h + g4));
-                            const uint4 q0 = dbuf[mt][2 * h], q1 = dbuf[mt][2 * h + 1];
-                            const uint32_t uw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e] = fma2(ah, bf2_to_f2(uw[e]), acc[e]);
+                        for (int c = 0; c < 4; ++c) {   // dims 16 (m/2) + 8 h + 2c + (m%2)
+                            const uint32_t af[4] = {movmatrix_trans(ra0[c]), movmatrix_trans(ra1[c]),
+                                                    movmatrix_trans(rb0[c]), movmatrix_trans(rb1[c])};
+                            mma16816(cdv[c], af, ba, bb);
                         }
                     }
                 }
@@ -688,23 +696,17 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    acc[e].x += __shfl_xor_sync(kFull, acc[e].x, o);
-                    acc[e].y += __shfl_xor_sync(kFull, acc[e].y, o);
-                }
-            }
-#pragma unroll
             for (int d = 0; d < DK; ++d)
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) dka[d] += __shfl_xor_sync(kFull, dka[d], o);
         }
-        if (g4 == 0) {                                         // lanes 0..3: 16 dims each
-            float4 *dst = reinterpret_cast<float4 *>(&sm.dvp[row][s4 * 16]);
+        if (s4 == 0) {              // lane 4m holds mma rows m and m+8 of column 0
+            const int d0 = 16 * (g4 >> 1) + (g4 & 1);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                dst[e] = make_float4(acc[2 * e].x, acc[2 * e].y, acc[2 * e + 1].x, acc[2 * e + 1].y);
+            for (int c = 0; c < 4; ++c) {
+                sm.dvp[row][d0 + 2 * c] = cdv[c][0];
+                sm.dvp[row][d0 + 8 + 2 * c] = cdv[c][2];
+            }
         }
         if (lane == 0) *reinterpret_cast<float4 *>(sm.dkp[row]) =
             make_float4(dka[0], dka[1], dka[2], dka[3]);

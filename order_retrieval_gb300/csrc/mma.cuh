@@ -47,6 +47,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 b16 matrix held one 32-bit pair per lane (lane L: row
+// L / 4, columns 2 (L % 4), +1) into the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // 16-byte load through the non-coherent path without L1 allocation: gathered
 // rows are used once by the loading warp.
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
