@@ -8,11 +8,13 @@
 //
 //  * One CTA = 64 consecutive queries of one chunk (4 warps x 16 rows).
 //  * Window part (a gather): a warp takes one query at a time; each lane owns
-//    two selected keys (index, coordinates, Cauchy weight), and eight lanes read
-//    one 128-byte bf16 value row with 16-byte loads, four rows per warp load,
-//    all 16 loads of a 64-key pass in flight together; the next query's indices
-//    are fetched while the current query is processed.  Partial sums
-//    (sum w v, sum w) go to shared memory in float32.
+//    two selected keys (index, coordinates, Cauchy weight); the gathered
+//    128-byte bf16 value rows come in with 16-byte loads, all 16 loads of a
+//    lane's 64-key pass in flight together, and the weighted sum V^T w runs
+//    on the tensor cores (rows transposed in registers by movmatrix, w in
+//    column 0 of B); the next query's indices are fetched while the current
+//    query is processed.  Partial sums (sum w v, sum w) go to shared memory in
+//    float32.
 //  * Own-chunk part (a dense causal C x C/2 x 64 contraction per chunk): key
 //    tiles of 64 rows are staged by cp.async into XOR-swizzled shared memory
 //    (double buffered); each thread builds its slice of the weight tile P
@@ -57,14 +59,6 @@ __device__ __forceinline__ float dist2k(const float (&a)[4], float4 b) {
         d = __fmaf_rn(e, e, d);
     }
     return d;
-}
-
-// acc[e] += w * row chunk (8 bf16), four packed f32x2 FMAs.
-__device__ __forceinline__ void bf16x8_fma(float2 (&acc)[4], uint4 raw, float w) {
-    const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
-    const float2 ww = dup2(w);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = fma2(ww, bf2_to_f2(u[e]), acc[e]);
 }
 
 // Stage own-chunk key tile `kt` (keys cC + kt*TK ...) into buffer b.
@@ -125,10 +119,15 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     // A pass covers up to 64 selected keys: lane L owns slots L and L+32
     // (index, key coordinates, weight); the 16 value-row loads of the pass are
     // all issued before any is used, and the first pass's indices of the next
-    // query are fetched while the current one is processed.
+    // query are fetched while the current one is processed.  The weighted sum
+    // runs on the tensor cores: for 16 selected keys, sum_j w_j v_j = V^T w is
+    // four m16n8k16 mma (16 dimensions each) with w (bf16, like the own-chunk
+    // P) in column 0 of B.  Lane (g, t) loads 16-byte slices 2t, 2t+1 of rows
+    // g and g+8 of the 16; movmatrix transposes them 8x8 block by block into
+    // A fragments, and the sums stay in the mma's column-0 registers.
     const int wq0 = i0 + warp * 16;
     const int nqw = c > 0 ? max(0, min(16, iend - wq0)) : 0;
-    const int grp = lane >> 3, sub = lane & 7;
+    const int g4 = lane >> 2, s4 = lane & 3;
     auto load_idx = [&](int i, int t0, int (&j)[2]) {
         const int32_t *irow = idx + (seg * N + i) * (int64_t)k + t0;
 #pragma unroll
@@ -141,9 +140,11 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     if (nqw > 0) load_idx(wq0, 0, jn);
     for (int r = 0; r < 16; ++r) {
         const int row = warp * 16 + r;
-        float2 acc[4];
+        float cacc[4][4];           // column 0 of four 16-dimension mma tiles
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = make_float2(0.f, 0.f);
+        for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cacc[cb][e] = 0.f;
         float sw = 0.f;
         float mrun = INFINITY;                     // softmax shift of this query
         if (r < nqw) {
@@ -168,14 +169,20 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     kk[s] = j[s] >= 0 ? load_k4(kb + (int64_t)j[s] * DK, DK)
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                const int nu = min(16, (k - t0 + 3) >> 2);   // 4-row loads in this pass
-                uint4 buf[16];
+                const int nmt = min(4, (k - t0 + 15) >> 4);  // 16-key tiles in this pass
+                uint4 buf[4][4];                    // rows g, g+8 of tile mt: slices 2t, 2t+1
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int src = u * 4 + grp;
-                    const int jr = __shfl_sync(kFull, j[u >> 3], src & 31);
-                    buf[u] = (u < nu && jr >= 0) ? ld_stream16(vb + (int64_t)jr * DV + sub * 8)
-                                                 : make_uint4(0u, 0u, 0u, 0u);
+                for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int slot = 16 * mt + 8 * h + g4;
+                        const int jr = __shfl_sync(kFull, j[mt >> 1], slot & 31);
+                        const bool ok = mt < nmt && jr >= 0;
+                        const uint4 *src =
+                            reinterpret_cast<const uint4 *>(vb + (int64_t)jr * DV + s4 * 16);
+                        buf[mt][2 * h] = ok ? ld_stream16(src) : make_uint4(0u, 0u, 0u, 0u);
+                        buf[mt][2 * h + 1] = ok ? ld_stream16(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 float d2v[2];
 #pragma unroll
@@ -188,7 +195,9 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     if (mn != mrun) {                    // uniform across the warp
                         const float sc = shift_scale(mn, mrun, inv_g2);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[e] = mul2(acc[e], dup2(sc));
+                        for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) cacc[cb][e] *= sc;
                         sw *= sc;
                         mrun = mn;
                     }
@@ -200,27 +209,39 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
                     sw += w[s];
                 }
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    if (u < nu) {
-                        const float wr = __shfl_sync(kFull, w[u >> 3], (u * 4 + grp) & 31);
-                        bf16x8_fma(acc, buf[u], wr);
+                for (int mt = 0; mt < 4; ++mt) {
+                    if (mt < nmt) {
+                        // weights of slots 16mt + 2t, +1, +8, +9 (owner lane = slot % 32)
+                        const int sb = 16 * mt + 2 * s4;
+                        const float e0 = __shfl_sync(kFull, w[mt >> 1], sb & 31);
+                        const float e1 = __shfl_sync(kFull, w[mt >> 1], (sb + 1) & 31);
+                        const float e2 = __shfl_sync(kFull, w[mt >> 1], (sb + 8) & 31);
+                        const float e3 = __shfl_sync(kFull, w[mt >> 1], (sb + 9) & 31);
+                        const uint32_t ba = g4 == 0 ? pack_bf16(e0, e1) : 0u;
+                        const uint32_t bb = g4 == 0 ? pack_bf16(e2, e3) : 0u;
+                        const uint32_t ra0[4] = {buf[mt][0].x, buf[mt][0].y, buf[mt][0].z, buf[mt][0].w};
+                        const uint32_t ra1[4] = {buf[mt][1].x, buf[mt][1].y, buf[mt][1].z, buf[mt][1].w};
+                        const uint32_t rb0[4] = {buf[mt][2].x, buf[mt][2].y, buf[mt][2].z, buf[mt][2].w};
+                        const uint32_t rb1[4] = {buf[mt][3].x, buf[mt][3].y, buf[mt][3].z, buf[mt][3].w};
+#pragma unroll
+                        for (int cb = 0; cb < 4; ++cb) {   // dims 16 (m/2) + 8 h + 2 cb + (m%2)
+                            const uint32_t af[4] = {movmatrix_trans(ra0[cb]), movmatrix_trans(ra1[cb]),
+                                                    movmatrix_trans(rb0[cb]), movmatrix_trans(rb1[cb])};
+                            mma16816(cacc[cb], af, ba, bb);
+                        }
                     }
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[e].x += __shfl_xor_sync(kFull, acc[e].x, 8);
-                acc[e].y += __shfl_xor_sync(kFull, acc[e].y, 8);
-                acc[e].x += __shfl_xor_sync(kFull, acc[e].x, 16);
-                acc[e].y += __shfl_xor_sync(kFull, acc[e].y, 16);
-            }
-#pragma unroll
             for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(kFull, sw, o);
         }
-        if (lane < 8) {
-            float4 *dst = reinterpret_cast<float4 *>(&sm.win[row][lane * 8]);
-            dst[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-            dst[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+        if (s4 == 0) {              // lane 4m holds mma rows m and m+8 of column 0
+            const int d0 = 16 * (g4 >> 1) + (g4 & 1);
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                sm.win[row][d0 + 2 * cb] = cacc[cb][0];
+                sm.win[row][d0 + 8 + 2 * cb] = cacc[cb][2];
+            }
         }
         if (lane == 0) {
             sm.swin[row] = sw;
