@@ -194,8 +194,10 @@ struct QAcc2 {
     }
 };
 
+// The softmax carries a shift and its rebasing through both parts; it gets
+// more registers (three CTAs per SM) instead of spilling.
 template <int DK, int WK>
-__global__ void __launch_bounds__(THREADS, 4)
+__global__ void __launch_bounds__(THREADS, WK == kWSoftmax ? 3 : 4)
 bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
              const __nv_bfloat16 *__restrict__ v, const float *__restrict__ gamma,
              const int32_t *__restrict__ idx, const __nv_bfloat16 *__restrict__ dout,
@@ -387,13 +389,16 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
     float2 mab = make_float2(sm.mpart[rowa_l], sm.mpart[rowa_l + 8]);   // softmax shifts
     auto tile = [&](const float4 *Ks, uint32_t vbase, int key0, auto masked) {
         if constexpr (WK == kWSoftmax) {           // move the shift to this tile's minimum
+            // (keys read through a volatile view: distances recomputed below are
+            // not kept alive across the mma)
+            const volatile float4 *Kv = Ks;
             float2 tmin = make_float2(INFINITY, INFINITY);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int kl = nt * 8 + 2 * tig + e;
-                    const float4 kv = Ks[kl];
+                    const float4 kv = make_float4(Kv[kl].x, Kv[kl].y, Kv[kl].z, Kv[kl].w);
                     const float kc[4] = {kv.x, kv.y, kv.z, kv.w};
                     float2 d2 = make_float2(0.f, 0.f);
 #pragma unroll
