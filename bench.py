@@ -30,6 +30,11 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# DRAM bytes (read + write) of one attend_fwd_tc launch on the efficiency
+# workload, from the ncu capture summarised in
+# profiles/attend_kernels_train_bf16_b2_n65536.md; None once that kernel changes.
+ATTEND_FWD_DRAM_BYTES = 623_364_096
+
 METRIC = "ZETA attention tokens/s (fwd, fwd+bwd) at N=65536 and % of GB300 HBM roofline"
 L2_FLUSH_BYTES = 256 << 20
 CPU_SAMPLE_TOKENS = 8192
@@ -539,7 +544,7 @@ def run_ours(args, w, rank, world):
         "variants": variants,
         "roofline": {"kernel": "attend_fwd_tc (efficiency workload, L2 flushed)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": ATTEND_FWD_DRAM_BYTES,
                      "algorithmic_bytes": fb, "peak_source": peak_src},
         "roofline_projection": {
             "kernel": "project_encode_tc (tcgen05, B=4 N=65536 D=512 F=64, L2 flushed)",
