@@ -53,6 +53,17 @@ def fwd_attend_bytes(w) -> int:
     return rows * (per_q + per_key_local)
 
 
+def fused_fwd_bytes(w) -> int:
+    """Algorithmic bytes of one fused select + attend launch: the attend
+    forward's bytes (the window read from the sorted prefix in place of an
+    index row), plus per query its code, the binary-search probes (one code per
+    halving of its prefix) and the index row written for the backward."""
+    rows = w.B * w.H * w.N
+    cb = 4 if w.d_K * w.bits <= 32 else 8
+    probes = max(1, (w.N - w.C).bit_length())
+    return fwd_attend_bytes(w) + rows * (cb + probes * cb + 4 * w.k)
+
+
 def bwd_attend_bytes(w) -> int:
     """Algorithmic bytes of one attend-backward call: per query, the window v
     rows again (query side) and the window dO rows gathered on the key side,
@@ -447,6 +458,33 @@ def run_ours(args, w, rank, world):
     fwd_e_ms = sum(fwd_e) / len(fwd_e)
     att_e_ms = sum(att_e) / len(att_e)
 
+    # --- fused select + attend (one launch) on the same workload
+    plan_f = ZetaPlan(pe, dev, backward=False, fused=True)
+    for _ in range(warm):
+        plan_f.forward(qe, ke, ve, gme)
+    fus_tot, fus_k = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        e = [ev() for _ in range(3)]
+        e[0].record()
+        zb.zeta_encode(pe, qe, plan_f.q_codes)
+        zb.zeta_encode(pe, ke, plan_f.k_codes)
+        zb.zeta_sort_chunks(pe, plan_f.k_codes, plan_f.prefix_codes, plan_f.prefix_idx,
+                            plan_f.sort_ws)
+        e[1].record()
+        zb.zeta_select_attend_fwd(pe, qe, ke, ve, gme, plan_f.q_codes, plan_f.prefix_codes,
+                                  plan_f.prefix_idx, plan_f.idx, plan_f.out, plan_f.rowsum,
+                                  plan_f.status)
+        e[2].record()
+        e[2].synchronize()
+        fus_tot.append(e[0].elapsed_time(e[2]))
+        fus_k.append(e[1].elapsed_time(e[2]))
+    if int(plan_f.status.item()) != 0:
+        raise RuntimeError(f"device status {plan_f.status.item()} (fused)")
+    fus_tot_ms = sum(fus_tot) / len(fus_tot)
+    fus_k_ms = sum(fus_k) / len(fus_k)
+    del plan_f
+
     # --- multi-curve variant (3 cyclic / 6 permuted coordinate orders) on the
     # efficiency workload: the whole forward, and its index part
     variants = {}
@@ -599,6 +637,14 @@ def run_ours(args, w, rank, world):
         "fwd_tokens_per_s": tokens / (fwd_train_ms * 1e-3),
         "fwd_efficiency": {"workload": we.name, "tokens_per_s": we.B * we.N * world /
                            (fwd_e_ms * 1e-3), "ms": fwd_e_ms, "attend_fwd_ms": att_e_ms},
+        "fwd_efficiency_fused": {
+            "workload": we.name, "call": "zeta_select_attend_fwd",
+            "tokens_per_s": we.B * we.N * world / (fus_tot_ms * 1e-3), "ms": fus_tot_ms,
+            "select_attend_ms": fus_k_ms,
+            "roofline": {"bound": "hbm", "achieved": fused_fwd_bytes(we) / (fus_k_ms * 1e-3) / 1e9,
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": fused_fwd_bytes(we) / (fus_k_ms * 1e-3) / 1e9 / hbm_peak,
+                         "algorithmic_bytes": fused_fwd_bytes(we)}},
         "per_call_ms": per_call,
         "variants": variants,
         "roofline": {"kernel": "attend_fwd_tc (efficiency workload, L2 flushed)", "bound": "hbm",

@@ -274,6 +274,30 @@ zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, const flo
                               cudaStream_t stream);
 
 /*
+ * zeta_select_attend_fwd -- zeta_select_topk and zeta_attend_fwd in one call.
+ * Passage: as for those two calls (OpenReview reply A3 "Chunking ... & Where
+ * efficiency is coming from": binary search of the insertion position; the
+ * attended set and weights of zeta_attend_fwd).
+ * On the tensor-core shapes (bf16 values, d_V = 64, d_K <= 4) one kernel finds
+ * each query's window by binary search in its sorted prefix, reads the window
+ * as a contiguous run of prefix_idx, attends, and writes the run to idx for
+ * zeta_attend_bwd; other shapes run the two calls one after the other.
+ * Results are those of zeta_select_topk followed by zeta_attend_fwd.
+ *   q, k, v, gamma   in : as for zeta_attend_fwd
+ *   q_codes          in : codes of the queries [B, H, N]
+ *   prefix_codes, prefix_idx  in : from zeta_sort_chunks
+ *   idx              out: int32 [B, H, N, k] (as zeta_select_topk writes it)
+ *   out, rowsum      out: as for zeta_attend_fwd
+ *   dev_status       optional int32 device word (as for zeta_attend_fwd)
+ * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED.
+ */
+zeta_status_t zeta_select_attend_fwd(const zeta_problem_t *p, const float *q, const float *k,
+                                     const void *v, const float *gamma, const void *q_codes,
+                                     const void *prefix_codes, const int32_t *prefix_idx,
+                                     int32_t *idx, void *out, float *rowsum,
+                                     int32_t *dev_status, cudaStream_t stream);
+
+/*
  * zeta_attend_bwd -- gradients through the weights, selection fixed.
  * Passage: the forward/backward timings of the OpenReview replies A3/A4 (the
  * method is trained end to end) and the forward definition above.

@@ -102,6 +102,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.zeta_attend_fwd.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.zeta_attend_fwd.restype = S
     L.zeta_attend_bwd.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+    L.zeta_select_attend_fwd.argtypes = [PP] + [P] * 12
+    L.zeta_select_attend_fwd.restype = S
     L.zeta_attend_bwd.restype = S
     _lib = L
     return L
@@ -306,6 +308,29 @@ def zeta_attend_fwd(p, q, k, v, gamma, idx, out, rowsum, dev_status=None, stream
            lib().zeta_attend_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
                                  _ptr(idx), _ptr(out), _ptr(rowsum), _ptr(dev_status),
                                  _stream(stream)))
+
+
+def zeta_select_attend_fwd(p, q, k, v, gamma, q_codes, prefix_codes, prefix_idx, idx, out,
+                           rowsum, dev_status=None, stream=None):
+    S = p.B * p.H * p.N
+    vt = v_torch_dtype(p)
+    T = zeta_prefix_entries(p)
+    _expect(q, "q", torch.float32, S * p.d_K)
+    _expect(k, "k", torch.float32, S * p.d_K)
+    _expect(v, "v", vt, S * p.d_V)
+    _expect(gamma, "gamma", torch.float32, p.H)
+    _expect(q_codes, "q_codes", code_dtype(p), S)
+    _expect(prefix_codes, "prefix_codes", code_dtype(p), p.B * p.H * T)
+    _expect(prefix_idx, "prefix_idx", torch.int32, p.B * p.H * T)
+    _expect(idx, "idx", torch.int32, S * p.k)
+    _expect(out, "out", vt, S * p.d_V)
+    _expect(rowsum, "rowsum", torch.float32, S)
+    _expect(dev_status, "dev_status", torch.int32, 1)
+    _check("zeta_select_attend_fwd",
+           lib().zeta_select_attend_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                                        _ptr(q_codes), _ptr(prefix_codes), _ptr(prefix_idx),
+                                        _ptr(idx), _ptr(out), _ptr(rowsum), _ptr(dev_status),
+                                        _stream(stream)))
 
 
 def zeta_attend_bwd(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, workspace,

@@ -189,6 +189,25 @@ ZETA_API zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, 
         zeta::launch_attend_fwd(pr, q, k, v, gamma, idx, out, rowsum, dev_status, stream));
 }
 
+ZETA_API zeta_status_t zeta_select_attend_fwd(const zeta_problem_t *p, const float *q,
+                                              const float *k, const void *v, const float *gamma,
+                                              const void *q_codes, const void *prefix_codes,
+                                              const int32_t *prefix_idx, int32_t *idx, void *out,
+                                              float *rowsum, int32_t *dev_status,
+                                              cudaStream_t stream) {
+    Prob pr;
+    zeta_status_t s = check_problem(p, &pr);
+    if (s != ZETA_OK) return s;
+    if (empty(pr)) return ZETA_OK;
+    if (!q || !k || !v || !gamma || !q_codes || !idx || !out || !rowsum)
+        return ZETA_ERR_INVALID_ARG;
+    if (pr.T > 0 && (!prefix_codes || !prefix_idx)) return ZETA_ERR_INVALID_ARG;
+    if (!aligned16(v) || !aligned16(out)) return ZETA_ERR_INVALID_ARG;
+    return from_cuda(zeta::launch_select_attend_fwd(pr, q, k, v, gamma, q_codes, prefix_codes,
+                                                    prefix_idx, idx, out, rowsum, dev_status,
+                                                    stream));
+}
+
 ZETA_API zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, const float *k,
                                        const void *v, const float *gamma, const int32_t *idx,
                                        const void *dout, float *dq, float *dk, void *dv,

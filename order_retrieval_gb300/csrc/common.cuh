@@ -117,6 +117,13 @@ cudaError_t launch_attend_fwd(const Prob &p, const float *q, const float *k, con
                               const float *gamma, const int32_t *idx, void *out, float *rowsum,
                               int32_t *status, cudaStream_t st);
 
+// Select + attend in one call (fused kernel on the tensor-core shapes).
+cudaError_t launch_select_attend_fwd(const Prob &p, const float *q, const float *k,
+                                     const void *v, const float *gamma, const void *q_codes,
+                                     const void *prefix_codes, const int32_t *prefix_idx,
+                                     int32_t *idx, void *out, float *rowsum, int32_t *status,
+                                     cudaStream_t st);
+
 // Tensor-core forward for bf16 values, d_V = 64, d_K <= 4.
 bool attend_fwd_tc_supported(const Prob &p);
 cudaError_t launch_attend_fwd_tc(const Prob &p, const float *q, const float *k, const void *v,

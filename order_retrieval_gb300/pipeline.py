@@ -21,9 +21,14 @@ from . import binding as zb
 
 class ZetaPlan:
     def __init__(self, p: zb.zeta_problem_t, device="cuda", backward: bool = True,
-                 curves: int = 1):
+                 curves: int = 1, fused: bool = False):
+        """fused: select and attend in one call (zeta_select_attend_fwd); one
+        curve only."""
+        if fused and curves != 1:
+            raise ValueError("the fused select + attend call takes one curve")
         self.p = p
         self.curves = curves
+        self.fused = fused
         self.axes = zb.curve_axes(p.d_K, curves)
         # Every curve's slices sort as one problem with curves*B batches.
         self.p_sort = zb.problem(p.B * curves, p.H, p.N, p.d_K, p.d_V, p.k, p.C, p.bits,
@@ -68,6 +73,11 @@ class ZetaPlan:
             zb.zeta_encode_curves(p, k, self.axes, self.k_codes, stream)
         zb.zeta_sort_chunks(self.p_sort, self.k_codes, self.prefix_codes, self.prefix_idx,
                             self.sort_ws, stream)
+        if self.fused:
+            zb.zeta_select_attend_fwd(p, q, k, v, gamma, self.q_codes, self.prefix_codes,
+                                      self.prefix_idx, self.idx, self.out, self.rowsum,
+                                      self.status, stream)
+            return self.out, self.rowsum, self.idx
         if self.curves == 1:
             zb.zeta_select_topk(p, self.q_codes, self.prefix_codes, self.prefix_idx, self.idx,
                                 stream)

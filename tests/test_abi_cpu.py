@@ -174,3 +174,23 @@ def test_project_encode_checks_its_arguments(L):
     # the binding's marshalling matches the C signature (empty problem: no launch)
     pe = zb.problem(0, 8, 1024, 3, 64, 16, 128, 10, "bf16")
     zb.zeta_project_encode(pe, 512, 64, *([None] * 9), stream=0)
+
+
+def test_select_attend_checks_its_arguments(L):
+    p = _prob()
+    P = ctypes.byref(p)
+    fake = ctypes.c_void_p(0x1000)
+    args = [fake] * 12
+    assert L.zeta_select_attend_fwd(None, *args) == 1
+    for pos in (0, 1, 2, 3, 4, 7, 8, 9):          # q, k, v, gamma, q_codes, idx, out, rowsum
+        bad = list(args)
+        bad[pos] = None
+        assert L.zeta_select_attend_fwd(P, *bad) == 1, pos
+    odd = list(args)
+    odd[2] = ctypes.c_void_p(0x1002)               # v not 16-B aligned
+    assert L.zeta_select_attend_fwd(P, *odd) == 1
+    assert L.zeta_select_attend_fwd(ctypes.byref(_prob(N=1000)), *args) == 1
+    e = _prob(B=0)
+    assert L.zeta_select_attend_fwd(ctypes.byref(e), *([None] * 12)) == 0
+    pe = zb.problem(0, 2, 1024, 3, 32, 16, 128, 10, "f32")
+    zb.zeta_select_attend_fwd(pe, *([None] * 10), stream=0)
