@@ -2,6 +2,7 @@
 // the ZETA library.  Nothing here is exported; the C ABI is include/zeta.h.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cstddef>
 #include <cuda_runtime.h>
@@ -27,6 +28,25 @@ struct Prob {
     int64_t T;        // prefix entries per slice
     int code64;       // 1 when d_K*bits > 32
     int wk;           // weight kernel (kWCauchy, kWSoftmax, kWInvEuclid)
+};
+
+// Launch set-up done once per device (for example cudaFuncSetAttribute, which
+// applies to a function on the current device only): one bit per device id
+// below 64 records that it ran; threads that race may both run it (the set-up
+// calls used with it are idempotent).
+struct PerDeviceOnce {
+    std::atomic<uint64_t> done{0};
+    template <typename Fn>
+    cudaError_t run(Fn &&fn) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+        if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+        e = fn();
+        if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+        return e;
+    }
 };
 
 // Record the first device-side error in an optional status word.

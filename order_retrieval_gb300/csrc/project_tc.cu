@@ -314,19 +314,15 @@ template <typename CodeT, int DK>
 cudaError_t launch_proj(const Prob &p, int D, const CUtensorMap &xmap, const CUtensorMap &wmap,
                         const float *b1, const float *w2, const float *b2, float *q, float *k,
                         void *q_codes, void *k_codes, int32_t *status, cudaStream_t st) {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(project_encode_tc<CodeT, DK>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kProjSmem);
-        if (e != cudaSuccess) {
-            sms = 0;
-            return e;
-        }
-    }
+    static PerDeviceOnce smem_once;
+    cudaError_t e = smem_once.run([] {
+        return cudaFuncSetAttribute(project_encode_tc<CodeT, DK>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kProjSmem);
+    });
+    int dev = 0, sms = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     const int64_t M = (int64_t)p.B * p.N;
     const int64_t units = (M + BM - 1) / BM * (2 * p.H * FH / BN);
     const unsigned grid = (unsigned)(units < sms ? units : sms);

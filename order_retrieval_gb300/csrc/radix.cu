@@ -271,14 +271,13 @@ cudaError_t run_pass(const Src &src, int shift, int64_t S, int64_t maxlen, Radix
     dim3 grid((unsigned)tiles, (unsigned)S);
     radix_upsweep<K, Src><<<grid, kRadixThreads, 0, st>>>(src, shift, ws.hist, tiles, status);
     radix_scan<<<(unsigned)S, 1024, 0, st>>>(ws.hist, tiles, seglen_out);
-    static bool smem_set = false;           // the attribute is set once, outside any capture
-    if (!smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(radix_downsweep<K, Src>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)downsweep_smem<K>());
-        if (e != cudaSuccess) return e;
-        smem_set = true;
-    }
+    static PerDeviceOnce smem_once;          // run once per device, outside any capture
+    cudaError_t e = smem_once.run([] {
+        return cudaFuncSetAttribute(radix_downsweep<K, Src>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)downsweep_smem<K>());
+    });
+    if (e != cudaSuccess) return e;
     radix_downsweep<K, Src><<<grid, kRadixThreads, downsweep_smem<K>(), st>>>(
         src, shift, ws.hist, tiles, static_cast<K *>(ws.keys[nxt]), ws.vals[nxt], out_stride);
     return cudaGetLastError();
