@@ -136,6 +136,23 @@ struct QAcc {
     template <int WK>
     __device__ void add(float w, float d2, float m, float g, const float (&qi)[4], float4 kk,
                         float inv_g2, float inv_g) {
+        if constexpr (WK == kWCauchy) {
+            // Cauchy: c = -2 u / gamma^2 and e = 2 (w - u) / gamma with u = w^2, so
+            // the sums are kept without the constants: x[2] = sum u g, x[3] = sum u,
+            // x[4+d] = sum u g (q-k)_d, x[8+d] = sum u (q-k)_d (see the epilogue).
+            const float u = w * w, ug = u * g;
+            x[0] += w;
+            x[1] = __fmaf_rn(w, g, x[1]);
+            x[2] += ug;
+            x[3] += u;
+            const float dq[4] = {qi[0] - kk.x, qi[1] - kk.y, qi[2] - kk.z, qi[3] - kk.w};
+#pragma unroll
+            for (int d = 0; d < 4; ++d) {
+                x[4 + d] = __fmaf_rn(ug, dq[d], x[4 + d]);
+                x[8 + d] = __fmaf_rn(u, dq[d], x[8 + d]);
+            }
+            return;
+        }
         const float c = -2.f * neg_dw_dd2<WK>(w, inv_g2);
         const float e = dw_dgamma<WK>(w, d2, m, inv_g2, inv_g);
         x[0] += w;
@@ -170,6 +187,19 @@ struct QAcc2 {
     template <int DK, int WK>
     __device__ void add(float2 w, float2 d2, float2 m, float2 g, const float2 (&dq)[4],
                         float2 m2ig2, float2 two_ig, float2 k2) {
+        if constexpr (WK == kWCauchy) {        // the same constant-free sums as QAcc::add
+            const float2 u = mul2(w, w), ug = mul2(u, g);
+            x[0] = add2(x[0], w);
+            x[1] = fma2(w, g, x[1]);
+            x[2] = add2(x[2], ug);
+            x[3] = add2(x[3], u);
+#pragma unroll
+            for (int d = 0; d < DK; ++d) {
+                x[4 + d] = fma2(ug, dq[d], x[4 + d]);
+                x[8 + d] = fma2(u, dq[d], x[8 + d]);
+            }
+            return;
+        }
         float2 c, e;
         if constexpr (WK == kWSoftmax) {
             c = mul2(w, m2ig2);                                   // -2 w / gamma^2
@@ -523,8 +553,18 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
             const float inv_s = __frcp_rn(t[0]);
             const float gb = t[1] * inv_s;
             const int64_t gi = seg * N + i;
-            for (int d = 0; d < DK; ++d) dq[gi * DK + d] = (t[4 + d] - gb * t[8 + d]) * inv_s;
-            dg_part[gi] = (t[2] - gb * t[3]) * inv_s;
+            if constexpr (WK == kWCauchy) {
+                // dq_d = -2/gamma^2 (sum u g (q-k)_d - gbar sum u (q-k)_d) / s and
+                // dgamma_i = 2/gamma (sum g w - sum g u - gbar (sum w - sum u)) / s
+                //          = 2/gamma (gbar sum u - sum u g) / s   (sum g w = gbar s)
+                const float cq = -2.f * inv_g2 * inv_s, cg = 2.f * inv_g * inv_s;
+                for (int d = 0; d < DK; ++d)
+                    dq[gi * DK + d] = (t[4 + d] - gb * t[8 + d]) * cq;
+                dg_part[gi] = (gb * t[3] - t[2]) * cg;
+            } else {
+                for (int d = 0; d < DK; ++d) dq[gi * DK + d] = (t[4 + d] - gb * t[8 + d]) * inv_s;
+                dg_part[gi] = (t[2] - gb * t[3]) * inv_s;
+            }
             const float *qq = tig == 0 ? qa : qbv;
             QRec rcd;
             rcd.q = make_float4(qq[0], qq[1], qq[2], qq[3]);
