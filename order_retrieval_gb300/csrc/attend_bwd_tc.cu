@@ -39,8 +39,9 @@ constexpr int T64 = 64;           // rows per CTA tile (queries or keys)
 constexpr int DV = 64;
 constexpr int THREADS = 128;
 
-// Per-query record for the key side: q (padded to 4), then {1/s, gbar, m, 0}
-// (m: the softmax shift; 0 for the other weight kernels).
+// Per-query record for the key side: q (padded to 4), then {1/s, gbar, m,
+// -gbar/s} (m: the softmax shift; 0 for the other weight kernels), so that
+// dL/dw_ij = g_ij / s - gbar / s is one fma.
 struct __align__(16) QRec {
     float4 q;
     float4 sg;
@@ -82,13 +83,6 @@ __device__ __forceinline__ float dist2k(const float (&a)[4], float4 b) {
         d = __fmaf_rn(e, e, d);
     }
     return d;
-}
-
-__device__ __forceinline__ float warp_group8_sum(float x) {
-    x += __shfl_xor_sync(kFull, x, 1);
-    x += __shfl_xor_sync(kFull, x, 2);
-    x += __shfl_xor_sync(kFull, x, 4);
-    return x;
 }
 
 // 64 rows x 64 bf16 of a [.., 64] row-major array into a swizzled tile;
@@ -568,7 +562,7 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
             const float *qq = tig == 0 ? qa : qbv;
             QRec rcd;
             rcd.q = make_float4(qq[0], qq[1], qq[2], qq[3]);
-            rcd.sg = make_float4(inv_s, gb, WK == kWSoftmax ? mfin : 0.f, 0.f);
+            rcd.sg = make_float4(inv_s, gb, WK == kWSoftmax ? mfin : 0.f, -gb * inv_s);
             rec[gi] = rcd;
         }
     }
@@ -677,7 +671,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                     }
                 }
                 // the owner's scalars for its entry
-                float a = 0.f, s2 = 0.f, inv_s = 0.f, gb = 0.f;
+                float a = 0.f, s2 = 0.f, inv_s = 0.f, ngbs = 0.f;
                 float dqk[4] = {0.f, 0.f, 0.f, 0.f};
                 if (own) {
                     const QRec qrc = rb_[ie];
@@ -690,9 +684,10 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                     }
                     const float w = weight_fast<WK>(d2, qrc.sg.z, inv_g2);
                     inv_s = qrc.sg.x;
-                    gb = qrc.sg.y;
+                    ngbs = qrc.sg.w;
                     a = w * inv_s;
-                    s2 = 2.f * neg_dw_dd2<WK>(w, inv_g2);
+                    // Cauchy: 2 w^2 / gamma^2 with the constant applied to dk at the end
+                    s2 = WK == kWCauchy ? w * w : 2.f * neg_dw_dd2<WK>(w, inv_g2);
                 }
                 float cg[2][4];
                 const uint32_t v0[4] = {vja.x, vja.y, vja.z, vja.w};
@@ -735,7 +730,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 const float gown = (lane >> 4) ? (((lane >> 3) & 1) ? x3 : x2)
                                                : (((lane >> 3) & 1) ? x1 : x0);
                 if (own) {
-                    const float coef = (gown - gb) * inv_s * s2;
+                    const float coef = __fmaf_rn(gown, inv_s, ngbs) * s2;
 #pragma unroll
                     for (int d = 0; d < DK; ++d) dka[d] = __fmaf_rn(coef, dqk[d], dka[d]);
                 }
@@ -820,7 +815,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                     const int ql = nt * 8 + 2 * tig + e;
                     const QRec qrc = qt_rec[ql];
                     const float qc[4] = {qrc.q.x, qrc.q.y, qrc.q.z, qrc.q.w};
-                    const float2 inv_s = dup2(qrc.sg.x), gb = dup2(qrc.sg.y);
+                    const float2 inv_s = dup2(qrc.sg.x), ngbs = dup2(qrc.sg.w);
                     const float2 mq = dup2(qrc.sg.z);
                     float2 dqk[4];
                     float2 d2 = make_float2(0.f, 0.f);
@@ -836,11 +831,11 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                         w.y = (i >= first_b && i < cend) ? w.y : 0.f;
                     }
                     const float2 aw = mul2(w, inv_s);
-                    const float2 dldw = mul2(sub2(make_float2(s[nt][e], s[nt][2 + e]), gb), inv_s);
+                    const float2 dldw = fma2(make_float2(s[nt][e], s[nt][2 + e]), inv_s, ngbs);
                     float2 ndw;                    // 2 (-dw/d(d^2))
                     if constexpr (WK == kWSoftmax) ndw = mul2(w, two_ig2);
                     else if constexpr (WK == kWInvEuclid) ndw = mul2(mul2(w, w), w);
-                    else ndw = mul2(mul2(w, w), two_ig2);
+                    else ndw = mul2(w, w);         // 2/gamma^2 applied to dk at the end
                     const float2 coef = mul2(dldw, ndw);
 #pragma unroll
                     for (int d = 0; d < DK; ++d) dkab[d] = fma2(coef, dqk[d], dkab[d]);
@@ -908,9 +903,10 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
         }
     }
     if (tig == 0) {
+        const float ks = WK == kWCauchy ? 2.f * inv_g2 : 1.f;   // the Cauchy terms' constant
         for (int d = 0; d < DK; ++d) {
-            if (ka < jend) dk[(seg * N + ka) * DK + d] = dkl_a[d] + sm.dkp[rowa][d];
-            if (kbi < jend) dk[(seg * N + kbi) * DK + d] = dkl_b[d] + sm.dkp[rowb][d];
+            if (ka < jend) dk[(seg * N + ka) * DK + d] = (dkl_a[d] + sm.dkp[rowa][d]) * ks;
+            if (kbi < jend) dk[(seg * N + kbi) * DK + d] = (dkl_b[d] + sm.dkp[rowb][d]) * ks;
         }
     }
 }
