@@ -9,7 +9,8 @@
 //   upsweep   per tile of 4096 items: digit histogram -> hist[seg][tile][digit]
 //   scan      per segment: exclusive scan of hist in (digit, tile) order
 //   downsweep per tile: stable rank of every item among equal digits (warp
-//             match + per-warp counters), scatter to hist offset + rank.
+//             match + per-warp counters bumped by one lane per digit group),
+//             scatter to hist offset + rank.
 #include "common.cuh"
 
 namespace zeta {
@@ -184,7 +185,7 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
     __shared__ uint32_t tds[256];           // tile-local start of each digit
     __shared__ uint32_t wsum[8];
     __shared__ uint32_t s_total;            // items of this tile that are sorted
-    __shared__ uint16_t wcnt[W][256];
+    __shared__ uint32_t wcnt[W][256];
     extern __shared__ __align__(16) unsigned char stage_raw[];
     K *skey = reinterpret_cast<K *>(stage_raw);
     uint32_t *sval = reinterpret_cast<uint32_t *>(stage_raw + sizeof(K) * kRadixTile);
@@ -202,20 +203,23 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
     int dig[kRadixItems];
     uint32_t rank[kRadixItems];
 #pragma unroll
-    for (int r = 0; r < kRadixItems; ++r) {
+    for (int r = 0; r < kRadixItems; ++r) {     // all of the thread's loads in flight first
         const int64_t p = base + w * (32 * kRadixItems) + r * 32 + lane;
         bool ok = false;
         if (p < len) ok = src.load(seg, p, key[r], val[r], nullptr);
         dig[r] = ok ? (int)((unsigned)(key[r] >> shift) & 255u) : 256;
+    }
+#pragma unroll
+    for (int r = 0; r < kRadixItems; ++r) {
+        // the lowest lane of each equal-digit group bumps the warp's counter for
+        // that digit and hands the old count to its group (a warp's atomics on one
+        // counter take effect in program order, so items keep their order)
         const unsigned peers = __match_any_sync(kFull, dig[r]);
-        uint32_t cur = 0;
-        if (ok) cur = wcnt[w][dig[r]];
-        __syncwarp();
-        if (ok) {
-            rank[r] = cur + __popc(peers & lt);
-            if ((peers & lt) == 0) wcnt[w][dig[r]] = (uint16_t)(cur + __popc(peers));
-        }
-        __syncwarp();
+        const int leader = __ffs(peers) - 1;
+        uint32_t old = 0;
+        if (dig[r] < 256 && lane == leader) old = atomicAdd(&wcnt[w][dig[r]], __popc(peers));
+        old = __shfl_sync(kFull, old, leader);
+        rank[r] = old + __popc(peers & lt);
     }
     __syncthreads();
     if (threadIdx.x < 256) {                // per digit: warp offsets, then the tile total
@@ -223,7 +227,7 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
         uint32_t run = 0;
         for (int ww = 0; ww < W; ++ww) {
             const uint32_t c = wcnt[ww][d];
-            wcnt[ww][d] = (uint16_t)run;
+            wcnt[ww][d] = run;
             run += c;
         }
         uint32_t inc = run;                 // exclusive scan of tile totals over digits
