@@ -116,7 +116,8 @@ zeta_status_t zeta_encode(const zeta_problem_t *p, const float *x, void *codes,
  * zeta_sort_chunks -- sorted key order of every chunk-aligned causal prefix.
  * Passage: OpenReview reply A3 "Chunking ... & Where efficiency is coming from"
  * (radix sort of the Z-order codes) and the atlas.scime.ai summary, "Approach"
- * (sort and chunk keys so every query searches its past in parallel).
+ * (keys are sorted and split into chunks, so that all queries search their
+ * causal past at the same time).
  * Prefix c holds the keys of chunks 0..c-1 ordered by (code, token index).
  *   key_codes     in : codes of the keys [B, H, N]
  *   prefix_codes  out: same code type [B, H, T]      (T = zeta_prefix_entries)
@@ -173,7 +174,8 @@ zeta_status_t zeta_select_topk(const zeta_problem_t *p, const void *q_codes,
 
 /*
  * zeta_encode_curves -- codes of every token along several Z-order curves.
- * Passage: OpenReview discussion, reply on the asymmetry of Z-order curves
+ * Passage: OpenReview discussion, follow-up reply on interleaving the bits of
+ * different dimensions (several curves)
  * (the key coordinates are interleaved in several orders: the three cyclic
  * shifts of (K^1, K^2, K^3), or all six orderings).
  * Curve m reads coordinate axes[m][s] into slot s, slot 0 being the most
@@ -192,7 +194,8 @@ zeta_status_t zeta_encode_curves(const zeta_problem_t *p, const float *x, int32_
 
 /*
  * zeta_select_topk_curves -- the union of one window per curve.
- * Passage: OpenReview discussion, reply on the asymmetry of Z-order curves
+ * Passage: OpenReview discussion, follow-up reply on interleaving the bits of
+ * different dimensions (several curves)
  * (every curve collects k // curves of the k tokens).
  * Reading of the union: with km = k // curves, curve m gives the km keys that
  * zeta_select_topk would give with km in place of k (its own prefix table);

@@ -22,9 +22,9 @@
  *               (trainable gamma in the Cauchy softmax acts as a temperature;
  *               gamma = 1 gives a Student-t kernel) and reply A3 "Justification
  *               for Euclidean Distance Claim".
- *   [SUM-app]   atlas.scime.ai summary, "Approach" (sort and chunk keys so each
- *               query retrieves its top-k neighbours under the causal mask;
- *               Adaptive Cauchy-Softmax).
+ *   [SUM-app]   atlas.scime.ai summary, "Approach" (keys sorted and split into
+ *               chunks, every query finds its top-k neighbours among its
+ *               causal past; Adaptive Cauchy-Softmax).
  *
  * Readings where the pages are silent:
  *   - normalisation is the fixed affine map [-1,1) -> [0,1); quantisation is done
@@ -362,8 +362,9 @@ void orc_exact_topk(const float *q, const float *kx, int64_t N, int64_t C, int d
 
 /* Codes of the coordinates read in the order axes[0..d_K) (a permutation of
  * 0..d_K-1): the curve of the tuple (x[axes[0]], x[axes[1]], ...), OpenReview
- * discussion, reply on the asymmetry of Z-order curves (shifted and permuted
- * coordinate orders (K^1,K^2,K^3), (K^2,K^3,K^1), ...). */
+ * discussion, follow-up reply on interleaving the bits of
+ * different dimensions (several curves): shifted and permuted
+ * coordinate orders (K^1,K^2,K^3), (K^2,K^3,K^1), ... */
 void orc_encode_axes(const float *x, int64_t ntok, int d_K, int bits, const int32_t *axes,
                      uint64_t *codes)
 {
@@ -398,7 +399,7 @@ void orc_merge_windows(const int32_t *win, int M, int km, int k, int32_t *out)
 
 /* Two-layer projection of one token onto the d_K key (or query) coordinates of
  * every head, OpenReview discussion, reply A "LLMs impact the selection of
- * d_K" (a two-layer neural network projects the input into keys):
+ * d_K" (the keys come out of a small network of two layers):
  *   h_f   = max(0, sum_e W1[hd*F + f][e] x[e] + b1[hd*F + f])     f < F
  *   y_c   = tanh(sum_f W2[hd][c][f] h_f + b2[hd][c])               c < d_K
  * tanh lands the coordinates in (-1, 1), the range the quantiser reads.

@@ -2,8 +2,8 @@
 //
 // The pages time a forward+backward pass (OpenReview discussion of "ZETA:
 // Leveraging Z-order Curves for Efficient Top-k Attention", replies A3/A4 on
-// time and memory; atlas.scime.ai summary, "Measured effects", the sequence
-// length 65536 forward + backward row), so the method is trained end to end.
+// time and memory; atlas.scime.ai summary, "Measured effects", whose table
+// times a 65,536-token training pass), so the method is trained end to end.
 // The window is not differentiated: idx is an input.
 //
 // With a_ij = w_ij / s_i, g_ij = dO_i . v_j, gbar_i = sum_j a_ij g_ij:

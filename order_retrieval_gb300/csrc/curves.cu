@@ -2,7 +2,8 @@
 // codes themselves come from encode.cu).
 //
 // Passage: OpenReview discussion of "ZETA: Leveraging Z-order Curves for
-// Efficient Top-k Attention", reply on the asymmetry of Z-order curves: the
+// Efficient Top-k Attention", follow-up reply on interleaving the bits of
+// different dimensions (several curves): the
 // coordinates of each key are interleaved in several orders (the three cyclic
 // shifts of (K^1, K^2, K^3), or all six orderings) and every curve contributes
 // k // curves of the k selected tokens.

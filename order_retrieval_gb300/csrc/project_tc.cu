@@ -2,8 +2,8 @@
 // encode, on the Blackwell tensor cores (tcgen05 + TMEM, TMA-fed).
 //
 // Passage: OpenReview discussion of "ZETA: Leveraging Z-order Curves for
-// Efficient Top-k Attention", reply A "LLMs impact the selection of d_K" (a
-// two-layer neural network projects the input into the low-dimensional keys),
+// Efficient Top-k Attention", reply A "LLMs impact the selection of d_K" (the
+// low-dimensional keys come out of a small network of two layers),
 // and reply A2 "Clarification of Binary Expansion and Precision" (the codes).
 // Per head hd and token t (queries and keys each with their own weights):
 //   h_f = max(0, W1[hd F + f] . x_t + b1[hd F + f]),   f < F

@@ -1,9 +1,9 @@
 // radix.cu -- segmented, stable LSD radix sort of (key, value) pairs.
 //
-// The pages sort Z-order codes with "an efficiently implemented radix sorting
-// operation" (OpenReview discussion of "ZETA: Leveraging Z-order Curves for
-// Efficient Top-k Attention", reply A3 "Chunking ... & Where efficiency is
-// coming from").  Here each (b, h) slice is one segment.  Every 8-bit digit pass
+// The pages sort the Z-order codes with a radix sort (OpenReview discussion of
+// "ZETA: Leveraging Z-order Curves for Efficient Top-k Attention", reply A3
+// "Chunking ... & Where efficiency is coming from").  Here each (b, h) slice is
+// one segment.  Every 8-bit digit pass
 // is three launches with no inter-block waiting (reduce, then scan, then
 // scatter), so nothing spins and the order is deterministic:
 //   upsweep   per tile of 4096 items: digit histogram -> hist[seg][tile][digit]

@@ -2,7 +2,8 @@
 per-curve windows).
 
 Source: "ZETA: Leveraging Z-order Curves for Efficient Top-k Attention",
-OpenReview discussion, reply on the asymmetry of Z-order curves: three curves
+OpenReview discussion, follow-up reply on interleaving the bits of
+different dimensions (several curves): three curves
 over the cyclic shifts of (K^1, K^2, K^3), or six over all orderings, each
 contributing k//3 (k//6) of the k selected tokens.
 
