@@ -530,9 +530,42 @@ def run_ours(args, w, rank, world):
     fus_k_ms = sum(fus_k) / len(fus_k)
     del plan_f
 
+    variants = {}
+    # --- the pages' 12-bit grid (36-bit codes in 64-bit words) on the same
+    # workload: the whole forward, and its index part
+    w12 = we.replace(bits=12)
+    p12 = zb.problem_of(w12)
+    plan12 = ZetaPlan(p12, dev, backward=False)
+    for _ in range(warm):
+        plan12.forward(qe, ke, ve, gme)
+    tot12, idx12 = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        e = [ev() for _ in range(3)]
+        e[0].record()
+        zb.zeta_encode(p12, qe, plan12.q_codes)
+        zb.zeta_encode(p12, ke, plan12.k_codes)
+        zb.zeta_sort_chunks(p12, plan12.k_codes, plan12.prefix_codes, plan12.prefix_idx,
+                            plan12.sort_ws)
+        zb.zeta_select_topk(p12, plan12.q_codes, plan12.prefix_codes, plan12.prefix_idx,
+                            plan12.idx)
+        e[1].record()
+        zb.zeta_attend_fwd(p12, qe, ke, ve, gme, plan12.idx, plan12.out, plan12.rowsum,
+                           plan12.status)
+        e[2].record()
+        e[2].synchronize()
+        tot12.append(e[0].elapsed_time(e[2]))
+        idx12.append(e[0].elapsed_time(e[1]))
+    if int(plan12.status.item()) != 0:
+        raise RuntimeError(f"device status {plan12.status.item()} (12-bit grid)")
+    ms12 = sum(tot12) / len(tot12)
+    variants["grid12"] = {"workload": we.name + " with bits=12 (u64 codes)",
+                          "fwd_tokens_per_s": we.B * we.N * world / (ms12 * 1e-3),
+                          "fwd_ms": ms12, "encode_sort_select_ms": sum(idx12) / len(idx12)}
+    del plan12
+
     # --- multi-curve variant (3 cyclic / 6 permuted coordinate orders) on the
     # efficiency workload: the whole forward, and its index part
-    variants = {}
     for curves in (3, 6):
         pc = ZetaPlan(pe, dev, backward=False, curves=curves)
         for _ in range(warm):
