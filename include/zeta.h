@@ -333,6 +333,21 @@ zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, const flo
                               void *workspace, size_t ws_bytes, int32_t *dev_status,
                               cudaStream_t stream);
 
+/*
+ * zeta_check_bounded_wait -- diagnostic of the device-side failure detection.
+ * The pages have no counterpart: every wait of the TMA-fed and tensor-core
+ * kernels (zeta_project_encode) on an mbarrier polls a bounded number of times
+ * and, when it gives up, records ZETA_ERR_DEVICE_TIMEOUT in the status word and
+ * lets the kernel return.  This call runs that wait on one barrier, completed
+ * beforehand when arrive != 0 and never completed otherwise, polling at most
+ * `iterations` times.
+ *   dev_status  int32 device word (required); ZETA_ERR_DEVICE_TIMEOUT is written
+ *               there when the wait gave up, nothing otherwise.
+ * Errors: ZETA_ERR_INVALID_ARG (null dev_status, zero iterations).
+ */
+zeta_status_t zeta_check_bounded_wait(uint32_t iterations, int32_t arrive, int32_t *dev_status,
+                                      cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -103,6 +103,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.zeta_attend_fwd.restype = S
     L.zeta_attend_bwd.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
     L.zeta_select_attend_fwd.argtypes = [PP] + [P] * 12
+    L.zeta_check_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_int32, P, P]
+    L.zeta_check_bounded_wait.restype = S
     L.zeta_select_attend_fwd.restype = S
     L.zeta_attend_bwd.restype = S
     _lib = L
@@ -277,6 +279,16 @@ def zeta_project_encode(p, D, F, x, w1, b1, w2, b2, q, k, q_codes, k_codes, dev_
                                      _ptr(b1), _ptr(w2), _ptr(b2), _ptr(q), _ptr(k),
                                      _ptr(q_codes), _ptr(k_codes), _ptr(dev_status),
                                      _stream(stream)))
+
+
+def zeta_check_bounded_wait(iterations, arrive, dev_status, stream=None):
+    """Run the kernels' bounded mbarrier wait on a barrier that is (arrive=1) or
+    is not (arrive=0) completed; a wait that gives up writes
+    ZETA_ERR_DEVICE_TIMEOUT to dev_status."""
+    _expect(dev_status, "dev_status", torch.int32, 1)
+    _check("zeta_check_bounded_wait",
+           lib().zeta_check_bounded_wait(int(iterations), int(arrive), _ptr(dev_status),
+                                         _stream(stream)))
 
 
 def curve_axes(d_K: int, curves: int) -> list:

@@ -229,3 +229,9 @@ ZETA_API zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, 
     return from_cuda(zeta::launch_attend_bwd(pr, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma,
                                              workspace, dev_status, stream));
 }
+
+ZETA_API zeta_status_t zeta_check_bounded_wait(uint32_t iterations, int32_t arrive,
+                                               int32_t *dev_status, cudaStream_t stream) {
+    if (!dev_status || iterations == 0) return ZETA_ERR_INVALID_ARG;
+    return from_cuda(zeta::launch_bounded_wait_check(iterations, arrive, dev_status, stream));
+}

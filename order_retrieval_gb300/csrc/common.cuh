@@ -137,6 +137,11 @@ cudaError_t launch_attend_fwd(const Prob &p, const float *q, const float *k, con
                               const float *gamma, const int32_t *idx, void *out, float *rowsum,
                               int32_t *status, cudaStream_t st);
 
+// The bounded mbarrier wait on a barrier that is (arrive != 0) or is not
+// completed; a wait that gives up records ZETA_ERR_DEVICE_TIMEOUT.
+cudaError_t launch_bounded_wait_check(uint32_t limit, int arrive, int32_t *status,
+                                      cudaStream_t st);
+
 // Select + attend in one call (fused kernel on the tensor-core shapes).
 cudaError_t launch_select_attend_fwd(const Prob &p, const float *q, const float *k,
                                      const void *v, const float *gamma, const void *q_codes,

@@ -194,3 +194,9 @@ def test_select_attend_checks_its_arguments(L):
     assert L.zeta_select_attend_fwd(ctypes.byref(e), *([None] * 12)) == 0
     pe = zb.problem(0, 2, 1024, 3, 32, 16, 128, 10, "f32")
     zb.zeta_select_attend_fwd(pe, *([None] * 10), stream=0)
+
+
+def test_bounded_wait_check_arguments(L):
+    fake = ctypes.c_void_p(0x1000)
+    assert L.zeta_check_bounded_wait(100, 0, None, None) == 1
+    assert L.zeta_check_bounded_wait(0, 0, fake, None) == 1
