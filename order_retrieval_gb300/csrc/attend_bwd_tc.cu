@@ -570,13 +570,27 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
 
 // ============================================================== key side ===
 
-struct __align__(16) KSmem {
+// Tiles of the own-chunk part.
+struct __align__(16) KOwn {
     __nv_bfloat16 v[T64 * DV];
     __nv_bfloat16 dO[2][T64 * DV];
     QRec qr[2][T64];
+};
+constexpr int kKeyWarps = THREADS / 32;
+constexpr uint32_t kRingBytes = 2 * 32 * DV * 2;   // one warp's two slots of 32 dO rows
+constexpr int kGs = 24;                            // row stride (floats) of the G scratch
+constexpr size_t kKeyBig = sizeof(KOwn) > kKeyWarps * kRingBytes ? sizeof(KOwn)
+                                                                 : kKeyWarps * kRingBytes;
+
+// The window walk's rings and the own-chunk tiles share `big` (the walk ends in
+// every warp before the tiles are staged); a warp's G scratch lives in its own
+// rows of dvp until its dv rows are written there.
+struct __align__(16) KSmem {
+    unsigned char big[kKeyBig];
     float dvp[T64][DV + 4];
     float dkp[T64][4];
 };
+static_assert(32 * kGs <= 16 * (DV + 4), "G scratch fits in a warp's dvp rows");
 
 template <int DK, int WK>
 __global__ void __launch_bounds__(THREADS, 4)
@@ -585,7 +599,9 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
            const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q, uint32_t csr_mask,
            const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
            __nv_bfloat16 *__restrict__ dv, int N, int H, int C, int tiles_per_chunk) {
-    __shared__ KSmem sm;
+    extern __shared__ __align__(16) unsigned char key_smem[];
+    KSmem &sm = *reinterpret_cast<KSmem *>(key_smem);
+    KOwn &own = *reinterpret_cast<KOwn *>(sm.big);
     const int64_t seg = blockIdx.y;
     const int c = blockIdx.x / tiles_per_chunk;
     const int kt = blockIdx.x % tiles_per_chunk;
@@ -601,156 +617,240 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     const QRec *rb_ = rec + seg * (int64_t)N;
 
     auto load_qtile = [&](int b, int iq0) {
-        stage_rows(sm.dO[b], db, iq0, cend);
+        stage_rows(own.dO[b], db, iq0, cend);
         if (threadIdx.x < T64 * 2) {
             const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
             const int i = iq0 + r;
             const bool ok = i < cend;
-            cp_async16(smem_u32(reinterpret_cast<float4 *>(&sm.qr[b][r]) + h),
+            cp_async16(smem_u32(reinterpret_cast<float4 *>(&own.qr[b][r]) + h),
                        reinterpret_cast<const float4 *>(rb_ + (ok ? i : iq0)) + h, ok ? 16 : 0);
         }
     };
-    stage_rows(sm.v, vb, j0, jend);
-    load_qtile(0, j0);                // query tiles start at the key tile
-    cp_async_commit();
-
     // ---------------------------------------------------- window part ---
+    // The queries that selected this warp's 16 keys are one contiguous run of
+    // the transposed lists (the lists of consecutive keys are adjacent), walked
+    // 32 entries at a time whatever key each entry belongs to.  Lane e owns
+    // entry e of a step: its key (the last key whose list starts at or before
+    // it), its query's record, w, a = w / s and the dk term.  The step's 32 dO
+    // rows are copied into a two-slot ring of swizzled 128-byte rows in shared
+    // memory (cp.async) one step ahead, the list positions two steps ahead.
+    // With the 16 keys' v rows as the columns of B, G = dO_rows . V_keys^T on
+    // the tensor cores gives every entry's g in the column of its key (read
+    // back through a small scratch tile), and dV_keys += dO^T A, A holding a in
+    // the column of the entry's key, accumulates all 16 keys' dv in the mma
+    // registers over the whole walk.  A key half (8 columns) that no entry of a
+    // 16-entry tile belongs to is skipped.  The dk terms are summed per key by a
+    // segmented scan over the step (entries of one key are adjacent), in the
+    // order of the list.
     const uint32_t *lst = csr_q + seg * csr_stride;
     const uint32_t *ob = off + seg * (int64_t)(N + 1);
-    // Each key's list is walked 32 entries at a time.  Lane e owns entry e of a
-    // chunk (its query's record, the weight w, a = w / s and the dk term).  The
-    // dO rows of a chunk are loaded as two 16-entry tiles, lane (g, t) taking
-    // 16-byte slices 2t, 2t+1 of rows g and g+8: these serve in place as the A
-    // fragments of G = dO_rows . v_j on the tensor cores (v_j in column 0 of B;
-    // the order of the dimensions does not matter for a dot product).  The
-    // same registers, transposed 8x8 block by block with movmatrix, are the A
-    // fragments of dv_j += dO^T a (16 dimensions per mma, a rounded to bf16 in
-    // column 0 of B, as the own-chunk P is), so dv_j accumulates in the mma's
-    // column-0 registers across the whole list.  The next chunk's list
-    // positions are fetched while the current chunk is processed.
+    constexpr uint32_t kNone = 0xffffffffu;
     const int wj0 = j0 + warp * 16;
     const int nkw = max(0, min(16, jend - wj0));
-    const uint32_t bnd = lane <= nkw ? ob[wj0 + lane] : 0u;     // list bounds of this warp
+    // lane r < nkw: start of key r's list; lane nkw: end of the last list;
+    // other lanes: a bound that no list position reaches
+    const uint32_t bnd = (nkw > 0 && lane <= nkw) ? ob[wj0 + lane] : kNone;
+    const uint32_t bnd_hi = __shfl_sync(kFull, bnd, (lane + 1) & 31);   // lane r: end of key r's list
+    const uint32_t P0 = __shfl_sync(kFull, bnd, 0);
+    const uint32_t P1 = __shfl_sync(kFull, bnd, nkw);
+    const int nch = nkw > 0 ? (int)((P1 - P0 + 31) >> 5) : 0;
     const int g4 = lane >> 2, s4 = lane & 3;
-    for (int r = 0; r < 16; ++r) {
-        const int row = warp * 16 + r;
-        const int j = wj0 + r;
-        float cdv[4][4];            // dv_j: column 0 of four 16-dimension mma tiles
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) cdv[c][e] = 0.f;
-        float dka[4] = {0.f, 0.f, 0.f, 0.f};
-        if (r < nkw) {
-            uint4 vja = make_uint4(0u, 0u, 0u, 0u), vjb = vja;   // B column 0: lanes 0..3
-            if (g4 == 0) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(vb + (int64_t)j * DV + s4 * 16);
-                vja = src[0];
-                vjb = src[1];
-            }
-            const float4 kj = load_k4(kb + (int64_t)j * DK, DK);
-            const float kjc[4] = {kj.x, kj.y, kj.z, kj.w};
-            const uint32_t p0 = __shfl_sync(kFull, bnd, r), p1 = __shfl_sync(kFull, bnd, r + 1);
-            uint32_t inext = p0 + lane < p1 ? (__ldg(lst + p0 + lane) & csr_mask) : 0xffffffffu;
-            for (uint32_t p = p0; p < p1; p += 32) {
-                const uint32_t ie = inext;
-                inext = p + 32 + lane < p1 ? (__ldg(lst + p + 32 + lane) & csr_mask) : 0xffffffffu;
-                const bool own = ie != 0xffffffffu;
-                const int nmt = min(2, (int)((p1 - p + 15) >> 4));   // 16-entry tiles
-                uint4 dbuf[2][4];                    // rows g, g+8 of tile mt: slices 2t, 2t+1
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t iu = __shfl_sync(kFull, ie, 16 * mt + 8 * h + g4);
-                        const bool ok = mt < nmt && iu != 0xffffffffu;
-                        const uint4 *src =
-                            reinterpret_cast<const uint4 *>(db + (int64_t)iu * DV + s4 * 16);
-                        dbuf[mt][2 * h] = ok ? ld_stream16(src) : make_uint4(0u, 0u, 0u, 0u);
-                        dbuf[mt][2 * h + 1] = ok ? ld_stream16(src + 1) : make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-                // the owner's scalars for its entry
-                float a = 0.f, s2 = 0.f, inv_s = 0.f, ngbs = 0.f;
-                float dqk[4] = {0.f, 0.f, 0.f, 0.f};
-                if (own) {
-                    const QRec qrc = rb_[ie];
-                    const float qc[4] = {qrc.q.x, qrc.q.y, qrc.q.z, qrc.q.w};
-                    float d2 = 0.f;
-#pragma unroll
-                    for (int d = 0; d < DK; ++d) {
-                        dqk[d] = qc[d] - kjc[d];
-                        d2 = __fmaf_rn(dqk[d], dqk[d], d2);
-                    }
-                    const float w = weight_fast<WK>(d2, qrc.sg.z, inv_g2);
-                    inv_s = qrc.sg.x;
-                    ngbs = qrc.sg.w;
-                    a = w * inv_s;
-                    // Cauchy: 2 w^2 / gamma^2 with the constant applied to dk at the end
-                    s2 = WK == kWCauchy ? w * w : 2.f * neg_dw_dd2<WK>(w, inv_g2);
-                }
-                float cg[2][4];
-                const uint32_t v0[4] = {vja.x, vja.y, vja.z, vja.w};
-                const uint32_t v1[4] = {vjb.x, vjb.y, vjb.z, vjb.w};
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) cg[mt][e] = 0.f;
-                    if (mt < nmt) {
-                        const uint32_t ra0[4] = {dbuf[mt][0].x, dbuf[mt][0].y, dbuf[mt][0].z, dbuf[mt][0].w};
-                        const uint32_t ra1[4] = {dbuf[mt][1].x, dbuf[mt][1].y, dbuf[mt][1].z, dbuf[mt][1].w};
-                        const uint32_t rb0[4] = {dbuf[mt][2].x, dbuf[mt][2].y, dbuf[mt][2].z, dbuf[mt][2].w};
-                        const uint32_t rb1[4] = {dbuf[mt][3].x, dbuf[mt][3].y, dbuf[mt][3].z, dbuf[mt][3].w};
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint32_t af[4] = {ra0[ks], rb0[ks], ra1[ks], rb1[ks]};
-                            mma16816(cg[mt], af, v0[ks], v1[ks]);
-                        }
-                        // dv_j += dO^T a: entries 2t, 2t+1 (+8) of the tile in B column 0
-                        const float e0 = __shfl_sync(kFull, a, 16 * mt + 2 * s4);
-                        const float e1 = __shfl_sync(kFull, a, 16 * mt + 2 * s4 + 1);
-                        const float e2 = __shfl_sync(kFull, a, 16 * mt + 2 * s4 + 8);
-                        const float e3 = __shfl_sync(kFull, a, 16 * mt + 2 * s4 + 9);
-                        const uint32_t ba = g4 == 0 ? pack_bf16(e0, e1) : 0u;
-                        const uint32_t bb = g4 == 0 ? pack_bf16(e2, e3) : 0u;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {   // dims 16 (m/2) + 8 h + 2c + (m%2)
-                            const uint32_t af[4] = {movmatrix_trans(ra0[c]), movmatrix_trans(ra1[c]),
-                                                    movmatrix_trans(rb0[c]), movmatrix_trans(rb1[c])};
-                            mma16816(cdv[c], af, ba, bb);
-                        }
-                    }
-                }
-                // entry L: tile L >> 4, row half (L >> 3) & 1, row L & 7 -> lane 4 (L & 7)
-                const int srcl = (lane & 7) * 4;
-                const float x0 = __shfl_sync(kFull, cg[0][0], srcl);
-                const float x1 = __shfl_sync(kFull, cg[0][2], srcl);
-                const float x2 = __shfl_sync(kFull, cg[1][0], srcl);
-                const float x3 = __shfl_sync(kFull, cg[1][2], srcl);
-                const float gown = (lane >> 4) ? (((lane >> 3) & 1) ? x3 : x2)
-                                               : (((lane >> 3) & 1) ? x1 : x0);
-                if (own) {
-                    const float coef = __fmaf_rn(gown, inv_s, ngbs) * s2;
-#pragma unroll
-                    for (int d = 0; d < DK; ++d) dka[d] = __fmaf_rn(coef, dqk[d], dka[d]);
-                }
-            }
-#pragma unroll
-            for (int d = 0; d < DK; ++d)
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) dka[d] += __shfl_xor_sync(kFull, dka[d], o);
-        }
-        if (s4 == 0) {              // lane 4m holds mma rows m and m+8 of column 0
-            const int d0 = 16 * (g4 >> 1) + (g4 & 1);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                sm.dvp[row][d0 + 2 * c] = cdv[c][0];
-                sm.dvp[row][d0 + 8 + 2 * c] = cdv[c][2];
-            }
-        }
-        if (lane == 0) *reinterpret_cast<float4 *>(sm.dkp[row]) =
-            make_float4(dka[0], dka[1], dka[2], dka[3]);
+    float kc[4] = {0.f, 0.f, 0.f, 0.f};                       // lane r: key r's coordinates
+    if (lane < nkw) {
+        const float4 t = load_k4(kb + (int64_t)(wj0 + lane) * DK, DK);
+        kc[0] = t.x; kc[1] = t.y; kc[2] = t.z; kc[3] = t.w;
     }
+    // B fragments of G: column g of key half h is v of key 8h + g; rows are the
+    // dimensions 16 ks + 2t, +1 and 16 ks + 2t + 8, +9
+    uint32_t vbf[2][4][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int key = 8 * h + g4;
+        const uint32_t *vr = reinterpret_cast<const uint32_t *>(vb + (int64_t)(wj0 + key) * DV);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            vbf[h][ks][0] = key < nkw ? vr[8 * ks + s4] : 0u;
+            vbf[h][ks][1] = key < nkw ? vr[8 * ks + s4 + 4] : 0u;
+        }
+    }
+    float cdv[4][2][4];          // dv of the 16 keys: dims 16c + g (+8) x keys 8h + 2t (+1)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cdv[c][h][e] = 0.f;
+    float dkacc[4] = {0.f, 0.f, 0.f, 0.f};                    // lane r: dk of key r
+    const uint32_t ring = smem_u32(sm.big) + (uint32_t)warp * kRingBytes;
+    float *gs = &sm.dvp[warp * 16][0];                        // G scratch: [32 entries][kGs]
+    auto list_at = [&](int n) -> uint32_t {
+        const uint32_t pp = P0 + 32u * (uint32_t)n + (uint32_t)lane;
+        return (n < nch && pp < P1) ? (__ldg(lst + pp) & csr_mask) : kNone;
+    };
+    auto issue = [&](int n, uint32_t ie) {                    // dO rows of step n
+        const uint32_t slot = ring + (uint32_t)(n & 1) * (kRingBytes / 2);
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            const int row = 4 * h + (lane >> 3), ch = lane & 7;
+            const uint32_t iu = __shfl_sync(kFull, ie, row);
+            const bool ok = iu != kNone;
+            cp_async16(slot + (uint32_t)swz(row, ch) * 2u, db + (int64_t)(ok ? iu : 0u) * DV + ch * 8,
+                       ok ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    auto record = [&](uint32_t ie, float4 &r0, float4 &r1) {
+        if (ie != kNone) {
+            const float4 *src = reinterpret_cast<const float4 *>(rb_ + ie);
+            r0 = __ldg(src);
+            r1 = __ldg(src + 1);
+        } else {
+            r0 = make_float4(0.f, 0.f, 0.f, 0.f);
+            r1 = r0;
+        }
+    };
+    uint32_t ie_cur = list_at(0);
+    float4 rn0, rn1;
+    if (nch > 0) issue(0, ie_cur);
+    record(ie_cur, rn0, rn1);
+    uint32_t ie_nxt = list_at(1);
+    for (int n = 0; n < nch; ++n) {
+        const float4 rq0 = rn0, rq1 = rn1;
+        const uint32_t ie = ie_cur;
+        if (n + 1 < nch) {
+            issue(n + 1, ie_nxt);
+            record(ie_nxt, rn0, rn1);
+        }
+        ie_cur = ie_nxt;
+        ie_nxt = list_at(n + 2);
+        if (n + 1 < nch) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        __syncwarp();
+        const uint32_t slot = ring + (uint32_t)(n & 1) * (kRingBytes / 2);
+        const uint32_t base = P0 + 32u * (uint32_t)n;
+        const uint32_t pos = base + (uint32_t)lane;
+        const bool valid = ie != kNone;
+        int kr = 0;
+#pragma unroll
+        for (int st = 8; st > 0; st >>= 1)
+            if (__shfl_sync(kFull, bnd, kr + st) <= pos) kr += st;
+        float kj[4];
+#pragma unroll
+        for (int d = 0; d < DK; ++d) kj[d] = __shfl_sync(kFull, kc[d], kr);
+        float a = 0.f, s2 = 0.f, inv_s = 0.f, ngbs = 0.f;
+        float dqk[4] = {0.f, 0.f, 0.f, 0.f};
+        if (valid) {
+            const float qc[4] = {rq0.x, rq0.y, rq0.z, rq0.w};
+            float d2 = 0.f;
+#pragma unroll
+            for (int d = 0; d < DK; ++d) {
+                dqk[d] = qc[d] - kj[d];
+                d2 = __fmaf_rn(dqk[d], dqk[d], d2);
+            }
+            const float w = weight_fast<WK>(d2, rq1.z, inv_g2);
+            inv_s = rq1.x;
+            ngbs = rq1.w;
+            a = w * inv_s;
+            // Cauchy: 2 w^2 / gamma^2 with the constant applied to dk at the end
+            s2 = WK == kWCauchy ? w * w : 2.f * neg_dw_dd2<WK>(w, inv_g2);
+        }
+        // keys met by each 16-entry tile (the step's entries are in key order)
+        const int last = min(31, (int)(P1 - base) - 1);
+        const int kr0 = __shfl_sync(kFull, kr, 0);
+        const int kr15 = __shfl_sync(kFull, kr, min(15, last));
+        const int kr16 = __shfl_sync(kFull, kr, 16);
+        const int kr31 = __shfl_sync(kFull, kr, last);
+        const uint32_t pk = ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) << 16) |
+                            (uint32_t)kr;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            if (mt == 1 && last < 16) break;
+            const int klo = mt ? kr16 : kr0, khi = mt ? kr31 : kr15;
+            const bool half[2] = {klo < 8, khi >= 8};
+            uint32_t af[4][4];
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                ldsm_x4(af[ks], slot + (uint32_t)swz(16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1),
+                                                    2 * ks + (lane >> 4)) * 2u);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (!half[h]) continue;
+                float cg[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma16816(cg, af[ks], vbf[h][ks][0], vbf[h][ks][1]);
+                *reinterpret_cast<float2 *>(gs + (16 * mt + g4) * kGs + 8 * h + 2 * s4) =
+                    make_float2(cg[0], cg[1]);
+                *reinterpret_cast<float2 *>(gs + (16 * mt + g4 + 8) * kGs + 8 * h + 2 * s4) =
+                    make_float2(cg[2], cg[3]);
+            }
+            // dV_keys += dO^T A: entries 2t, 2t+1 (+8) of the tile in the rows of B
+            const uint32_t e0 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4);
+            const uint32_t e1 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 1);
+            const uint32_t e2 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 8);
+            const uint32_t e3 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 9);
+            uint32_t at[4][4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ldsm_x4_trans(at[c], slot + (uint32_t)swz(16 * mt + (lane & 7) + 8 * (lane >> 4),
+                                                         2 * c + ((lane >> 3) & 1)) * 2u);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (!half[h]) continue;
+                const uint32_t key = (uint32_t)(8 * h + g4);
+                auto pick = [key](uint32_t e) { return (e & 0xffffu) == key ? (e >> 16) : 0u; };
+                const uint32_t b0 = pick(e0) | (pick(e1) << 16);
+                const uint32_t b1 = pick(e2) | (pick(e3) << 16);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mma16816(cdv[c][h], at[c], b0, b1);
+            }
+        }
+        __syncwarp();
+        const float gown = valid ? gs[lane * kGs + kr] : 0.f;
+        const float coef = valid ? __fmaf_rn(gown, inv_s, ngbs) * s2 : 0.f;
+        float x[4];
+#pragma unroll
+        for (int d = 0; d < DK; ++d) x[d] = coef * dqk[d];
+        // segmented inclusive scan: a lane adds only entries of its own key
+        const uint32_t kst = __shfl_sync(kFull, bnd, kr);
+        const int first = kst > base ? (int)(kst - base) : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+            for (int d = 0; d < DK; ++d) {
+                const float y = __shfl_up_sync(kFull, x[d], o);
+                if (lane - o >= first) x[d] += y;
+            }
+        }
+        // lane r < nkw takes key r's run of this step from the run's last entry
+        const bool has = lane < nkw && bnd_hi > base && bnd < base + 32u && bnd < bnd_hi;
+        const int tail = has ? (int)(min(bnd_hi, base + 32u) - 1u - base) : 0;
+#pragma unroll
+        for (int d = 0; d < DK; ++d) {
+            const float y = __shfl_sync(kFull, x[d], tail);
+            if (has) dkacc[d] += y;
+        }
+        __syncwarp();
+    }
+    // this warp's dv and dk rows (keys 8h + 2t (+1), dims 16c + g (+8))
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int row = warp * 16 + 8 * h + 2 * s4;
+            const int col = 16 * c + g4;
+            sm.dvp[row][col] = cdv[c][h][0];
+            sm.dvp[row + 1][col] = cdv[c][h][1];
+            sm.dvp[row][col + 8] = cdv[c][h][2];
+            sm.dvp[row + 1][col + 8] = cdv[c][h][3];
+        }
+    if (lane < 16)
+        *reinterpret_cast<float4 *>(sm.dkp[warp * 16 + lane]) =
+            make_float4(dkacc[0], dkacc[1], dkacc[2], dkacc[3]);
+    // every warp's walk is done before the rings become the own-chunk tiles
+    __syncthreads();
+    stage_rows(own.v, vb, j0, jend);
+    load_qtile(0, j0);                // query tiles start at the key tile
+    cp_async_commit();
 
     // ------------------------------------------------- own-chunk part ---
     const int g8 = lane >> 2, tig = lane & 3;
@@ -780,8 +880,8 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     const int warp_key_last = j0 + warp * 16 + 15;
     const bool warp_keys_full = warp_key_last < jend;
     auto qtile = [&](int t, int iq0, auto masked) {
-        const uint32_t vbase = smem_u32(sm.v);
-        const uint32_t dbase = smem_u32(sm.dO[t & 1]);
+        const uint32_t vbase = smem_u32(own.v);
+        const uint32_t dbase = smem_u32(own.dO[t & 1]);
         // S^T = V . dO^T : 16 keys x 64 queries per warp
         float s[8][4];
 #pragma unroll
@@ -803,7 +903,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
         }
         // element-wise terms for key rows (a, b) packed; P^T into A fragments,
         // then dV += P^T . dO
-        const QRec *qt_rec = sm.qr[t & 1];
+        const QRec *qt_rec = own.qr[t & 1];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             float pa_[8];
@@ -937,23 +1037,39 @@ void bwd_query_tc_dk(const Prob &p, dim3 grid, int tpc, const float *q, const fl
 #undef ZETA_BQ
 }
 
+template <int D, int WK>
+cudaError_t bwd_key_tc_launch(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
+                              const float *gamma, const void *dout, const void *rec,
+                              const uint32_t *csr_q, uint32_t csr_mask, const uint32_t *off,
+                              int64_t csr_stride, float *dk, void *dv, cudaStream_t st) {
+    static PerDeviceOnce smem_once;          // run once per device, outside any capture
+    const cudaError_t e = smem_once.run([] {
+        return cudaFuncSetAttribute(bwd_key_tc<D, WK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)sizeof(KSmem));
+    });
+    if (e != cudaSuccess) return e;
+    bwd_key_tc<D, WK><<<grid, THREADS, sizeof(KSmem), st>>>(
+        k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout),
+        static_cast<const QRec *>(rec), csr_q, csr_mask, off, csr_stride, dk,
+        static_cast<__nv_bfloat16 *>(dv), p.N, p.H, p.C, tpc);
+    return cudaGetLastError();
+}
+
 template <int WK>
-void bwd_key_tc_dk(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
-                   const float *gamma, const void *dout, const void *rec, const uint32_t *csr_q,
-                   uint32_t csr_mask, const uint32_t *off, int64_t csr_stride, float *dk, void *dv,
-                   cudaStream_t st) {
-#define ZETA_BK(D)                                                                              \
-    bwd_key_tc<D, WK><<<grid, THREADS, 0, st>>>(                                               \
-        k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout), \
-        static_cast<const QRec *>(rec), csr_q, csr_mask, off, csr_stride, dk,                 \
-        static_cast<__nv_bfloat16 *>(dv), p.N, p.H, p.C, tpc)
+cudaError_t bwd_key_tc_dk(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
+                          const float *gamma, const void *dout, const void *rec,
+                          const uint32_t *csr_q, uint32_t csr_mask, const uint32_t *off,
+                          int64_t csr_stride, float *dk, void *dv, cudaStream_t st) {
     switch (p.dK) {
-        case 1: ZETA_BK(1); break;
-        case 2: ZETA_BK(2); break;
-        case 3: ZETA_BK(3); break;
-        default: ZETA_BK(4); break;
+        case 1: return bwd_key_tc_launch<1, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+                                                csr_mask, off, csr_stride, dk, dv, st);
+        case 2: return bwd_key_tc_launch<2, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+                                                csr_mask, off, csr_stride, dk, dv, st);
+        case 3: return bwd_key_tc_launch<3, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+                                                csr_mask, off, csr_stride, dk, dv, st);
+        default: return bwd_key_tc_launch<4, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+                                                 csr_mask, off, csr_stride, dk, dv, st);
     }
-#undef ZETA_BK
 }
 
 cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, const void *v,
@@ -981,15 +1097,13 @@ cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, cons
     const int tpc = (p.C + T64 - 1) / T64;
     const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
     if (p.wk == kWSoftmax)
-        bwd_key_tc_dk<kWSoftmax>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
-                                 csr_stride, dk, dv, st);
-    else if (p.wk == kWInvEuclid)
-        bwd_key_tc_dk<kWInvEuclid>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
+        return bwd_key_tc_dk<kWSoftmax>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask,
+                                        off, csr_stride, dk, dv, st);
+    if (p.wk == kWInvEuclid)
+        return bwd_key_tc_dk<kWInvEuclid>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask,
+                                          off, csr_stride, dk, dv, st);
+    return bwd_key_tc_dk<kWCauchy>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
                                    csr_stride, dk, dv, st);
-    else
-        bwd_key_tc_dk<kWCauchy>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
-                                csr_stride, dk, dv, st);
-    return cudaGetLastError();
 }
 
 }  // namespace zeta

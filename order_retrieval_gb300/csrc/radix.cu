@@ -8,8 +8,9 @@
 // scatter), so nothing spins and the order is deterministic:
 //   upsweep   per tile of 4096 items: digit histogram -> hist[seg][tile][digit]
 //   scan      per segment: exclusive scan of hist in (digit, tile) order
-//   downsweep per tile: stable rank of every item among equal digits (warp
-//             match + per-warp counters bumped by one lane per digit group),
+//   downsweep per tile: stable rank of every item among equal digits (digit
+//             groups from ballots + per-warp counters bumped by one lane per
+//             group),
 //             scatter to hist offset + rank.
 #include "common.cuh"
 
@@ -211,10 +212,17 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
     }
 #pragma unroll
     for (int r = 0; r < kRadixItems; ++r) {
-        // the lowest lane of each equal-digit group bumps the warp's counter for
-        // that digit and hands the old count to its group (a warp's atomics on one
-        // counter take effect in program order, so items keep their order)
-        const unsigned peers = __match_any_sync(kFull, dig[r]);
+        // lanes with this lane's digit: eight ballots, one per digit bit (far
+        // cheaper here than a warp match); the lowest lane of each group bumps
+        // the warp's counter for that digit and hands the old count to its group
+        // (a warp's atomics on one counter take effect in program order, so
+        // items keep their order)
+        unsigned peers = __ballot_sync(kFull, dig[r] < 256);
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const unsigned bal = __ballot_sync(kFull, (dig[r] >> b) & 1);
+            peers &= ((dig[r] >> b) & 1) ? bal : ~bal;
+        }
         const int leader = __ffs(peers) - 1;
         uint32_t old = 0;
         if (dig[r] < 256 && lane == leader) old = atomicAdd(&wcnt[w][dig[r]], __popc(peers));
