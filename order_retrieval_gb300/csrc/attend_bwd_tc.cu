@@ -579,6 +579,9 @@ struct __align__(16) KOwn {
 constexpr int kKeyWarps = THREADS / 32;
 constexpr uint32_t kRingBytes = 2 * 32 * DV * 2;   // one warp's two slots of 32 dO rows
 constexpr int kGs = 24;                            // row stride (floats) of the G scratch
+// Column swizzle of the G scratch (even, so float2 pairs stay together): the
+// read of one column by all 32 rows spreads over 16 banks instead of 4.
+__device__ __forceinline__ int gs_swz(int row) { return ((row >> 2) & 3) << 1; }
 constexpr size_t kKeyBig = sizeof(KOwn) > kKeyWarps * kRingBytes ? sizeof(KOwn)
                                                                  : kKeyWarps * kRingBytes;
 
@@ -778,9 +781,10 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 float cg[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) mma16816(cg, af[ks], vbf[h][ks][0], vbf[h][ks][1]);
-                *reinterpret_cast<float2 *>(gs + (16 * mt + g4) * kGs + 8 * h + 2 * s4) =
+                const int ra = 16 * mt + g4, rb2 = ra + 8;
+                *reinterpret_cast<float2 *>(gs + ra * kGs + ((8 * h + 2 * s4) ^ gs_swz(ra))) =
                     make_float2(cg[0], cg[1]);
-                *reinterpret_cast<float2 *>(gs + (16 * mt + g4 + 8) * kGs + 8 * h + 2 * s4) =
+                *reinterpret_cast<float2 *>(gs + rb2 * kGs + ((8 * h + 2 * s4) ^ gs_swz(rb2))) =
                     make_float2(cg[2], cg[3]);
             }
             // dV_keys += dO^T A: entries 2t, 2t+1 (+8) of the tile in the rows of B
@@ -788,11 +792,16 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             const uint32_t e1 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 1);
             const uint32_t e2 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 8);
             const uint32_t e3 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 9);
+            // A of dim block c: the 8x8 blocks of the G fragments transposed in
+            // registers (entries 0-7 | 8-15 x dims 0-7 | 8-15 of the block)
             uint32_t at[4][4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                ldsm_x4_trans(at[c], slot + (uint32_t)swz(16 * mt + (lane & 7) + 8 * (lane >> 4),
-                                                         2 * c + ((lane >> 3) & 1)) * 2u);
+            for (int c = 0; c < 4; ++c) {
+                at[c][0] = movmatrix_trans(af[c][0]);
+                at[c][1] = movmatrix_trans(af[c][2]);
+                at[c][2] = movmatrix_trans(af[c][1]);
+                at[c][3] = movmatrix_trans(af[c][3]);
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (!half[h]) continue;
@@ -805,7 +814,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             }
         }
         __syncwarp();
-        const float gown = valid ? gs[lane * kGs + kr] : 0.f;
+        const float gown = valid ? gs[lane * kGs + (kr ^ gs_swz(lane))] : 0.f;
         const float coef = valid ? __fmaf_rn(gown, inv_s, ngbs) * s2 : 0.f;
         float x[4];
 #pragma unroll
@@ -879,33 +888,31 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     // or after its last key (within the chunk): no mask needed there
     const int warp_key_last = j0 + warp * 16 + 15;
     const bool warp_keys_full = warp_key_last < jend;
+    // A of S^T: this warp's 16 key rows of V, loaded once the tiles are staged
+    uint32_t va[4][4];
     auto qtile = [&](int t, int iq0, auto masked) {
-        const uint32_t vbase = smem_u32(own.v);
         const uint32_t dbase = smem_u32(own.dO[t & 1]);
-        // S^T = V . dO^T : 16 keys x 64 queries per warp
-        float s[8][4];
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t a[4];
-            ldsm_x4(a, vbase + (uint32_t)swz(warp * 16 + (m & 1) * 8 + rr, ks * 2 + (m >> 1)) * 2u);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                const int qrow = np * 16 + (m >> 1) * 8 + rr;
-                uint32_t b[4];
-                ldsm_x4(b, dbase + (uint32_t)swz(qrow, ks * 2 + (m & 1)) * 2u);
-                mma16816(s[2 * np], a, b[0], b[1]);
-                mma16816(s[2 * np + 1], a, b[2], b[3]);
-            }
-        }
-        // element-wise terms for key rows (a, b) packed; P^T into A fragments,
-        // then dV += P^T . dO
         const QRec *qt_rec = own.qr[t & 1];
+        // per 16 queries: S^T = V . dO^T (16 keys x 16 queries), the element-wise
+        // terms for key rows (a, b) packed, P^T into A fragments, then
+        // dV += P^T . dO with the same dO fragments transposed in registers
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
+            uint32_t bq[4][4];     // queries 16 kk + (0-7 | 8-15) x dims 16 ks + (0-7 | 8-15)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                ldsm_x4(bq[ks], dbase + (uint32_t)swz(kk * 16 + (m >> 1) * 8 + rr,
+                                                     ks * 2 + (m & 1)) * 2u);
+            float s[2][4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[hh][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                mma16816(s[0], va[ks], bq[ks][0], bq[ks][1]);
+                mma16816(s[1], va[ks], bq[ks][2], bq[ks][3]);
+            }
             float pa_[8];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -931,7 +938,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                         w.y = (i >= first_b && i < cend) ? w.y : 0.f;
                     }
                     const float2 aw = mul2(w, inv_s);
-                    const float2 dldw = fma2(make_float2(s[nt][e], s[nt][2 + e]), inv_s, ngbs);
+                    const float2 dldw = fma2(make_float2(s[hh][e], s[hh][2 + e]), inv_s, ngbs);
                     float2 ndw;                    // 2 (-dw/d(d^2))
                     if constexpr (WK == kWSoftmax) ndw = mul2(w, two_ig2);
                     else if constexpr (WK == kWInvEuclid) ndw = mul2(mul2(w, w), w);
@@ -949,12 +956,10 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             pa[2] = pack_bf16(pa_[4], pa_[5]);     // key row g,   queries +8
             pa[3] = pack_bf16(pa_[6], pa_[7]);     // key row g+8, queries +8
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                const int qrow = kk * 16 + (m & 1) * 8 + rr;
-                uint32_t b[4];
-                ldsm_x4_trans(b, dbase + (uint32_t)swz(qrow, np * 2 + (m >> 1)) * 2u);
-                mma16816(dva[2 * np], pa, b[0], b[1]);
-                mma16816(dva[2 * np + 1], pa, b[2], b[3]);
+            for (int np = 0; np < 4; ++np) {       // dims 16 np + (0-7 | 8-15)
+                mma16816(dva[2 * np], pa, movmatrix_trans(bq[np][0]), movmatrix_trans(bq[np][2]));
+                mma16816(dva[2 * np + 1], pa, movmatrix_trans(bq[np][1]),
+                         movmatrix_trans(bq[np][3]));
             }
         }
     };
@@ -964,6 +969,13 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
+        if (t == 0) {
+            const uint32_t vbase = smem_u32(own.v);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                ldsm_x4(va[ks], vbase + (uint32_t)swz(warp * 16 + (m & 1) * 8 + rr,
+                                                     ks * 2 + (m >> 1)) * 2u);
+        }
         if (warp_keys_full && iq0 >= warp_key_last && iq0 + T64 <= cend)
             qtile(t, iq0, std::false_type{});
         else
