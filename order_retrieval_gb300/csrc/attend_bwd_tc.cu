@@ -102,13 +102,24 @@ __device__ __forceinline__ void stage_rows(__nv_bfloat16 *tile, const __nv_bfloa
 
 // ============================================================ query side ===
 
-struct __align__(16) QSmem {
+// Tiles of the own-chunk part.
+struct __align__(16) QOwn {
     __nv_bfloat16 dO[T64 * DV];
     __nv_bfloat16 v[2][T64 * DV];
     float4 kt[2][T64];
-    float part[T64][12];
-    float mpart[T64];             // softmax: the window part's shift per query
 };
+// Dynamic shared memory of the query side: the window walk's rings (four warps
+// x two slots of q_ring_rows(k) value rows), which become the own-chunk tiles
+// once every warp's walk is done, then the window part's sums per query and
+// (softmax) its shift per query.
+__host__ __device__ inline int q_ring_rows(int k) { return k >= 64 ? 64 : (k + 15) & ~15; }
+__host__ __device__ inline size_t q_big_bytes(int k) {
+    const size_t ring = (size_t)(THREADS / 32) * 2 * q_ring_rows(k) * DV * 2;
+    return ring > sizeof(QOwn) ? ring : sizeof(QOwn);
+}
+__host__ __device__ inline size_t q_smem_bytes(int k) {
+    return q_big_bytes(k) + sizeof(float) * T64 * 12 + sizeof(float) * T64;
+}
 
 // Accumulators of one query row: x[0] = sum w, x[1] = sum w g, x[2] = sum g e,
 // x[3] = sum e, x[4..7] = sum g c (q-k), x[8..11] = sum c (q-k).
@@ -227,7 +238,10 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
              const int32_t *__restrict__ idx, const __nv_bfloat16 *__restrict__ dout,
              float *__restrict__ dq, QRec *__restrict__ rec, float *__restrict__ dg_part,
              int32_t *status, int N, int H, int k, int C, int tiles_per_chunk) {
-    __shared__ QSmem sm;
+    extern __shared__ __align__(16) unsigned char qsm[];
+    QOwn &own = *reinterpret_cast<QOwn *>(qsm);
+    float(*qpart)[12] = reinterpret_cast<float(*)[12]>(qsm + q_big_bytes(k));
+    float *qmpart = reinterpret_cast<float *>(qsm + q_big_bytes(k) + sizeof(float) * T64 * 12);
     const int64_t seg = blockIdx.y;
     const int c = blockIdx.x / tiles_per_chunk;
     const int qt = blockIdx.x % tiles_per_chunk;
@@ -245,148 +259,191 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
     const int nkt = (iend - 1 - cC) / T64 + 1;
 
     auto load_ktile = [&](int b, int key0) {
-        stage_rows(sm.v[b], vb, key0, cend);
+        stage_rows(own.v[b], vb, key0, cend);
         if (threadIdx.x < T64) {
             const int key = key0 + threadIdx.x;
-            sm.kt[b][threadIdx.x] =
+            own.kt[b][threadIdx.x] =
                 key < cend ? load_k4(kb + (int64_t)key * DK, DK) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
-    stage_rows(sm.dO, db, i0, iend);
-    load_ktile(0, cC);
-    cp_async_commit();
-
     // ---------------------------------------------------- window part ---
-    // A pass covers up to 64 selected keys.  Lane L owns slots L and L+32 (index,
-    // coordinates, the pair's weight terms).  The dot products g_ij = dO_i . v_j
-    // run on the tensor cores: for 16 selected keys, G = V_J . dO_i is one
-    // m16n8k16 mma per 16 dimensions, A the gathered value rows and dO_i in
-    // column 0 of B.  A dot product does not depend on the order of the
-    // dimensions, so each lane's two 16-byte slices of a row (slices 2t, 2t+1
-    // for t = lane % 4) serve as its A fragments directly, with dO_i's slices
-    // of the same numbers in B: no unpacking, no shuffle reductions.  The
-    // owner picks g up from the lane holding column 0.  The next query's
-    // indices are fetched while this one runs.
+    // A unit is one pass of a query over up to 64 selected keys; lane L owns
+    // slots L and L+32 (index, coordinates, the pair's weight terms).  Each
+    // unit's value rows are copied into a two-slot ring of swizzled 128-byte
+    // rows in shared memory (cp.async) one unit ahead, its indices two units
+    // ahead, its key coordinates and dO_i one unit ahead in registers.  The dot
+    // products g_ij = dO_i . v_j run on the tensor cores: for 16 selected keys,
+    // G = V_J . dO_i is one m16n8k16 mma per 16 dimensions, A the staged rows
+    // (ldmatrix) and dO_i in column 0 of B; the owner picks g up from the lane
+    // holding column 0.
     const int g4 = lane >> 2, s4 = lane & 3;
     const int wq0 = i0 + warp * 16;
     const int nqw = c > 0 ? max(0, min(16, iend - wq0)) : 0;
-    auto load_idx = [&](int i, int t0, int (&j)[2]) {
-        const int32_t *irow = idx + (seg * N + i) * (int64_t)k + t0;
+    const int npass = (k + 63) >> 6;
+    const int nunit = nqw * npass;
+    const int rr_ring = q_ring_rows(k);
+    const uint32_t slot_bytes = (uint32_t)rr_ring * 128u;
+    const uint32_t ring = smem_u32(qsm) + (uint32_t)warp * 2u * slot_bytes;
+    auto unit_idx = [&](int u, int (&j)[2]) {            // raw indices of unit u
+        j[0] = j[1] = -1;
+        if (u < nunit) {
+            const int r = u / npass, t0 = (u - r * npass) * 64;
+            const int32_t *irow = idx + (seg * N + wq0 + r) * (int64_t)k + t0;
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            const int t = t0 + s * 32 + lane;
-            j[s] = t < k ? __ldg(irow + s * 32 + lane) : -1;
+            for (int s = 0; s < 2; ++s)
+                if (t0 + s * 32 + lane < k) j[s] = __ldg(irow + s * 32 + lane);
         }
     };
-    int jn[2] = {-1, -1};
-    if (nqw > 0) load_idx(wq0, 0, jn);
-    const float k2 = 2.f * inv_g2 * inv_g;
-    for (int r = 0; r < 16; ++r) {
-        const int row = warp * 16 + r;
-        QAcc acc;
-        acc.zero();
-        float mrun = INFINITY;                     // softmax shift of this query
-        if (r < nqw) {
-            const int i = wq0 + r;
-            float qi[4];
+    auto validate = [&](int (&j)[2]) {                   // keys outside the prefix -> -1
 #pragma unroll
-            for (int d = 0; d < 4; ++d) qi[d] = d < DK ? qb[(int64_t)i * DK + d] : 0.f;
-            uint4 doa = make_uint4(0u, 0u, 0u, 0u), dob = doa;   // B column 0: lanes 0..3
-            if (g4 == 0) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(db + (int64_t)i * DV + s4 * 16);
-                doa = src[0];
-                dob = src[1];
+        for (int s = 0; s < 2; ++s)
+            if (j[s] != -1 && (unsigned)j[s] >= (unsigned)cC) {
+                set_status(status, ZETA_ERR_BOUNDS);
+                j[s] = -1;
             }
-            for (int t0 = 0; t0 < k; t0 += 64) {
-                int j[2] = {jn[0], jn[1]};
-                if (t0 + 64 < k) load_idx(i, t0 + 64, jn);
-                else if (r + 1 < nqw) load_idx(i + 1, 0, jn);
-                float4 kk[2];
+    };
+    auto issue = [&](int u, const int (&j)[2]) {         // value rows of unit u
+        const int t0 = (u % npass) * 64;
+        const int nrows = min(rr_ring, (min(64, k - t0) + 15) & ~15);
+        const uint32_t slot = ring + (uint32_t)(u & 1) * slot_bytes;
+        for (int h = 0; 4 * h < nrows; ++h) {
+            const int row = 4 * h + (lane >> 3), ch = lane & 7;
+            const int jr = __shfl_sync(kFull, row < 32 ? j[0] : j[1], row & 31);
+            const bool ok = jr >= 0;
+            cp_async16(slot + (uint32_t)swz(row, ch) * 2u, vb + (int64_t)(ok ? jr : 0) * DV + ch * 8,
+                       ok ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    auto unit_keys = [&](const int (&j)[2], float4 (&kk)[2]) {
 #pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    if (j[s] != -1 && (unsigned)j[s] >= (unsigned)cC) {
-                        set_status(status, ZETA_ERR_BOUNDS);
-                        j[s] = -1;
-                    }
-                    kk[s] = j[s] >= 0 ? load_k4(kb + (int64_t)j[s] * DK, DK)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < 2; ++s)
+            kk[s] = j[s] >= 0 ? load_k4(kb + (int64_t)j[s] * DK, DK) : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto unit_dout = [&](int u) -> uint32_t {            // word `lane` of dO_i of unit u
+        if (u >= nunit) return 0u;
+        const int i = wq0 + u / npass;
+        return reinterpret_cast<const uint32_t *>(db + (int64_t)i * DV)[lane];
+    };
+    const float k2 = 2.f * inv_g2 * inv_g;
+    // rows without a window part
+    for (int r = nqw; r < 16; ++r) {
+        if (lane < 12) qpart[warp * 16 + r][lane] = 0.f;
+        if (lane == 0) qmpart[warp * 16 + r] = INFINITY;
+    }
+    int jc[2], jn[2], jn2[2];
+    unit_idx(0, jc);
+    validate(jc);
+    if (nunit > 0) issue(0, jc);
+    float4 kc[2], kn[2];
+    unit_keys(jc, kc);
+    uint32_t dwc = unit_dout(0), dwn = 0u;
+    auto unit_q = [&](int u, float (&x)[4]) {           // q_i of unit u
+#pragma unroll
+        for (int d = 0; d < 4; ++d)
+            x[d] = (u < nunit && d < DK) ? qb[(int64_t)(wq0 + u / npass) * DK + d] : 0.f;
+    };
+    float qi[4], qn[4];
+    unit_q(0, qi);
+    unit_idx(1, jn);
+    QAcc acc;
+    acc.zero();
+    float mrun = INFINITY;                       // softmax shift of this query
+    for (int u = 0; u < nunit; ++u) {
+        const int r = u / npass, t0 = (u - r * npass) * 64;
+        unit_idx(u + 2, jn2);
+        if (u + 1 < nunit) {
+            validate(jn);
+            issue(u + 1, jn);
+            unit_keys(jn, kn);
+            dwn = unit_dout(u + 1);
+            unit_q(u + 1, qn);
+        }
+        // dO_i in column 0 of B: lanes 0..3 take words 8 ks + t and 8 ks + t + 4
+        uint32_t bd[4][2];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t x0 = __shfl_sync(kFull, dwc, 8 * ks + s4);
+            const uint32_t x1 = __shfl_sync(kFull, dwc, 8 * ks + s4 + 4);
+            bd[ks][0] = g4 == 0 ? x0 : 0u;
+            bd[ks][1] = g4 == 0 ? x1 : 0u;
+        }
+        if (u + 1 < nunit) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        __syncwarp();
+        const uint32_t slot = ring + (uint32_t)(u & 1) * slot_bytes;
+        const int nmt = min(4, (k - t0 + 15) >> 4);      // 16-key tiles in this pass
+        float cg[4][4];
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cg[mt][e] = 0.f;
+            if (mt < nmt) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    uint32_t af[4];
+                    ldsm_x4(af, slot + (uint32_t)swz(16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1),
+                                                     2 * ks + (lane >> 4)) * 2u);
+                    mma16816(cg[mt], af, bd[ks][0], bd[ks][1]);
                 }
-                const int nmt = min(4, (k - t0 + 15) >> 4);  // 16-key tiles in this pass
-                uint4 buf[4][4];                    // rows g, g+8 of tile mt: slices 2t, 2t+1
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int slot = 16 * mt + 8 * h + g4;
-                        const int jr = __shfl_sync(kFull, j[mt >> 1], slot & 31);
-                        const bool ok = mt < nmt && jr >= 0;
-                        const uint4 *src =
-                            reinterpret_cast<const uint4 *>(vb + (int64_t)jr * DV + s4 * 16);
-                        buf[mt][2 * h] = ok ? ld_stream16(src) : make_uint4(0u, 0u, 0u, 0u);
-                        buf[mt][2 * h + 1] = ok ? ld_stream16(src + 1) : make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-                float cg[4][4];
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) cg[mt][e] = 0.f;
-                    if (mt < nmt) {
-                        const uint32_t ra0[4] = {buf[mt][0].x, buf[mt][0].y, buf[mt][0].z, buf[mt][0].w};
-                        const uint32_t ra1[4] = {buf[mt][1].x, buf[mt][1].y, buf[mt][1].z, buf[mt][1].w};
-                        const uint32_t rb0[4] = {buf[mt][2].x, buf[mt][2].y, buf[mt][2].z, buf[mt][2].w};
-                        const uint32_t rb1[4] = {buf[mt][3].x, buf[mt][3].y, buf[mt][3].z, buf[mt][3].w};
-                        const uint32_t d0[4] = {doa.x, doa.y, doa.z, doa.w};
-                        const uint32_t d1[4] = {dob.x, dob.y, dob.z, dob.w};
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint32_t af[4] = {ra0[ks], rb0[ks], ra1[ks], rb1[ks]};
-                            mma16816(cg[mt], af, d0[ks], d1[ks]);
-                        }
-                    }
-                }
-                // slot L: tile L >> 4, row half (L >> 3) & 1, row L & 7 -> lane 4 (L & 7)
-                float gown[2] = {0.f, 0.f};
-                const int srcl = (lane & 7) * 4;
-                const bool hi = (lane >> 3) & 1, up = lane >> 4;
-#pragma unroll
-                for (int sl = 0; sl < 2; ++sl) {
-                    if (2 * sl < nmt) {
-                        const float x0 = __shfl_sync(kFull, cg[2 * sl][0], srcl);
-                        const float x1 = __shfl_sync(kFull, cg[2 * sl][2], srcl);
-                        const float x2 = __shfl_sync(kFull, cg[2 * sl + 1][0], srcl);
-                        const float x3 = __shfl_sync(kFull, cg[2 * sl + 1][2], srcl);
-                        gown[sl] = up ? (hi ? x3 : x2) : (hi ? x1 : x0);
-                    }
-                }
-                float d2v[2];
-#pragma unroll
-                for (int s = 0; s < 2; ++s) d2v[s] = j[s] >= 0 ? dist2k<DK>(qi, kk[s]) : INFINITY;
-                if constexpr (WK == kWSoftmax) {
-                    float pm = fminf(d2v[0], d2v[1]);
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) pm = fminf(pm, __shfl_xor_sync(kFull, pm, o));
-                    const float mn = fminf(mrun, pm);
-                    if (mn != mrun) {                    // uniform across the warp
-                        if (mrun != INFINITY) acc.rebase(mn - mrun, shift_scale(mn, mrun, inv_g2), k2);
-                        mrun = mn;
-                    }
-                }
-#pragma unroll
-                for (int s = 0; s < 2; ++s)
-                    if (j[s] >= 0)
-                        acc.add<WK>(weight_fast<WK>(d2v[s], mrun, inv_g2), d2v[s], mrun, gown[s],
-                                    qi, kk[s], inv_g2, inv_g);
             }
         }
-        float tv[16];
+        __syncwarp();                            // slot reads done before it is refilled
+        // slot L: tile L >> 4, row half (L >> 3) & 1, row L & 7 -> lane 4 (L & 7)
+        float gown[2] = {0.f, 0.f};
+        const int srcl = (lane & 7) * 4;
+        const bool hi = (lane >> 3) & 1, up = lane >> 4;
 #pragma unroll
-        for (int y = 0; y < 16; ++y) tv[y] = y < 12 ? acc.x[y] : 0.f;
-        const float tot = warp_transpose_sum16(tv, lane);      // value (lane >> 1)
-        if (!(lane & 1) && (lane >> 1) < 12) sm.part[row][lane >> 1] = tot;
-        if (lane == 0) sm.mpart[row] = mrun;
+        for (int sl = 0; sl < 2; ++sl) {
+            if (2 * sl < nmt) {
+                const float x0 = __shfl_sync(kFull, cg[2 * sl][0], srcl);
+                const float x1 = __shfl_sync(kFull, cg[2 * sl][2], srcl);
+                const float x2 = __shfl_sync(kFull, cg[2 * sl + 1][0], srcl);
+                const float x3 = __shfl_sync(kFull, cg[2 * sl + 1][2], srcl);
+                gown[sl] = up ? (hi ? x3 : x2) : (hi ? x1 : x0);
+            }
+        }
+        float d2v[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) d2v[s] = jc[s] >= 0 ? dist2k<DK>(qi, kc[s]) : INFINITY;
+        if constexpr (WK == kWSoftmax) {
+            float pm = fminf(d2v[0], d2v[1]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) pm = fminf(pm, __shfl_xor_sync(kFull, pm, o));
+            const float mn = fminf(mrun, pm);
+            if (mn != mrun) {                    // uniform across the warp
+                if (mrun != INFINITY) acc.rebase(mn - mrun, shift_scale(mn, mrun, inv_g2), k2);
+                mrun = mn;
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+            if (jc[s] >= 0)
+                acc.add<WK>(weight_fast<WK>(d2v[s], mrun, inv_g2), d2v[s], mrun, gown[s], qi, kc[s],
+                            inv_g2, inv_g);
+        if (t0 + 64 >= k) {                      // the query's last pass: its window sums
+            float tv[16];
+#pragma unroll
+            for (int y = 0; y < 16; ++y) tv[y] = y < 12 ? acc.x[y] : 0.f;
+            const float tot = warp_transpose_sum16(tv, lane);      // value (lane >> 1)
+            const int row = warp * 16 + r;
+            if (!(lane & 1) && (lane >> 1) < 12) qpart[row][lane >> 1] = tot;
+            if (lane == 0) qmpart[row] = mrun;
+            acc.zero();
+            mrun = INFINITY;
+        }
+        jc[0] = jn[0]; jc[1] = jn[1];
+        jn[0] = jn2[0]; jn[1] = jn2[1];
+        kc[0] = kn[0]; kc[1] = kn[1];
+        dwc = dwn;
+#pragma unroll
+        for (int d = 0; d < 4; ++d) qi[d] = qn[d];
     }
-    __syncwarp();
+    // every warp's walk is done before the rings become the own-chunk tiles
+    __syncthreads();
+    stage_rows(own.dO, db, i0, iend);
+    load_ktile(0, cC);
+    cp_async_commit();
 
     // ------------------------------------------------- own-chunk part ---
     const int g8 = lane >> 2, tig = lane & 3;
@@ -410,7 +467,7 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
     lab.zero();
     uint32_t afr[4][4];
     const int rowa_l = warp * 16 + g8;
-    float2 mab = make_float2(sm.mpart[rowa_l], sm.mpart[rowa_l + 8]);   // softmax shifts
+    float2 mab = make_float2(qmpart[rowa_l], qmpart[rowa_l + 8]);   // softmax shifts
     auto tile = [&](const float4 *Ks, uint32_t vbase, int key0, auto masked) {
         if constexpr (WK == kWSoftmax) {           // move the shift to this tile's minimum
             // (keys read through a volatile view: distances recomputed below are
@@ -495,7 +552,7 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
         cp_async_wait<1>();
         __syncthreads();
         if (kt == 0) {
-            const uint32_t dbase = smem_u32(sm.dO);
+            const uint32_t dbase = smem_u32(own.dO);
             const int m = lane >> 3, rr = lane & 7;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
@@ -505,8 +562,8 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
         }
         const int key0 = cC + kt * T64;
         if (key0 <= warp_last) {
-            const float4 *Ks = sm.kt[kt & 1];
-            const uint32_t vbase = smem_u32(sm.v[kt & 1]);
+            const float4 *Ks = own.kt[kt & 1];
+            const uint32_t vbase = smem_u32(own.v[kt & 1]);
             if (warp_rows_full && key0 + T64 - 1 <= warp_first)
                 tile(Ks, vbase, key0, std::false_type{});
             else
@@ -535,10 +592,10 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
         if (i < iend) {
             QAcc wpart;                            // the window part, on the final shift
 #pragma unroll
-            for (int y = 0; y < 12; ++y) wpart.x[y] = sm.part[rloc][y];
+            for (int y = 0; y < 12; ++y) wpart.x[y] = qpart[rloc][y];
             const float mfin = tig == 0 ? mab.x : mab.y;
             if constexpr (WK == kWSoftmax) {
-                const float mw = sm.mpart[rloc];
+                const float mw = qmpart[rloc];
                 if (mw != INFINITY) wpart.rebase(mfin - mw, shift_scale(mfin, mw, inv_g2), k2);
             }
             float t[12];
@@ -1031,22 +1088,40 @@ bool attend_bwd_tc_supported(const Prob &p) {
 
 size_t bwd_tc_rec_bytes(const Prob &p) { return sizeof(QRec) * (size_t)(p.S * p.N); }
 
+template <int D, int WK>
+cudaError_t bwd_query_tc_launch(const Prob &p, dim3 grid, int tpc, const float *q, const float *k,
+                                const void *v, const float *gamma, const int32_t *idx,
+                                const void *dout, float *dq, void *rec, float *dg_part,
+                                int32_t *status, cudaStream_t st) {
+    static PerDeviceOnce smem_once;          // run once per device, outside any capture
+    const cudaError_t e = smem_once.run([] {  // the largest ring (k >= 64)
+        return cudaFuncSetAttribute(bwd_query_tc<D, WK>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)q_smem_bytes(64));
+    });
+    if (e != cudaSuccess) return e;
+    bwd_query_tc<D, WK><<<grid, THREADS, q_smem_bytes(p.k), st>>>(
+        q, k, static_cast<const __nv_bfloat16 *>(v), gamma, idx,
+        static_cast<const __nv_bfloat16 *>(dout), dq, static_cast<QRec *>(rec), dg_part, status,
+        p.N, p.H, p.k, p.C, tpc);
+    return cudaGetLastError();
+}
+
 template <int WK>
-void bwd_query_tc_dk(const Prob &p, dim3 grid, int tpc, const float *q, const float *k,
-                     const void *v, const float *gamma, const int32_t *idx, const void *dout,
-                     float *dq, void *rec, float *dg_part, int32_t *status, cudaStream_t st) {
-#define ZETA_BQ(D)                                                                              \
-    bwd_query_tc<D, WK><<<grid, THREADS, 0, st>>>(                                             \
-        q, k, static_cast<const __nv_bfloat16 *>(v), gamma, idx,                              \
-        static_cast<const __nv_bfloat16 *>(dout), dq, static_cast<QRec *>(rec), dg_part, status, \
-        p.N, p.H, p.k, p.C, tpc)
+cudaError_t bwd_query_tc_dk(const Prob &p, dim3 grid, int tpc, const float *q, const float *k,
+                            const void *v, const float *gamma, const int32_t *idx,
+                            const void *dout, float *dq, void *rec, float *dg_part,
+                            int32_t *status, cudaStream_t st) {
     switch (p.dK) {
-        case 1: ZETA_BQ(1); break;
-        case 2: ZETA_BQ(2); break;
-        case 3: ZETA_BQ(3); break;
-        default: ZETA_BQ(4); break;
+        case 1: return bwd_query_tc_launch<1, WK>(p, grid, tpc, q, k, v, gamma, idx, dout, dq,
+                                                  rec, dg_part, status, st);
+        case 2: return bwd_query_tc_launch<2, WK>(p, grid, tpc, q, k, v, gamma, idx, dout, dq,
+                                                  rec, dg_part, status, st);
+        case 3: return bwd_query_tc_launch<3, WK>(p, grid, tpc, q, k, v, gamma, idx, dout, dq,
+                                                  rec, dg_part, status, st);
+        default: return bwd_query_tc_launch<4, WK>(p, grid, tpc, q, k, v, gamma, idx, dout, dq,
+                                                   rec, dg_part, status, st);
     }
-#undef ZETA_BQ
 }
 
 template <int D, int WK>
@@ -1091,15 +1166,13 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
     const int tpc = (p.C + T64 - 1) / T64;
     const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
     if (p.wk == kWSoftmax)
-        bwd_query_tc_dk<kWSoftmax>(p, grid, tpc, q, k, v, gamma, idx, dout, dq, rec, dg_part,
-                                   status, st);
-    else if (p.wk == kWInvEuclid)
-        bwd_query_tc_dk<kWInvEuclid>(p, grid, tpc, q, k, v, gamma, idx, dout, dq, rec, dg_part,
+        return bwd_query_tc_dk<kWSoftmax>(p, grid, tpc, q, k, v, gamma, idx, dout, dq, rec,
+                                          dg_part, status, st);
+    if (p.wk == kWInvEuclid)
+        return bwd_query_tc_dk<kWInvEuclid>(p, grid, tpc, q, k, v, gamma, idx, dout, dq, rec,
+                                            dg_part, status, st);
+    return bwd_query_tc_dk<kWCauchy>(p, grid, tpc, q, k, v, gamma, idx, dout, dq, rec, dg_part,
                                      status, st);
-    else
-        bwd_query_tc_dk<kWCauchy>(p, grid, tpc, q, k, v, gamma, idx, dout, dq, rec, dg_part,
-                                  status, st);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
