@@ -11,8 +11,9 @@
 //  * One CTA = 64 consecutive queries of one chunk (4 warps x 16 rows).
 //  * Window part (a gather): a warp takes one query at a time; each lane owns
 //    two selected keys (index, coordinates, Cauchy weight); the gathered
-//    128-byte bf16 value rows come in with 16-byte loads, all 16 loads of a
-//    lane's 64-key pass in flight together, and the weighted sum V^T w runs
+//    128-byte bf16 value rows come in with 32-byte loads (four lanes per row),
+//    all 8 loads of a lane's 64-key pass in flight together, and the weighted
+//    sum V^T w runs
 //    on the tensor cores (rows transposed in registers by movmatrix, w in
 //    column 0 of B); the next query's indices are fetched while the current
 //    query is processed.  Partial sums (sum w v, sum w) go to shared memory in
@@ -144,7 +145,8 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     // runs on the tensor cores: for 16 selected keys, sum_j w_j v_j = V^T w is
     // four m16n8k16 mma (16 dimensions each) with w (bf16, like the own-chunk
     // P) in column 0 of B.  Lane (g, t) loads 16-byte slices 2t, 2t+1 of rows
-    // g and g+8 of the 16; movmatrix transposes them 8x8 block by block into
+    // g and g+8 of the 16 (one 32-byte access per row: each sector of a row is
+    // requested once); movmatrix transposes them 8x8 block by block into
     // A fragments, and the sums stay in the mma's column-0 registers.
     const int wq0 = i0 + warp * 16;
     const int nqw = c > 0 ? max(0, min(16, iend - wq0)) : 0;
@@ -231,10 +233,8 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
                         const int slot = 16 * mt + 8 * h + g4;
                         const int jr = __shfl_sync(kFull, j[mt >> 1], slot & 31);
                         const bool ok = mt < nmt && jr >= 0;
-                        const uint4 *src =
-                            reinterpret_cast<const uint4 *>(vb + (int64_t)jr * DV + s4 * 16);
-                        buf[mt][2 * h] = ok ? ld_stream16(src) : make_uint4(0u, 0u, 0u, 0u);
-                        buf[mt][2 * h + 1] = ok ? ld_stream16(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+                        ld_stream32(vb + (int64_t)(ok ? jr : 0) * DV + s4 * 16, ok, buf[mt][2 * h],
+                                    buf[mt][2 * h + 1]);
                     }
                 }
                 float d2v[2];

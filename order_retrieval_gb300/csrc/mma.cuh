@@ -1,6 +1,6 @@
 // mma.cuh -- inline-PTX helpers shared by the tensor-core kernels:
 // cp.async staging, ldmatrix, mma.sync m16n8k16 (bf16 in, f32 accumulate),
-// streaming 16-byte loads and bf16 packing.
+// streaming 32-byte loads and bf16 packing.
 #pragma once
 
 #include "common.cuh"
@@ -55,14 +55,17 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
     return d;
 }
 
-// 16-byte load through the non-coherent path without L1 allocation: gathered
-// rows are used once by the loading warp.
-__device__ __forceinline__ uint4 ld_stream16(const void *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
+// 32-byte load through the non-coherent path without L1 allocation (gathered
+// rows are used once by the loading warp): two adjacent 16-byte slices at a
+// 32-byte aligned address in one 256-bit access; zeros where `ok` is false.
+__device__ __forceinline__ void ld_stream32(const void *p, bool ok, uint4 &a, uint4 &b) {
+    a = make_uint4(0u, 0u, 0u, 0u);
+    b = a;
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.b32 q, %9, 0;\n"
+        " @q ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n}\n"
+        : "+r"(a.x), "+r"(a.y), "+r"(a.z), "+r"(a.w), "+r"(b.x), "+r"(b.y), "+r"(b.z), "+r"(b.w)
+        : "l"(p), "r"((int)ok));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
