@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 # DRAM bytes (read + write) of one attend_fwd_tc launch on the efficiency
 # workload, from the ncu capture summarised in
 # profiles/attend_kernels_train_bf16_b2_n65536.md; None once that kernel changes.
-ATTEND_FWD_DRAM_BYTES = 623_472_128
+ATTEND_FWD_DRAM_BYTES = 263_295_232
 
 METRIC = "ZETA attention tokens/s (fwd, fwd+bwd) at N=65536 and % of GB300 HBM roofline"
 L2_FLUSH_BYTES = 256 << 20
