@@ -346,7 +346,10 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
     float qi[4], qn[4];
     unit_q(0, qi);
     unit_idx(1, jn);
-    QAcc acc;
+    // the lane's two slots packed (x: slot L, y: slot L+32)
+    const float2 ig2w = dup2(inv_g2), m2ig2w = dup2(-2.f * inv_g2), two_igw = dup2(2.f * inv_g);
+    const float2 k2w = dup2(k2);
+    QAcc2 acc;
     acc.zero();
     float mrun = INFINITY;                       // softmax shift of this query
     for (int u = 0; u < nunit; ++u) {
@@ -412,19 +415,32 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
             for (int o = 16; o > 0; o >>= 1) pm = fminf(pm, __shfl_xor_sync(kFull, pm, o));
             const float mn = fminf(mrun, pm);
             if (mn != mrun) {                    // uniform across the warp
-                if (mrun != INFINITY) acc.rebase(mn - mrun, shift_scale(mn, mrun, inv_g2), k2);
+                if (mrun != INFINITY)
+                    acc.rebase(dup2(mn - mrun), dup2(shift_scale(mn, mrun, inv_g2)), k2w);
                 mrun = mn;
             }
         }
+        {
+            // empty slots: weight 0 and d2 = m, so that they add nothing (the shift
+            // is still infinite only while every slot so far was empty)
+            const bool v0 = jc[0] >= 0, v1 = jc[1] >= 0;
+            const float mf = mrun == INFINITY ? 0.f : mrun;
+            const float2 d2p = make_float2(v0 ? d2v[0] : mf, v1 ? d2v[1] : mf);
+            const float2 mp = dup2(mf);
+            float2 w = weight_fast2<WK>(d2p, mp, ig2w);
+            w.x = v0 ? w.x : 0.f;
+            w.y = v1 ? w.y : 0.f;
+            const float kc0[4] = {kc[0].x, kc[0].y, kc[0].z, kc[0].w};
+            const float kc1[4] = {kc[1].x, kc[1].y, kc[1].z, kc[1].w};
+            float2 dqp[4];
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
-            if (jc[s] >= 0)
-                acc.add<WK>(weight_fast<WK>(d2v[s], mrun, inv_g2), d2v[s], mrun, gown[s], qi, kc[s],
-                            inv_g2, inv_g);
+            for (int d = 0; d < 4; ++d) dqp[d] = make_float2(qi[d] - kc0[d], qi[d] - kc1[d]);
+            acc.add<DK, WK>(w, d2p, mp, make_float2(gown[0], gown[1]), dqp, m2ig2w, two_igw, k2w);
+        }
         if (t0 + 64 >= k) {                      // the query's last pass: its window sums
             float tv[16];
 #pragma unroll
-            for (int y = 0; y < 16; ++y) tv[y] = y < 12 ? acc.x[y] : 0.f;
+            for (int y = 0; y < 16; ++y) tv[y] = y < 12 ? acc.x[y].x + acc.x[y].y : 0.f;
             const float tot = warp_transpose_sum16(tv, lane);      // value (lane >> 1)
             const int row = warp * 16 + r;
             if (!(lane & 1) && (lane >> 1) < 12) qpart[row][lane >> 1] = tot;
