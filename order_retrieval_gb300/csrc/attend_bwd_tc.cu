@@ -5,11 +5,14 @@
 // held fixed), organised like the fast forward:
 //
 // Query side, one CTA per 64 queries of a chunk:
-//   window part  - eight lanes per gathered value row: g_ij = dO_i . v_j by a
-//                  16-byte slice dot plus a 3-step shuffle, then the Cauchy
-//                  terms of the pair (w, c = -2 w^2 / gamma^2, e = 2 w (1-w) /
-//                  gamma) accumulate sum w, sum w g, sum g e, sum e,
-//                  sum g c (q-k), sum c (q-k).
+//   window part  - a pipeline of units (one query's pass over up to 64 selected
+//                  keys): the unit's value rows are copied into a two-slot
+//                  shared-memory ring by cp.async one unit ahead, g_ij =
+//                  dO_i . v_j runs on the tensor cores (the rows as A fragments,
+//                  dO_i in column 0 of B), and a lane's two slots accumulate the
+//                  pair terms packed: sum w, sum w g, sum g e, sum e,
+//                  sum g c (q-k), sum c (q-k) (Cauchy: the same sums on u = w^2
+//                  with the constants applied at the end).
 //   own chunk    - G = dO . V^T on tensor cores (mma.sync, dO fragments held
 //                  in registers, V tiles cp.async-staged), then the same terms
 //                  per element.
@@ -17,9 +20,11 @@
 //                  32-byte record {q_i, 1/s_i, gbar_i} for the key side.
 // Key side, one CTA per 64 keys of a chunk:
 //   window part  - the queries that selected key j (a transpose of idx sorted
-//                  by query), 32 at a time: one lane per listed query for the
-//                  scalar terms, eight lanes per dO row for the row work:
-//                  dv_j += a_ij dO_i and dk_j += dL/dw_ij 2 w^2/gamma^2 (q_i - k_j).
+//                  by query): a warp walks the lists of its 16 keys as one run,
+//                  32 entries per step, the step's dO rows staged in a ring one
+//                  step ahead; G = dO_rows . V_keys^T and dV_keys += dO^T A on
+//                  the tensor cores, dk_j += dL/dw_ij (-2 dw/d(d^2)) (q_i - k_j)
+//                  summed per key by a segmented scan.
 //   own chunk    - S^T = V . dO^T on tensor cores, the element-wise terms, then
 //                  dV += P^T . dO with P^T re-packed from the accumulator
 //                  fragments (their layout is the A-fragment layout).
