@@ -149,17 +149,37 @@ bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
 
 // off[seg][j] = first position of key j in the sorted (key, query) list; the
 // key of a sorted word is word >> key_shift (0: plain keys, 16: packed words).
+// Four positions per thread and step, read with one 16-byte load where the
+// segment's words are 16-byte aligned.
 __global__ void csr_offsets(const uint32_t *__restrict__ skeys, const uint32_t *__restrict__ seglen,
                             int64_t stride, int N, int key_shift, uint32_t *__restrict__ off) {
     const int64_t seg = blockIdx.y;
     const int64_t L = seglen[seg];
     const uint32_t *K = skeys + seg * stride;
     uint32_t *o = off + seg * (int64_t)(N + 1);
-    for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p <= L;
-         p += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t hiK = p < L ? (int64_t)(K[p] >> key_shift) : (int64_t)N;
-        const int64_t loK = p > 0 ? (int64_t)(K[p - 1] >> key_shift) : -1;
-        for (int64_t j = loK + 1; j <= hiK; ++j) o[j] = (uint32_t)p;
+    const bool vec = (reinterpret_cast<uintptr_t>(K) & 15u) == 0;
+    for (int64_t p0 = 4 * (blockIdx.x * (int64_t)blockDim.x + threadIdx.x); p0 <= L;
+         p0 += 4 * (int64_t)gridDim.x * blockDim.x) {
+        // key[0]: key before p0 (-1 at the start); key[1 + e]: key at p0 + e (N at L)
+        int64_t key[5];
+        key[0] = p0 > 0 ? (int64_t)(K[p0 - 1] >> key_shift) : -1;
+        if (vec && p0 + 4 <= L) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(K + p0);
+            key[1] = (int64_t)(w.x >> key_shift);
+            key[2] = (int64_t)(w.y >> key_shift);
+            key[3] = (int64_t)(w.z >> key_shift);
+            key[4] = (int64_t)(w.w >> key_shift);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                key[1 + e] = p0 + e < L ? (int64_t)(K[p0 + e] >> key_shift) : (int64_t)N;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int64_t p = p0 + e;
+            if (p > L) break;
+            for (int64_t j = key[e] + 1; j <= key[e + 1]; ++j) o[j] = (uint32_t)p;
+        }
     }
 }
 

@@ -45,21 +45,54 @@ struct PairsSrc {          // later passes: ping-pong buffers
     }
 };
 
+// Query and chunk start of window slot p (p = i k + t): i = p / k and
+// cC = C floor(i / C).  Below 2^24 the quotients come from a float reciprocal and
+// one integer correction: p and i are exact in float, the product carries a
+// relative error under 2^-23, so for d >= 2 the truncated estimate is within one
+// of the quotient (for d = 1 the reciprocal and the product are exact); the
+// remainder's sign and size then fix it.  Larger slots fall back to integer
+// division.
+struct SlotDiv {
+    uint32_t k, C;
+    float inv_k, inv_C;
+    bool fast;                // N k <= 2^24
+    static __device__ __forceinline__ uint32_t quot(uint32_t n, uint32_t d, float inv_d) {
+        uint32_t q = __float2uint_rz(__uint2float_rn(n) * inv_d);
+        const int64_t r = (int64_t)n - (int64_t)q * d;
+        if (r < 0) --q;
+        else if (r >= (int64_t)d) ++q;
+        return q;
+    }
+    __device__ __forceinline__ void split(uint32_t p, uint32_t &i, uint32_t &cC) const {
+        if (fast) {
+            i = quot(p, k, inv_k);
+            cC = quot(i, C, inv_C) * C;
+        } else {
+            i = p / k;
+            cC = i - i % C;
+        }
+    }
+};
+inline SlotDiv slot_div(int64_t N, int k, int C) {
+    return SlotDiv{(uint32_t)k, (uint32_t)C, 1.0f / (float)k, 1.0f / (float)C,
+                   N * (int64_t)k <= (int64_t(1) << 24)};
+}
+
 struct IdxSrc {            // window indices: key = selected key, value = query
     static constexpr bool kHasVal = true;
     const int32_t *idx;
     int64_t N;
     int k;
-    int C;
+    SlotDiv dv;
     __device__ int64_t len(int64_t) const { return N * k; }
     __device__ bool load(int64_t seg, int64_t p, uint32_t &key, uint32_t &val, int32_t *st) const {
         const int32_t j = idx[seg * N * k + p];
         if (j == -1) return false;
-        const uint32_t i = static_cast<uint32_t>(p) / static_cast<uint32_t>(k);  // N*k < 2^31
-        const uint32_t cC = i - i % static_cast<uint32_t>(C);
+        uint32_t i, cC;
+        dv.split(static_cast<uint32_t>(p), i, cC);                                 // N*k < 2^31
         if (static_cast<uint32_t>(j) >= cC) { set_status(st, ZETA_ERR_BOUNDS); return false; }
         key = static_cast<uint32_t>(j);
-        val = static_cast<uint32_t>(i);
+        val = i;
         return true;
     }
 };
@@ -72,13 +105,13 @@ struct PackedIdxSrc {
     const int32_t *idx;
     int64_t N;
     int k;
-    int C;
+    SlotDiv dv;
     __device__ int64_t len(int64_t) const { return N * k; }
     __device__ bool load(int64_t seg, int64_t p, uint32_t &key, uint32_t &, int32_t *st) const {
         const int32_t j = idx[seg * N * k + p];
         if (j == -1) return false;
-        const uint32_t i = static_cast<uint32_t>(p) / static_cast<uint32_t>(k);
-        const uint32_t cC = i - i % static_cast<uint32_t>(C);
+        uint32_t i, cC;
+        dv.split(static_cast<uint32_t>(p), i, cC);
         if (static_cast<uint32_t>(j) >= cC) { set_status(st, ZETA_ERR_BOUNDS); return false; }
         key = (static_cast<uint32_t>(j) << 16) | i;
         return true;
@@ -335,7 +368,7 @@ cudaError_t radix_sort_idx(const int32_t *idx, int64_t S, int64_t N, int k, int 
         const int nxt = cur == 0 ? 1 : 0;
         cudaError_t e;
         if (ps == 0)
-            e = run_pass<uint32_t>(IdxSrc{idx, N, k, C}, 0, S, L, ws, nxt, L, ws.seglen, status, st);
+            e = run_pass<uint32_t>(IdxSrc{idx, N, k, slot_div(N, k, C)}, 0, S, L, ws, nxt, L, ws.seglen, status, st);
         else
             e = run_pass<uint32_t>(
                 PairsSrc<uint32_t>{static_cast<const uint32_t *>(ws.keys[cur]), ws.vals[cur], L,
@@ -351,7 +384,7 @@ cudaError_t radix_sort_idx(const int32_t *idx, int64_t S, int64_t N, int k, int 
 cudaError_t radix_sort_idx_packed(const int32_t *idx, int64_t S, int64_t N, int k, int C,
                                   RadixWs &ws, int *out_buf, int32_t *status, cudaStream_t st) {
     const int64_t L = N * (int64_t)k;
-    cudaError_t e = run_pass<uint32_t>(PackedIdxSrc{idx, N, k, C}, 16, S, L, ws, 0, L, ws.seglen,
+    cudaError_t e = run_pass<uint32_t>(PackedIdxSrc{idx, N, k, slot_div(N, k, C)}, 16, S, L, ws, 0, L, ws.seglen,
                                        status, st);
     if (e != cudaSuccess) return e;
     e = run_pass<uint32_t>(PackedSrc{static_cast<const uint32_t *>(ws.keys[0]), L, ws.seglen}, 24,
