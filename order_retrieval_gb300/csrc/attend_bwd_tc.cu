@@ -127,7 +127,10 @@ __host__ __device__ inline size_t q_smem_bytes(int k) {
 }
 
 // Accumulators of one query row: x[0] = sum w, x[1] = sum w g, x[2] = sum g e,
-// x[3] = sum e, x[4..7] = sum g c (q-k), x[8..11] = sum c (q-k).
+// x[3] = sum e, x[4..7] = sum g c (q-k), x[8..11] = sum c (q-k).  Cauchy:
+// c = -2 u / gamma^2 and e = 2 (w - u) / gamma with u = w^2, so the sums are
+// kept without the constants: x[2] = sum u g, x[3] = sum u, x[4+d] =
+// sum u g (q-k)_d, x[8+d] = sum u (q-k)_d (the epilogue applies them).
 // With the softmax, e = 2 w (d2 - m) / gamma^3 depends on the shift m: moving
 // the sums from shift m to m' = m + dm multiplies every term by
 // sc = exp(dm / gamma^2) and subtracts dm 2/gamma^3 w from each e.
@@ -142,40 +145,6 @@ struct QAcc {
         x[3] -= dm * k2 * x[0];
 #pragma unroll
         for (int y = 0; y < 12; ++y) x[y] *= sc;
-    }
-    template <int WK>
-    __device__ void add(float w, float d2, float m, float g, const float (&qi)[4], float4 kk,
-                        float inv_g2, float inv_g) {
-        if constexpr (WK == kWCauchy) {
-            // Cauchy: c = -2 u / gamma^2 and e = 2 (w - u) / gamma with u = w^2, so
-            // the sums are kept without the constants: x[2] = sum u g, x[3] = sum u,
-            // x[4+d] = sum u g (q-k)_d, x[8+d] = sum u (q-k)_d (see the epilogue).
-            const float u = w * w, ug = u * g;
-            x[0] += w;
-            x[1] = __fmaf_rn(w, g, x[1]);
-            x[2] += ug;
-            x[3] += u;
-            const float dq[4] = {qi[0] - kk.x, qi[1] - kk.y, qi[2] - kk.z, qi[3] - kk.w};
-#pragma unroll
-            for (int d = 0; d < 4; ++d) {
-                x[4 + d] = __fmaf_rn(ug, dq[d], x[4 + d]);
-                x[8 + d] = __fmaf_rn(u, dq[d], x[8 + d]);
-            }
-            return;
-        }
-        const float c = -2.f * neg_dw_dd2<WK>(w, inv_g2);
-        const float e = dw_dgamma<WK>(w, d2, m, inv_g2, inv_g);
-        x[0] += w;
-        x[1] = __fmaf_rn(w, g, x[1]);
-        x[2] = __fmaf_rn(g, e, x[2]);
-        x[3] += e;
-        const float dq[4] = {qi[0] - kk.x, qi[1] - kk.y, qi[2] - kk.z, qi[3] - kk.w};
-#pragma unroll
-        for (int d = 0; d < 4; ++d) {
-            const float t = c * dq[d];
-            x[4 + d] = __fmaf_rn(g, t, x[4 + d]);
-            x[8 + d] += t;
-        }
     }
 };
 
@@ -197,7 +166,7 @@ struct QAcc2 {
     template <int DK, int WK>
     __device__ void add(float2 w, float2 d2, float2 m, float2 g, const float2 (&dq)[4],
                         float2 m2ig2, float2 two_ig, float2 k2) {
-        if constexpr (WK == kWCauchy) {        // the same constant-free sums as QAcc::add
+        if constexpr (WK == kWCauchy) {        // the constant-free sums (see QAcc)
             const float2 u = mul2(w, w), ug = mul2(u, g);
             x[0] = add2(x[0], w);
             x[1] = fma2(w, g, x[1]);

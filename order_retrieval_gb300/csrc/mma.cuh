@@ -73,24 +73,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Eight bf16 (one 16-byte chunk) -> eight floats, exactly.
-__device__ __forceinline__ void unpack8(uint4 raw, float (&f)[8]) {
-    const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        f[2 * e] = __uint_as_float(u[e] << 16);
-        f[2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
-    }
-}
-
-__device__ __forceinline__ float dist2_4(const float (&a)[4], float4 b) {
-    const float e0 = a[0] - b.x, e1 = a[1] - b.y, e2 = a[2] - b.z, e3 = a[3] - b.w;
-    float d = e0 * e0;
-    d = __fmaf_rn(e1, e1, d);
-    d = __fmaf_rn(e2, e2, d);
-    return __fmaf_rn(e3, e3, d);
-}
-
 __device__ __forceinline__ float4 load_k4(const float *row, int dK) {
     return make_float4(row[0], dK > 1 ? row[1] : 0.f, dK > 2 ? row[2] : 0.f,
                        dK > 3 ? row[3] : 0.f);
@@ -100,7 +82,7 @@ __device__ __forceinline__ float4 load_k4(const float *row, int dK) {
 
 namespace zeta {
 
-// ------------------------------------------------- mbarrier + TMA gather ---
+// ------------------------------------------------------------- mbarrier ---
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
@@ -109,12 +91,6 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 // Make barrier initialisation visible to the asynchronous (TMA) proxy.
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-}
-
-// Order this thread's generic-proxy shared-memory accesses before later
-// async-proxy (TMA) writes to the same buffer.
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
@@ -143,18 +119,6 @@ __device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, 
 }
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
     return mbar_wait_limit(bar, parity, kWaitLimit);
-}
-
-// Four rows (row coordinates r0..r3, column 0) of a 2-D tensor map whose box is
-// one row high, into consecutive rows at `dst`; completion counted on `bar`.
-// Callers pass in-range rows only.
-__device__ __forceinline__ void tma_gather4(void *dst, const void *tmap, int r0, int r1, int r2,
-                                            int r3, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(smem_u32(dst)),
-        "l"(tmap), "r"(0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-        : "memory");
 }
 
 // Cauchy weight with CUDA's fast division intrinsic (documented error of at
@@ -237,11 +201,6 @@ __device__ __forceinline__ float2 weight_fast2(float2 d2, float2 m, float2 inv_g
 // (exactly 1 when the shift did not move, 0 when nothing was summed yet).
 __device__ __forceinline__ float shift_scale(float m_new, float m_old, float inv_g2) {
     return m_new == m_old ? 1.f : __expf((m_new - m_old) * inv_g2);
-}
-
-// Two bf16 (one 32-bit word) -> float2, exactly.
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
 }  // namespace zeta
