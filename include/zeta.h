@@ -138,9 +138,12 @@ zeta_status_t zeta_sort_chunks(const zeta_problem_t *p, const void *key_codes,
  * footprint must stay fixed after start-up).  The pages have no counterpart:
  * this is an interface convenience, not part of the method.
  * Scratch: one file-scope device array of 32 MiB, which every GPU that loads
- * this library holds until the process exits.  Problems whose
- * zeta_sort_workspace_bytes exceeds 32 MiB are rejected with
- * ZETA_ERR_WORKSPACE before anything is launched.
+ * this library holds until the process exits.
+ * Checks, in order, before anything is launched: every check of
+ * zeta_sort_chunks (the same errors; a problem with nothing to sort, empty or
+ * with fewer than two chunks, returns ZETA_OK and touches no scratch), then
+ * the scratch size: a problem whose zeta_sort_workspace_bytes exceeds 32 MiB
+ * is rejected with ZETA_ERR_WORKSPACE.
  * Set-up: the first call on a device (with that device current) looks up the
  * array's device address with cudaGetSymbolAddress and caches it; make that
  * first call before any stream capture on that device.
@@ -148,7 +151,7 @@ zeta_status_t zeta_sort_chunks(const zeta_problem_t *p, const void *key_codes,
  * contents (nothing in it needs to start at zero).  Calls whose work overlaps
  * on the GPU (different streams, or different host threads on one device)
  * race on the array; order them on one stream.
- * Arguments, results and other errors are those of zeta_sort_chunks.
+ * Arguments and results are those of zeta_sort_chunks.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  */
 zeta_status_t zeta_sort_chunks_noalloc(const zeta_problem_t *p, const void *key_codes,

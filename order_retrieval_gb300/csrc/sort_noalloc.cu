@@ -46,7 +46,14 @@ zeta_status_t scratch_on_current_device(void **out) {
 ZETA_API zeta_status_t zeta_sort_chunks_noalloc(const zeta_problem_t *p, const void *key_codes,
                                                 void *prefix_codes, int32_t *prefix_idx,
                                                 cudaStream_t stream) {
-    if (zeta_prefix_entries(p) < 0) return ZETA_ERR_INVALID_ARG;
+    // Every check of zeta_sort_chunks first, with no workspace: that call
+    // returns before launching anything, with ZETA_OK when there is nothing to
+    // sort (an empty problem, or fewer than two chunks), its own error for an
+    // invalid or unsupported problem, and ZETA_ERR_WORKSPACE when the problem
+    // is valid and needs scratch.  Only then is the scratch size compared.
+    const zeta_status_t pre =
+        zeta_sort_chunks(p, key_codes, prefix_codes, prefix_idx, nullptr, 0, stream);
+    if (pre != ZETA_ERR_WORKSPACE) return pre;
     if (zeta_sort_workspace_bytes(p) > kNoallocScratchBytes) return ZETA_ERR_WORKSPACE;
     void *scratch = nullptr;
     const zeta_status_t s = scratch_on_current_device(&scratch);

@@ -28,6 +28,25 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     assert fn(ctypes.byref(bad), fake, fake, fake, None) == 1
 
 
+def test_noalloc_checks_come_in_the_order_of_the_workspace_sort():
+    """zeta_sort_chunks' own checks run before the scratch-size check: more
+    than 1024 chunks is ZETA_ERR_UNSUPPORTED even when the problem would also
+    need more than 32 MiB, and a problem with nothing to sort (one chunk) is
+    ZETA_OK whatever its size, touching nothing."""
+    L = zb.lib()
+    fn = L.zeta_sort_chunks_noalloc
+    fn.argtypes = [ctypes.POINTER(zb.zeta_problem_t)] + [ctypes.c_void_p] * 4
+    fn.restype = ctypes.c_int
+    fake = ctypes.c_void_p(0x1000)
+    many = zb.problem(1, 8, 1 << 22, 3, 64, 16, 2048, 10, "bf16")   # 2048 chunks
+    assert zb.zeta_sort_workspace_bytes(many) > 32 << 20
+    assert fn(ctypes.byref(many), fake, fake, fake, None) == 2
+    one = zb.problem(4, 8, 1 << 20, 3, 64, 16, 1 << 20, 10, "bf16")  # a single chunk
+    assert zb.zeta_sort_workspace_bytes(one) > 32 << 20
+    assert fn(ctypes.byref(one), fake, fake, fake, None) == 0
+    assert L.zeta_sort_chunks(ctypes.byref(one), fake, fake, fake, None, 0, None) == 0
+
+
 def _sorted_both_ways(w):
     g = W.generate(w)
     p = zb.problem_of(w)
