@@ -54,6 +54,8 @@ def _load():
     lib.orc_select.argtypes = [P, P, I64, I64, I, P, I64, P]
     lib.orc_attend_fwd.argtypes = [P, P, P, D, P, I64, I64, I, I, I, P, I64, P, P, I]
     lib.orc_attend_bwd.argtypes = [P, P, P, D, P, P, I64, I64, I, I, I, P, P, P, P, I]
+    lib.orc_attend_bwd_rows.argtypes = [P, P, P, D, P, P, I64, I64, I, I, I, P, I64,
+                                        P, P, P, P, I]
     lib.orc_exact_topk.argtypes = [P, P, I64, I64, I, I, P, I64, P]
     lib.orc_encode_axes.argtypes = [P, I64, I, I, P, P]
     lib.orc_project.argtypes = [P, I64, I, I, I, I, P, P, P, P, P]
@@ -232,8 +234,12 @@ def attend_fwd(q, k, v, gamma: float, idx, C: int, rows=None, kind: int = CAUCHY
     return out, rs
 
 
-def attend_bwd(q, k, v, gamma: float, idx, dout, C: int, kind: int = CAUCHY):
-    """One slice, selection fixed.  Returns (dq, dk, dv, dgamma) in float64."""
+def attend_bwd(q, k, v, gamma: float, idx, dout, C: int, kind: int = CAUCHY, rows=None):
+    """One slice, selection fixed.  Returns (dq, dk, dv, dgamma) in float64.
+
+    rows None: the gradients (idx [N, k]).  rows given: only the listed
+    queries contribute (idx holds their rows, [len(rows), k]); the results are
+    their shares of the sums."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     kx = np.ascontiguousarray(k, dtype=np.float64)
     v = np.ascontiguousarray(v, dtype=np.float64)
@@ -246,8 +252,10 @@ def attend_bwd(q, k, v, gamma: float, idx, dout, C: int, kind: int = CAUCHY):
     dk = np.empty_like(kx)
     dv = np.empty_like(v)
     dg = np.zeros(1, dtype=np.float64)
-    _load().orc_attend_bwd(_p(q), _p(kx), _p(v), float(gamma), _p(idx), _p(do), N, C, d_K, d_V,
-                           kk, _p(dq), _p(dk), _p(dv), _p(dg), int(kind))
+    r, nr = _rows(rows)
+    _load().orc_attend_bwd_rows(_p(q), _p(kx), _p(v), float(gamma), _p(idx), _p(do), N, C, d_K,
+                                d_V, kk, _p(r) if r is not None else None, nr, _p(dq), _p(dk),
+                                _p(dv), _p(dg), int(kind))
     return dq, dk, dv, float(dg[0])
 
 

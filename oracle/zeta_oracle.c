@@ -267,11 +267,28 @@ void orc_attend_fwd(const double *q, const double *kx, const double *v, double g
  *   dq_i  += dL/dw_ij * dw/d(d2) * 2 (q_i - k_j),  dk_j gets the negation
  *   dv_j  += a_ij dO_i,                  dgamma += dL/dw_ij * dw/dgamma
  * (Cauchy: dw/d(d2) = -w^2 / gamma^2, dw/dgamma = 2 w (1 - w) / gamma.)
- * Outputs are overwritten.  dgamma is this slice's sum. */
+ * Outputs are overwritten.  dgamma is this slice's sum.  rows == NULL: every
+ * query contributes (the gradient); otherwise only the queries listed in
+ * rows[0..nrows) do, idx holding their rows ([nrows][k]), so the outputs are
+ * those queries' shares of the sums (used to time a bounded sample). */
+void orc_attend_bwd_rows(const double *q, const double *kx, const double *v, double gamma,
+                         const int32_t *idx, const double *dout, int64_t N, int64_t C,
+                         int d_K, int d_V, int k, const int64_t *rows, int64_t nrows,
+                         double *dq, double *dk, double *dv, double *dgamma, int kind);
+
 void orc_attend_bwd(const double *q, const double *kx, const double *v, double gamma,
                     const int32_t *idx, const double *dout, int64_t N, int64_t C,
                     int d_K, int d_V, int k,
                     double *dq, double *dk, double *dv, double *dgamma, int kind)
+{
+    orc_attend_bwd_rows(q, kx, v, gamma, idx, dout, N, C, d_K, d_V, k, NULL, 0,
+                        dq, dk, dv, dgamma, kind);
+}
+
+void orc_attend_bwd_rows(const double *q, const double *kx, const double *v, double gamma,
+                         const int32_t *idx, const double *dout, int64_t N, int64_t C,
+                         int d_K, int d_V, int k, const int64_t *rows, int64_t nrows,
+                         double *dq, double *dk, double *dv, double *dgamma, int kind)
 {
     int64_t *set = (int64_t *)malloc((size_t)(k + C + 1) * sizeof(int64_t));
     double *w = (double *)malloc((size_t)(k + C + 1) * sizeof(double));
@@ -280,8 +297,10 @@ void orc_attend_bwd(const double *q, const double *kx, const double *v, double g
     memset(dk, 0, (size_t)N * d_K * sizeof(double));
     memset(dv, 0, (size_t)N * d_V * sizeof(double));
     double dg = 0.0;
-    for (int64_t i = 0; i < N; ++i) {
-        int64_t m = orc_set(idx + i * k, k, i, C, set);
+    int64_t cnt = rows ? nrows : N;
+    for (int64_t t = 0; t < cnt; ++t) {
+        int64_t i = rows ? rows[t] : t;
+        int64_t m = orc_set(idx + t * k, k, i, C, set);
         const double *qi = q + i * d_K;
         const double *doi = dout + i * d_V;
         double sh = orc_shift(kind, qi, kx, set, m, d_K);

@@ -358,6 +358,29 @@ def test_backward_invariants(oracle_mod):
     np.testing.assert_allclose(dv.sum(0), do.sum(0), atol=1e-11)
 
 
+def test_backward_row_shares_sum_to_the_gradient(oracle_mod):
+    """The gradients are sums over queries: the shares of a partition of the
+    queries (each part listed in rows, with its idx rows) add up to the full
+    backward, and a part's dq is zero outside its rows."""
+    N, C, k = 128, 32, 8
+    q, kx, v = _inputs(41, N, d_V=5)
+    do = np.random.default_rng(42).normal(size=(N, 5))
+    qc, kc = oracle_mod.encode(q, 10), oracle_mod.encode(kx, 10)
+    idx = oracle_mod.select(qc[None], kc[None], C, k)[0]
+    full = oracle_mod.attend_bwd(q, kx, v, 0.7, idx, do, C)
+    perm = np.random.default_rng(43).permutation(N)
+    parts = [np.sort(perm[:50]), np.sort(perm[50:90]), np.sort(perm[90:])]
+    tot = [np.zeros_like(full[0]), np.zeros_like(full[1]), np.zeros_like(full[2]), 0.0]
+    for rows in parts:
+        dq, dk, dv, dg = oracle_mod.attend_bwd(q, kx, v, 0.7, idx[rows], do, C, rows=rows)
+        outside = np.setdiff1d(np.arange(N), rows)
+        assert (dq[outside] == 0).all()
+        tot = [tot[0] + dq, tot[1] + dk, tot[2] + dv, tot[3] + dg]
+    for a, b in zip(tot[:3], full[:3]):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+    assert abs(tot[3] - full[3]) <= 1e-12 * max(1.0, abs(full[3]))
+
+
 # ---------------------------------------------------------------- recall ---
 
 def test_exact_topk_matches_lexsort(oracle_mod):
