@@ -10,13 +10,18 @@ carries the HBM roofline figure.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+The 1,048,576-token workload (B=1, H=8, k=64, C=4096) is timed forward only,
+and the peak device memory of each workload is reported.
+
 --impl reference times the CPU oracle (single thread) on a bounded sample of
-the same workload.  Under torchrun every rank runs its own batch (weak scaling)
-and the gamma gradient is summed across ranks (the only exchange the path has).
+the same workload: the queries of two chunks of one full-length slice.  Under
+torchrun every rank runs its own batch (weak scaling) and the gamma gradient is
+summed across ranks (the only exchange the path has).
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -30,14 +35,29 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-# DRAM bytes (read + write) of one attend_fwd_tc launch on the efficiency
-# workload, from the ncu capture summarised in
-# profiles/attend_kernels_train_bf16_b2_n65536.md; None once that kernel changes.
-ATTEND_FWD_DRAM_BYTES = 263_295_232
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# forward attend kernel on the efficiency workload, from one ncu capture, with a
+# digest of the kernel's sources at that time.  The line reports the figure only
+# while the sources still have that digest (else null: the kernel has changed).
+ATTEND_FWD_TRAFFIC = {
+    "bytes": None,
+    "sources_sha256": None,
+    "capture": "attend_fwd_tc, efficiency_bf16_n65536, ncu --metrics "
+               "dram__bytes_read.sum,dram__bytes_write.sum",
+}
+ATTEND_FWD_SOURCES = ("attend_fwd_tc.cu", "attend_fwd_tc.cuh", "mma.cuh", "common.cuh")
 
 METRIC = "ZETA attention tokens/s (fwd, fwd+bwd) at N=65536 and % of GB300 HBM roofline"
 L2_FLUSH_BYTES = 256 << 20
-CPU_SAMPLE_TOKENS = 8192
+PAGES_FWD_MB = 17348.2        # the pages' forward memory at 65,536 tokens (context)
+
+
+def sources_digest(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "order_retrieval_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 # ------------------------------------------------------------ byte models ---
@@ -148,51 +168,70 @@ def physical_gpu_index(local: int) -> int:
 
 # ------------------------------------------------------------ reference arm ---
 
-def cpu_sample(w):
-    """Bounded sample: the first CPU_SAMPLE_TOKENS tokens of slice (b=0, h=0),
-    run as their own causal problem.  Causality makes its forward identical
-    to the full workload's for those tokens."""
+def cpu_slice(w):
+    """Oracle inputs of one (b, h) slice of the workload at its full length N:
+    the generator's draw of a one-slice version of the workload (same
+    distribution and sizes, its own random values)."""
     from order_retrieval_gb300 import workloads as W
     g = W.generate(w.replace(B=1, H=1), with_dout=True)
-    n = CPU_SAMPLE_TOKENS
-    q, k = g["q"][0, 0, :n], g["k"][0, 0, :n]
-    v = W.values_f64(w, g["v"][0, 0, :n])
-    do = W.values_f64(w, g["dout"][0, 0, :n])
+    q, k = g["q"][0, 0], g["k"][0, 0]
+    v = W.values_f64(w, g["v"][0, 0])
+    do = W.values_f64(w, g["dout"][0, 0])
     return q, k, v, do, float(g["gamma"][0])
 
 
-def oracle_step(w, sample):
+def sample_rows(w):
+    """The queries of two chunks placed symmetrically about the middle of the
+    sequence (chunks n/4 and 3n/4 - 1 of n).  The oracle's work per query is
+    constant in the attend steps and linear in the chunk index in its select
+    (a count over the prefix), so the mean cost per query of the pair is the
+    mean over the whole slice."""
+    n = w.N // w.C
+    cs = sorted({n // 4, max(0, 3 * n // 4 - 1)})
+    return np.concatenate([np.arange(c * w.C, (c + 1) * w.C) for c in cs])
+
+
+def oracle_step(w, sample, rows=None):
+    """The oracle's path on one slice: encode, select, attend forward and
+    backward, for every query (rows None) or the listed ones."""
     import oracle
     q, k, v, do, gamma = sample
     qc = oracle.encode(q, w.bits)
     kc = oracle.encode(k, w.bits)
-    idx = oracle.select(qc[None], kc[None], w.C, w.k)[0]
-    oracle.attend_fwd(q, k, v, gamma, idx, w.C)
-    oracle.attend_bwd(q, k, v, gamma, idx, do, w.C)
+    idx = oracle.select(qc[None], kc[None], w.C, w.k, rows=rows)[0]
+    oracle.attend_fwd(q, k, v, gamma, idx, w.C, rows=rows)
+    oracle.attend_bwd(q, k, v, gamma, idx, do, w.C, rows=rows)
 
 
-def _oracle_shard(payload):
+def oracle_tokens_per_s(w, queries: int, seconds: float) -> float:
+    """A slice's queries belong to one of H heads: H of them make one token of
+    the metric (B*N tokens per step)."""
+    return queries / w.H / seconds
+
+
+def _oracle_shard(wname):
     """One host core's share of the sharded CPU baseline (a spawned process;
-    no GPU work): the oracle's step on the sample, timed."""
-    wname, sample = payload
+    no GPU work): draws its slice, then times the oracle on it."""
     from order_retrieval_gb300 import workloads as W
+    w = W.ALL[wname]
+    sample = cpu_slice(w)
     t0 = time.perf_counter()
-    oracle_step(W.ALL[wname], sample)
+    oracle_step(w, sample)
     return time.perf_counter() - t0
 
 
-def cpu_sharded(w, sample):
-    """The oracle on every host core at once, one process per core (spawned),
-    each on the sample; slices are independent, so this is the oracle sharded
+def cpu_sharded(w):
+    """The oracle on every host core at once, one spawned process per core,
+    each on a full slice; slices are independent, so this is the oracle sharded
     by (b, h).  Returns (tokens/s, cores)."""
     import multiprocessing as mp
     n = os.cpu_count() or 1
     try:
         with mp.get_context("spawn").Pool(n) as pool:
-            times = pool.map_async(_oracle_shard, [(w.name, sample)] * n).get(timeout=300)
+            times = pool.map_async(_oracle_shard, [w.name] * n).get(timeout=600)
     except (mp.TimeoutError, OSError):
         return None, n
-    return n * CPU_SAMPLE_TOKENS / w.H / max(times), n
+    return n * oracle_tokens_per_s(w, w.N, 1.0) / max(times), n
 
 
 def cpu_model() -> str:
@@ -206,26 +245,24 @@ def cpu_model() -> str:
     return "unknown"
 
 
-def cpu_tokens_per_s(w, sample, seconds: float) -> float:
-    """Tokens of the sample are single-head tokens: H of them make one token."""
-    return CPU_SAMPLE_TOKENS / w.H / seconds
-
-
 def run_reference(args, w, rank):
     if rank != 0:
         return
     import oracle
     oracle.build()
-    sample = cpu_sample(w)
+    sample = cpu_slice(w)
+    rows = sample_rows(w)
     for _ in range(args.warmup):
-        oracle_step(w, sample)
+        oracle_step(w, sample, rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(w, sample)
+        oracle_step(w, sample, rows)
     dt = (time.perf_counter() - t0) / args.steps
-    val = cpu_tokens_per_s(w, sample, dt)
-    desc = (f"first {CPU_SAMPLE_TOKENS} tokens of one (b,h) slice of {w.name}, as their own "
-            "causal problem: encode, select, attend fwd + bwd")
+    val = oracle_tokens_per_s(w, len(rows), dt)
+    n = w.N // w.C
+    desc = (f"per step the queries of chunks {n // 4} and {3 * n // 4 - 1} ({len(rows)} queries) "
+            f"of one full-length (N={w.N}) slice of {w.name}: encode, select, attend fwd + bwd; "
+            "tokens/s = queries / H / time")
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -272,6 +309,21 @@ def run_ours(args, w, rank, world):
     g = W.generate(wr, with_dout=True)
     p = zb.problem_of(wr)
     warm = max(3, args.warmup)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak_mb = {}
+
+    def mem_start():
+        """Peak-memory window of one workload: everything it allocates from
+        here on (inputs, buffers, workspaces) is counted."""
+        torch.cuda.synchronize(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        return torch.cuda.memory_allocated(dev)
+
+    def mem_peak(base):
+        torch.cuda.synchronize(dev)
+        return (torch.cuda.max_memory_allocated(dev) - base) / 2 ** 20
+
+    mem0 = mem_start()
 
     def to_dev(a, vals=False):
         t = torch.from_numpy(np.ascontiguousarray(a)).reshape(-1)
@@ -283,7 +335,6 @@ def run_ours(args, w, rank, world):
         to_dev(g["q"]), to_dev(g["k"]), to_dev(g["v"], True), to_dev(g["gamma"]),
         to_dev(g["dout"], True))
     plan = ZetaPlan(p, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def barrier():
         if world > 1:
@@ -316,6 +367,7 @@ def run_ours(args, w, rank, world):
     barrier()
     if int(plan.status.item()) != 0:
         raise RuntimeError(f"device status {plan.status.item()}")
+    peak_mb[w.name + " (fwd+bwd)"] = mem_peak(mem0)
 
     # --- timed: K graph replays, each bracketed by events; L2 flushed between steps
     step_ms = []
@@ -335,6 +387,8 @@ def run_ours(args, w, rank, world):
         barrier()
         wall = time.perf_counter() - t_wall
     dev_ms = sum(step_ms) / len(step_ms)
+    step_stats = {"mean": dev_ms, "median": statistics.median(step_ms), "min": min(step_ms),
+                  "max": max(step_ms), "n": len(step_ms)}
     t = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -467,11 +521,13 @@ def run_ours(args, w, rank, world):
     we = W.EFFICIENCY.replace(seed=W.EFFICIENCY.seed + 1000 * rank)
     ge = W.generate(we)
     pe = zb.problem_of(we)
+    mem_e = mem_start()
     qe, ke = to_dev(ge["q"])[1], to_dev(ge["k"])[1]
     ve, gme = to_dev(ge["v"], True)[1], to_dev(ge["gamma"])[1]
     plan_e = ZetaPlan(pe, dev, backward=False)
     for _ in range(warm):
         plan_e.forward(qe, ke, ve, gme)
+    peak_mb[we.name + " (fwd)"] = mem_peak(mem_e)
     fwd_e, att_e = [], []
     for _ in range(args.steps):
         flush.zero_()
@@ -529,6 +585,44 @@ def run_ours(args, w, rank, world):
     fus_tot_ms = sum(fus_tot) / len(fus_tot)
     fus_k_ms = sum(fus_k) / len(fus_k)
     del plan_f
+
+    # --- the 1,048,576-token workload (B=1, H=8, k=64, C=4096): forward alone,
+    # its index part (encode, sort, select) and the attend kernel
+    wl = W.LONG.replace(seed=W.LONG.seed + 1000 * rank)
+    gl = W.generate(wl)
+    pl = zb.problem_of(wl)
+    mem_l = mem_start()
+    ql, kl = to_dev(gl["q"])[1], to_dev(gl["k"])[1]
+    vl, gml = to_dev(gl["v"], True)[1], to_dev(gl["gamma"])[1]
+    del gl
+    plan_l = ZetaPlan(pl, dev, backward=False)
+    for _ in range(warm):
+        plan_l.forward(ql, kl, vl, gml)
+    peak_mb[wl.name + " (fwd)"] = mem_peak(mem_l)
+    long_tot, long_idx = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        e = [ev() for _ in range(3)]
+        e[0].record()
+        zb.zeta_encode(pl, ql, plan_l.q_codes)
+        zb.zeta_encode(pl, kl, plan_l.k_codes)
+        zb.zeta_sort_chunks(pl, plan_l.k_codes, plan_l.prefix_codes, plan_l.prefix_idx,
+                            plan_l.sort_ws)
+        zb.zeta_select_topk(pl, plan_l.q_codes, plan_l.prefix_codes, plan_l.prefix_idx,
+                            plan_l.idx)
+        e[1].record()
+        zb.zeta_attend_fwd(pl, ql, kl, vl, gml, plan_l.idx, plan_l.out, plan_l.rowsum,
+                           plan_l.status)
+        e[2].record()
+        e[2].synchronize()
+        long_tot.append(e[0].elapsed_time(e[2]))
+        long_idx.append(e[0].elapsed_time(e[1]))
+    if int(plan_l.status.item()) != 0:
+        raise RuntimeError(f"device status {plan_l.status.item()} (1M tokens)")
+    long_ms = sum(long_tot) / len(long_tot)
+    long_idx_ms = sum(long_idx) / len(long_idx)
+    del plan_l, ql, kl, vl, gml
+    torch.cuda.empty_cache()
 
     variants = {}
     # --- the pages' 12-bit grid (36-bit codes in 64-bit words) on the same
@@ -693,18 +787,22 @@ def run_ours(args, w, rank, world):
     fbt = fwd_attend_bytes(wr)
     bb = bwd_attend_bytes(wr)
 
-    # CPU baseline: the oracle on a bounded sample of this workload
+    # CPU baseline: the oracle on one full-length slice of this workload
     import oracle
     oracle.build()
-    sample = cpu_sample(w)
+    sample = cpu_slice(w)
     t0 = time.perf_counter()
     oracle_step(w, sample)
     cpu_dt = time.perf_counter() - t0
-    sharded_rate, sharded_cores = cpu_sharded(w, sample)
+    sharded_rate, sharded_cores = cpu_sharded(w)
+    digest = sources_digest(ATTEND_FWD_SOURCES)
+    traffic = (ATTEND_FWD_TRAFFIC["bytes"]
+               if ATTEND_FWD_TRAFFIC["sources_sha256"] == digest else None)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warm, "ms_per_step": dev_ms,
+        "ms_per_step_stats": step_stats,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "dtype_detail": "v, dO, out, dv bf16; q, k, weights and accumulation f32",
         "data": "synthetic",
@@ -717,6 +815,15 @@ def run_ours(args, w, rank, world):
         "fwd_efficiency": {"workload": we.name, "tokens_per_s": we.B * we.N * world /
                            (fwd_e_ms * 1e-3), "ms": fwd_e_ms, "attend_fwd_ms": att_e_ms,
                            "attend_fwd_ms_warm_l2": att_warm_ms},
+        "fwd_long": {"workload": wl.name, "tokens_per_s": wl.B * wl.N * world / (long_ms * 1e-3),
+                     "ms": long_ms, "encode_sort_select_ms": long_idx_ms,
+                     "attend_fwd_ms": long_ms - long_idx_ms,
+                     "attend_fwd_frac": fwd_attend_bytes(wl) / ((long_ms - long_idx_ms) * 1e-3)
+                                        / 1e9 / hbm_peak},
+        "peak_device_mb": {**peak_mb, "how": "torch max_memory_allocated over each workload's "
+                                              "inputs, buffers, workspaces and outputs (the "
+                                              "library allocates nothing itself)",
+                           "pages_fwd_65536_tokens_mb": PAGES_FWD_MB},
         "fwd_efficiency_fused": {
             "workload": we.name, "call": "zeta_select_attend_fwd",
             "tokens_per_s": we.B * we.N * world / (fus_tot_ms * 1e-3), "ms": fus_tot_ms,
@@ -729,7 +836,9 @@ def run_ours(args, w, rank, world):
         "variants": variants,
         "roofline": {"kernel": "attend_fwd_tc (efficiency workload, L2 flushed)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": ATTEND_FWD_DRAM_BYTES,
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "traffic_source": ATTEND_FWD_TRAFFIC["capture"] + (
+                         "" if traffic is not None else " (null: kernel sources changed since)"),
                      "algorithmic_bytes": fb, "peak_source": peak_src},
         "roofline_projection": {
             "kernel": "project_encode_tc (tcgen05, B=4 N=65536 D=512 F=64, L2 flushed)",
@@ -753,15 +862,18 @@ def run_ours(args, w, rank, world):
                        "overlapping the neighbouring steps' compute",
                 "serial_value": e2e_serial},
         "gpu_launches": launches_per_step(w) * args.steps,
-        "cpu_baseline": {"value": cpu_tokens_per_s(w, sample, cpu_dt), "unit": "tokens/s",
+        "cpu_baseline": {"value": oracle_tokens_per_s(w, w.N, cpu_dt), "unit": "tokens/s",
                          "cores": 1, "kind": "oracle",
-                         "sample": f"first {CPU_SAMPLE_TOKENS} tokens of one (b,h) slice of "
-                                   f"{w.name} as their own causal problem; fwd+bwd",
+                         "sample": f"one full-length slice (N={w.N} queries of one head) of "
+                                   f"{w.name}: encode, select, attend fwd + bwd; extrapolated "
+                                   f"to the B*H = {w.B * w.H} slices of a step "
+                                   "(tokens/s = N / H / time of the slice)",
+                         "slice_s": cpu_dt,
                          "cpu_model": cpu_model(),
                          "sharded": {"value": sharded_rate, "unit": "tokens/s",
                                      "cores": sharded_cores,
                                      "how": "one spawned process per host core, each on "
-                                            "the same sample (slices are independent)"}},
+                                            "a full slice (slices are independent)"}},
         "clocks": clk.summary(),
         "wall_s_timed": wall,
     }
@@ -772,7 +884,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     args = ap.parse_args()
     from order_retrieval_gb300 import workloads as W
