@@ -1,5 +1,8 @@
 """Helpers for the GPU parity tests: move seeded inputs to the device, run the
 library through its C ABI, bring results back as numpy."""
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import torch
 
@@ -73,6 +76,16 @@ class Run:
     def status(self):
         return int(self.plan.status.item())
 
+    def idx_slice(self, s):
+        return self.plan.idx.view(self.S, self.N, self.w.k)[s].cpu().numpy()
+
+    def grads_slice(self, s):
+        """(dq, dk, dv) of slice s as float64 numpy."""
+        w = self.w
+        return (self.plan.dq.view(self.S, self.N, w.d_K)[s].cpu().numpy().astype(np.float64),
+                self.plan.dk.view(self.S, self.N, w.d_K)[s].cpu().numpy().astype(np.float64),
+                host_vals(self.plan.dv.view(self.S, self.N, w.d_V)[s]))
+
     def grads(self):
         w = self.w
         return (self.plan.dq.cpu().numpy().astype(np.float64).reshape(self.S, self.N, w.d_K),
@@ -105,3 +118,11 @@ def assert_close_f32(got, ref, atol=1e-5, what=""):
     bound = atol * np.maximum(1.0, np.abs(ref))
     bad = err > bound
     assert not bad.any(), f"{what}: {bad.sum()} entries off, worst {err.max():.3e}"
+
+
+def in_threads(fn, items):
+    """fn over items on every host core; the oracle's C calls release the GIL,
+    so threads run them in parallel.  Results in the order of items."""
+    items = list(items)
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(items), os.cpu_count() or 1))) as ex:
+        return list(ex.map(fn, items))

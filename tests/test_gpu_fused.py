@@ -13,7 +13,8 @@ from order_retrieval_gb300 import binding as zb
 from order_retrieval_gb300 import workloads as W
 from order_retrieval_gb300.pipeline import ZetaPlan
 
-from gpu_util import assert_close_bf16, assert_close_f32, dev_vals, host_vals, slice_inputs
+from gpu_util import (assert_close_bf16, assert_close_f32, dev_vals, host_vals, in_threads,
+                      slice_inputs)
 
 pytestmark = [
     pytest.mark.gpu,
@@ -21,7 +22,10 @@ pytestmark = [
 ]
 
 
-def _run(w, weight="cauchy", rows=None, slices=(0,)):
+def _run(w, weight="cauchy", rows=None, slices=(0,), full=()):
+    """Fused and two-call forwards of w, bit for bit equal; the listed slices
+    against the oracle on `rows` (all rows when None), the slices in `full` on
+    all rows."""
     g = W.generate(w)
     p = zb.problem_of(w, weight=weight)
     q = torch.from_numpy(g["q"]).cuda().reshape(-1)
@@ -43,17 +47,21 @@ def _run(w, weight="cauchy", rows=None, slices=(0,)):
     out = host_vals(one.out).reshape(S, w.N, w.d_V)
     rs = one.rowsum.cpu().numpy().astype(np.float64).reshape(S, w.N)
     kind = {"cauchy": oracle.CAUCHY, "softmax": oracle.SOFTMAX, "inv_euclid": oracle.INV_EUCLID}
-    for s in slices:
+
+    def check(case):
+        s, r = case
         qs, ks, vs, gamma, _ = slice_inputs(w, g, s)
         ref = oracle.select(oracle.encode(qs, w.bits)[None], oracle.encode(ks, w.bits)[None],
-                            w.C, w.k, rows=rows)[0]
-        got = idx[s] if rows is None else idx[s][rows]
-        assert np.array_equal(got, ref)
-        o_ref, s_ref = oracle.attend_fwd(qs, ks, vs, gamma, ref, w.C, rows=rows,
+                            w.C, w.k, rows=r)[0]
+        sel = slice(None) if r is None else r
+        assert np.array_equal(idx[s][sel], ref)
+        o_ref, s_ref = oracle.attend_fwd(qs, ks, vs, gamma, ref, w.C, rows=r,
                                          kind=kind[weight])
         close = assert_close_bf16 if w.v_dtype == "bf16" else assert_close_f32
-        close(out[s] if rows is None else out[s][rows], o_ref, what="out")
-        assert_close_f32(rs[s] if rows is None else rs[s][rows], s_ref, what="rowsum")
+        close(out[s][sel], o_ref, what="out")
+        assert_close_f32(rs[s][sel], s_ref, what="rowsum")
+
+    in_threads(check, [(s, rows) for s in slices] + [(s, None) for s in full])
 
 
 def test_tiny_f32_takes_the_two_call_path():
@@ -78,7 +86,10 @@ def test_tensor_core_shapes(kw):
 
 
 @pytest.mark.parametrize("w", [W.EFFICIENCY, W.PAGES12], ids=lambda w: w.name)
-def test_efficiency_scale_sampled(w):
+def test_efficiency_scale_full_slice(w):
+    """The timed 65,536-token workload (and the pages' 12-bit grid): every
+    slice of the fused call equal to the two-call path bit for bit, slice 5
+    whole against the oracle element by element, slice 0 on sampled rows."""
     rng = np.random.default_rng(5)
     rows = np.sort(np.concatenate([rng.choice(w.N, 40, replace=False), [0, w.C, w.N - 1]]))
-    _run(w, rows=rows, slices=(0, 5))
+    _run(w, rows=rows, slices=(0,), full=(5,))

@@ -15,7 +15,7 @@ from order_retrieval_gb300 import binding as zb
 from order_retrieval_gb300 import workloads as W
 
 from gpu_util import (Run, assert_close_bf16, assert_close_f32, codes_np, dev_vals,
-                      slice_inputs)
+                      in_threads, slice_inputs)
 
 pytestmark = [
     pytest.mark.gpu,
@@ -38,22 +38,26 @@ def _prefix_is_sorted_permutation(pc, pi, w):
         assert (idx[1:][tie] > idx[:-1][tie]).all()
 
 
-def _check_forward_slice(run, s, rows=None, bf16=False):
-    w, g = run.w, run.g
+def _check_forward_host(w, g, s, idx_s, out_s, rs_s, rows=None, bf16=False):
+    """Slice s of a forward (device results already on the host, all N rows)
+    against the oracle: idx bit for bit, rowsum at float32, out at the
+    tolerance of its dtype; rows limits the check to those queries."""
     q, k, v, gamma, _ = slice_inputs(w, g, s)
     qc = oracle.encode(q, w.bits)
     kc = oracle.encode(k, w.bits)
     idx_ref = oracle.select(qc[None], kc[None], w.C, w.k, rows=rows)[0]
-    idx_gpu = run.idx()[s] if rows is None else run.idx()[s][rows]
-    assert np.array_equal(idx_gpu, idx_ref)
+    sel = slice(None) if rows is None else rows
+    assert np.array_equal(idx_s[sel], idx_ref)
     out_ref, rs_ref = oracle.attend_fwd(q, k, v, gamma, idx_ref, w.C, rows=rows)
-    out = run.out()[s] if rows is None else run.out()[s][rows]
-    rs = run.rowsum()[s] if rows is None else run.rowsum()[s][rows]
-    assert_close_f32(rs, rs_ref, what="rowsum")
+    assert_close_f32(rs_s[sel], rs_ref, what="rowsum")
     if bf16:
-        assert_close_bf16(out, out_ref, what="out")
+        assert_close_bf16(out_s[sel], out_ref, what="out")
     else:
-        assert_close_f32(out, out_ref, what="out")
+        assert_close_f32(out_s[sel], out_ref, what="out")
+
+
+def _check_forward_slice(run, s, rows=None, bf16=False):
+    _check_forward_host(run.w, run.g, s, run.idx()[s], run.out()[s], run.rowsum()[s], rows, bf16)
 
 
 # ------------------------------------------------------------------ encode ---
@@ -143,8 +147,11 @@ def test_forward_efficiency_sampled(w):
     rng = np.random.default_rng(0)
     rows = np.sort(np.concatenate([rng.choice(w.N, 120, replace=False),
                                    [0, w.C - 1, w.C, 2 * w.C - 1, w.N - 1]]))
-    for s in range(run.S):
-        _check_forward_slice(run, s, rows=rows, bf16=True)
+    idx, out, rs = run.idx(), run.out(), run.rowsum()
+    # slice 5 whole, element by element; the other slices on the sampled rows
+    cases = [(s, None if s == 5 else rows) for s in range(run.S)]
+    in_threads(lambda c: _check_forward_host(w, g, c[0], idx[c[0]], out[c[0]], rs[c[0]],
+                                             rows=c[1], bf16=True), cases)
 
 
 # ---------------------------------------------------------------- backward ---
@@ -204,23 +211,66 @@ def test_backward_fd_workload_f32():
     assert_close_f32(run.grads()[3], _dgamma_ref(run), what="dgamma")
 
 
+def _train_slices_against_oracle(run, full, head, bf16):
+    """The training workload's backward: dq, dk, dv of the slices in `full`
+    element by element, and dgamma of `head`, which sums over that head's B
+    slices s = b*H + head, against the sum of the oracle's per-slice values.
+    Each slice's selection comes from the oracle (checked against the device's
+    bit for bit); the oracle runs on all listed slices at once in threads."""
+    w, g = run.w, run.g
+    hs = [b * w.H + head for b in range(w.B)]
+    todo = sorted(set(full) | set(hs))
+    dev_idx = {s: run.idx_slice(s) for s in todo}
+
+    def one(s):
+        q, k, v, gamma, dout = slice_inputs(w, g, s)
+        ref = oracle.select(oracle.encode(q, w.bits)[None], oracle.encode(k, w.bits)[None],
+                            w.C, w.k)[0]
+        assert np.array_equal(dev_idx[s], ref), f"idx of slice {s}"
+        return oracle.attend_bwd(q, k, v, gamma, ref, dout, w.C)
+
+    refs = dict(zip(todo, in_threads(one, todo)))
+    close = assert_close_bf16 if bf16 else assert_close_f32
+    for s in full:
+        dq, dk, dv = run.grads_slice(s)
+        dq_r, dk_r, dv_r, _ = refs[s]
+        close(dq, dq_r, what=f"dq[{s}]")
+        close(dk, dk_r, what=f"dk[{s}]")
+        close(dv, dv_r, what=f"dv[{s}]")
+    dg = run.plan.dgamma.cpu().numpy().astype(np.float64)
+    dg_ref = sum(refs[s][3] for s in hs)
+    close(np.array([dg[head]]), np.array([dg_ref]), what=f"dgamma[{head}]")
+
+
 def test_backward_train_f32_sampled():
     """The training workload (B=4, H=8, N=65536, k=48, C=1024) with float32
-    values and upstream gradients, two slices against the oracle."""
+    values and upstream gradients: slices 0 and 29 whole, and the gamma
+    gradient of head 5 (slices 5, 13, 21, 29) against the oracle."""
     w = W.TRAIN.replace(v_dtype="f32")
     run = Run(w, backward=True)
     assert run.status() == 0
-    for s in (0, 29):
-        _check_backward_slice(run, s)
+    _train_slices_against_oracle(run, full=(0, 29), head=5, bf16=False)
 
 
 def test_backward_train_bf16_sampled():
     """The timed training workload itself (bf16 values and dO, tensor-core
-    kernels), slices 0 and 31 against the oracle."""
+    kernels): slices 0 and 31 whole, and the gamma gradient of head 7
+    (slices 7, 15, 23, 31) against the oracle."""
     run = Run(W.TRAIN, backward=True)
     assert run.status() == 0
-    for s in (0, 31):
-        _check_backward_slice(run, s, bf16=True)
+    _train_slices_against_oracle(run, full=(0, 31), head=7, bf16=True)
+
+
+def test_backward_beyond_float_slot_division():
+    """N k above 2^24 (N = 65536, k = 260): the backward's transpose maps a
+    window slot to its query by integer division instead of the float
+    reciprocal; one slice against the oracle."""
+    w = W.TRAIN.replace(name="train_k260", B=1, H=1, k=260)
+    assert w.N * w.k > 1 << 24
+    run = Run(w, backward=True)
+    assert run.status() == 0
+    _check_backward_slice(run, 0, bf16=True)
+    assert_close_bf16(run.grads()[3], _dgamma_ref(run), what="dgamma")
 
 
 def test_backward_beyond_16bit_sequence_bf16():

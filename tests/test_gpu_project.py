@@ -3,9 +3,11 @@ network per head, OpenReview discussion of "ZETA: Leveraging Z-order Curves
 for Efficient Top-k Attention", reply A "LLMs impact the selection of d_K").
 
 Coordinates are compared with the oracle's double-precision projection of the
-same bf16 inputs; the codes are compared bit for bit with the oracle's encode
-of the coordinates the device produced (the quantiser's decision is taken on
-the same float32 value on both sides)."""
+same bf16 inputs.  The codes are compared with the oracle's encode of the
+oracle's own coordinates: they must be equal except where a coordinate of the
+oracle lies within the coordinate tolerance of a grid cell edge (there the two
+sides' coordinates, within that tolerance of each other, may fall in
+neighbouring cells), and such excused codes must be few."""
 import numpy as np
 import pytest
 import torch
@@ -50,8 +52,23 @@ def run_projection(pj, g, bits=None):
             codes_np(qc).reshape(shape[:3]), codes_np(kc).reshape(shape[:3]))
 
 
+# At most this fraction of the codes may be excused (a coordinate of the oracle
+# near a cell edge and the device on the other side of it).  The device's
+# coordinates are typically within ~1e-6 of the oracle's, so a code is excused
+# with probability about 2 * 1e-6 * d_K / cell width (~0.3 % at 10 bits).
+EXCUSED_MAX = 0.01
+
+
+def _near_cell_edge(y, bits, tol):
+    """True where some coordinate of y (float64 [..., d_K]) lies within tol of a
+    cell edge of the 2^bits grid on [-1, 1): x = m / 2^(bits-1) - 1."""
+    t = (y + 1.0) * 2.0 ** (bits - 1)
+    return (np.abs(t - np.round(t)) <= tol * 2.0 ** (bits - 1)).any(axis=-1)
+
+
 def _check(pj, g, w, q, k, qc, kc, tokens):
     x = W.bf16_bits_to_f32(g["x"]).astype(np.float64)
+    excused = total = 0
     for pr, (y, codes) in enumerate(((q, qc), (k, kc))):
         W1 = W.bf16_bits_to_f32(g["W1"][pr]).astype(np.float64)
         for b in range(w.B):
@@ -59,8 +76,13 @@ def _check(pj, g, w, q, k, qc, kc, tokens):
             got = y[b][:, tokens].transpose(1, 0, 2)                 # [T, H, d_K]
             err = np.abs(got - ref).max()
             assert err <= COORD_ATOL, f"projection {pr}: max err {err:.3e}"
-            want = oracle.encode(got, w.bits)                          # [T, H]
-            assert np.array_equal(codes[b][:, tokens].T, want)
+            want = oracle.encode(ref, w.bits)                          # [T, H]
+            off = codes[b][:, tokens].T != want
+            near = _near_cell_edge(ref, w.bits, COORD_ATOL)
+            assert not (off & ~near).any(), f"projection {pr}: code off away from a cell edge"
+            excused += int(off.sum())
+            total += off.size
+    assert excused <= EXCUSED_MAX * total, f"{excused} of {total} codes excused"
 
 
 @pytest.mark.parametrize("bits", [10, 12])
