@@ -89,11 +89,9 @@ size_t zeta_code_bytes(const zeta_problem_t *p);
  * Returns -1 when the problem is invalid. */
 int64_t zeta_prefix_entries(const zeta_problem_t *p);
 
-/* Workspace bytes needed by zeta_sort_chunks / zeta_attend_bwd /
- * zeta_attend_bwd_windows (0 if invalid). */
+/* Workspace bytes needed by zeta_sort_chunks / zeta_attend_bwd (0 if invalid). */
 size_t zeta_sort_workspace_bytes(const zeta_problem_t *p);
 size_t zeta_bwd_workspace_bytes(const zeta_problem_t *p);
-size_t zeta_bwd_windows_workspace_bytes(const zeta_problem_t *p);
 
 /* Human-readable name of a status code (static storage). */
 const char *zeta_status_string(zeta_status_t s);
@@ -337,41 +335,6 @@ zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, const flo
                               const void *dout, float *dq, float *dk, void *dv, float *dgamma,
                               void *workspace, size_t ws_bytes, int32_t *dev_status,
                               cudaStream_t stream);
-
-/*
- * zeta_attend_bwd_windows -- zeta_attend_bwd for idx rows that are windows of
- * the sorted prefixes, as zeta_select_topk and zeta_select_attend_fwd write
- * them.
- * Passage: OpenReview reply A3 "Chunking ... & Where efficiency is coming
- * from" (one sort, then a binary search of each query's insertion position)
- * and reply A2 "Clarification" (the window centred at that position): every
- * window is one contiguous run of its chunk's sorted prefix.
- * The gradients are those of zeta_attend_bwd.  The queries that selected a
- * key are found from the windows themselves instead of a sort of idx: ordered
- * by window start, the queries of a chunk that selected the key at prefix
- * position p are one contiguous range (those whose start lies in (p - k, p]).
- * Every sum still runs in a fixed order, so results are bit-reproducible; the
- * order differs from zeta_attend_bwd's, so the two agree to rounding.
- *   prefix_idx   in : the prefix table the rows were selected from
- *                     (zeta_sort_chunks), [B, H, T]
- *   idx          in : int32 [B, H, N, k]: row i of chunk c >= 1 must be the
- *                     entries [start, start + k) of prefix c for some start
- *   other arguments as for zeta_attend_bwd; workspace of at least
- *   zeta_bwd_windows_workspace_bytes.
- * A row of chunk c >= 1 whose first entry is not a key of prefix c, or whose
- * last entry is not the prefix entry k - 1 places after the first, records
- * ZETA_ERR_INVALID_ARG in dev_status (the key-side gradients are then
- * meaningless: use zeta_attend_bwd for rows of any other origin, such as the
- * union of several curves).  Problems outside the tensor-core shapes (bf16
- * values, d_V = 64, d_K <= 4) or with C > 4096 run zeta_attend_bwd's path.
- * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED, ZETA_ERR_WORKSPACE.
- */
-zeta_status_t zeta_attend_bwd_windows(const zeta_problem_t *p, const float *q, const float *k,
-                                      const void *v, const float *gamma,
-                                      const int32_t *prefix_idx, const int32_t *idx,
-                                      const void *dout, float *dq, float *dk, void *dv,
-                                      float *dgamma, void *workspace, size_t ws_bytes,
-                                      int32_t *dev_status, cudaStream_t stream);
 
 /*
  * zeta_check_bounded_wait -- diagnostic of the device-side failure detection.

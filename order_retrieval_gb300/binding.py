@@ -85,8 +85,6 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.zeta_sort_workspace_bytes.restype = ctypes.c_size_t
     L.zeta_bwd_workspace_bytes.argtypes = [PP]
     L.zeta_bwd_workspace_bytes.restype = ctypes.c_size_t
-    L.zeta_bwd_windows_workspace_bytes.argtypes = [PP]
-    L.zeta_bwd_windows_workspace_bytes.restype = ctypes.c_size_t
     L.zeta_status_string.argtypes = [S]
     L.zeta_status_string.restype = ctypes.c_char_p
     L.zeta_encode.argtypes = [PP, P, P, P]
@@ -104,8 +102,6 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
     L.zeta_attend_fwd.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     L.zeta_attend_fwd.restype = S
     L.zeta_attend_bwd.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
-    L.zeta_attend_bwd_windows.argtypes = [PP] + [P] * 12 + [ctypes.c_size_t, P, P]
-    L.zeta_attend_bwd_windows.restype = S
     L.zeta_select_attend_fwd.argtypes = [PP] + [P] * 12
     L.zeta_check_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_int32, P, P]
     L.zeta_check_bounded_wait.restype = S
@@ -180,10 +176,6 @@ def zeta_sort_workspace_bytes(p: zeta_problem_t) -> int:
 
 def zeta_bwd_workspace_bytes(p: zeta_problem_t) -> int:
     return lib().zeta_bwd_workspace_bytes(ctypes.byref(p))
-
-
-def zeta_bwd_windows_workspace_bytes(p) -> int:
-    return int(lib().zeta_bwd_windows_workspace_bytes(ctypes.byref(p)))
 
 
 def zeta_status_string(code: int) -> str:
@@ -374,27 +366,3 @@ def zeta_attend_bwd(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, workspace,
                                  _ptr(idx), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                                  _ptr(dgamma), _ptr(workspace), ws_bytes, _ptr(dev_status),
                                  _stream(stream)))
-
-
-def zeta_attend_bwd_windows(p, q, k, v, gamma, prefix_idx, idx, dout, dq, dk, dv, dgamma,
-                            workspace, dev_status=None, stream=None):
-    S = p.B * p.H * p.N
-    vt = v_torch_dtype(p)
-    _expect(q, "q", torch.float32, S * p.d_K)
-    _expect(k, "k", torch.float32, S * p.d_K)
-    _expect(v, "v", vt, S * p.d_V)
-    _expect(gamma, "gamma", torch.float32, p.H)
-    _expect(prefix_idx, "prefix_idx", torch.int32, p.B * p.H * zeta_prefix_entries(p))
-    _expect(idx, "idx", torch.int32, S * p.k)
-    _expect(dout, "dout", vt, S * p.d_V)
-    _expect(dq, "dq", torch.float32, S * p.d_K)
-    _expect(dk, "dk", torch.float32, S * p.d_K)
-    _expect(dv, "dv", vt, S * p.d_V)
-    _expect(dgamma, "dgamma", torch.float32, p.H)
-    _expect(dev_status, "dev_status", torch.int32, 1)
-    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check("zeta_attend_bwd_windows",
-           lib().zeta_attend_bwd_windows(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
-                                         _ptr(prefix_idx), _ptr(idx), _ptr(dout), _ptr(dq),
-                                         _ptr(dk), _ptr(dv), _ptr(dgamma), _ptr(workspace),
-                                         ws_bytes, _ptr(dev_status), _stream(stream)))

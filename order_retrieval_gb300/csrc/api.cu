@@ -70,12 +70,6 @@ ZETA_API size_t zeta_bwd_workspace_bytes(const zeta_problem_t *p) {
     return zeta::bwd_ws_bytes(pr);
 }
 
-ZETA_API size_t zeta_bwd_windows_workspace_bytes(const zeta_problem_t *p) {
-    Prob pr;
-    if (check_problem(p, &pr) != ZETA_OK) return 0;
-    return zeta::bwd_windows_ws_bytes(pr);
-}
-
 ZETA_API const char *zeta_status_string(zeta_status_t s) {
     switch (s) {
         case ZETA_OK: return "ZETA_OK";
@@ -234,31 +228,6 @@ ZETA_API zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, 
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ZETA_ERR_WORKSPACE;
     return from_cuda(zeta::launch_attend_bwd(pr, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma,
                                              workspace, dev_status, stream));
-}
-
-ZETA_API zeta_status_t zeta_attend_bwd_windows(const zeta_problem_t *p, const float *q,
-                                               const float *k, const void *v, const float *gamma,
-                                               const int32_t *prefix_idx, const int32_t *idx,
-                                               const void *dout, float *dq, float *dk, void *dv,
-                                               float *dgamma, void *workspace, size_t ws_bytes,
-                                               int32_t *dev_status, cudaStream_t stream) {
-    Prob pr;
-    zeta_status_t s = check_problem(p, &pr);
-    if (s != ZETA_OK) return s;
-    if (empty(pr)) {
-        if (pr.H > 0 && !dgamma) return ZETA_ERR_INVALID_ARG;
-        if (pr.H > 0) return from_cuda(cudaMemsetAsync(dgamma, 0, sizeof(float) * pr.H, stream));
-        return ZETA_OK;
-    }
-    if (!q || !k || !v || !gamma || !idx || !dout || !dq || !dk || !dv || !dgamma)
-        return ZETA_ERR_INVALID_ARG;
-    if (pr.T > 0 && !prefix_idx) return ZETA_ERR_INVALID_ARG;
-    if (!aligned16(v) || !aligned16(dout) || !aligned16(dv)) return ZETA_ERR_INVALID_ARG;
-    if (!workspace || ws_bytes < zeta::bwd_windows_ws_bytes(pr)) return ZETA_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ZETA_ERR_WORKSPACE;
-    return from_cuda(zeta::launch_attend_bwd_windows(pr, q, k, v, gamma, prefix_idx, idx, dout,
-                                                     dq, dk, dv, dgamma, workspace, dev_status,
-                                                     stream));
 }
 
 ZETA_API zeta_status_t zeta_check_bounded_wait(uint32_t iterations, int32_t arrive,

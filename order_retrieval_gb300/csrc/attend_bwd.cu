@@ -406,12 +406,8 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
         const uint32_t *sorted = static_cast<const uint32_t *>(w.rw.keys[ob]);
         csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(sorted, w.rw.seglen, L, p.N,
                                                               packed ? 16 : 0, w.off);
-        KeyLists lists;
-        lists.lst = packed ? sorted : w.rw.vals[ob];
-        lists.mask = packed ? 0xffffu : 0xffffffffu;
-        lists.off = w.off;
-        lists.stride = L;
-        e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, lists, false, dk, dv, st);
+        e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, packed ? sorted : w.rw.vals[ob],
+                              packed ? 0xffffu : 0xffffffffu, w.off, L, dk, dv, st);
         if (e != cudaSuccess) return e;
         dgamma_reduce(p, w, dgamma, st);
         return cudaGetLastError();
@@ -420,62 +416,6 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
         return bwd_dispatch<__nv_bfloat16>(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, ws,
                                            status, st);
     return bwd_dispatch<float>(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, ws, status, st);
-}
-
-// Workspace of the windows path: the query side's records and dgamma shares,
-// then the window lists (windows.cu).
-namespace {
-struct BwdWinWs {
-    float *dgp;
-    void *rec;
-    double *slice_sum;
-    WinLists wl;
-};
-BwdWinWs carve_bwd_win(const Prob &p, void *base, size_t *bytes) {
-    Carver cv(base);
-    BwdWinWs w;
-    w.dgp = cv.take<float>(p.S * p.N);
-    w.rec = cv.take<char>(bwd_tc_rec_bytes(p));
-    w.slice_sum = cv.take<double>(p.S);
-    char *lists = cv.take<char>(win_ws_bytes(p));
-    w.wl = carve_win(p, lists);
-    if (bytes) *bytes = cv.bytes();
-    return w;
-}
-}  // namespace
-
-bool bwd_windows_path(const Prob &p) { return attend_bwd_tc_supported(p) && win_lists_supported(p); }
-
-size_t bwd_windows_ws_bytes(const Prob &p) {
-    if (!bwd_windows_path(p)) return bwd_ws_bytes(p);
-    size_t b = 0;
-    carve_bwd_win(p, nullptr, &b);
-    return b;
-}
-
-cudaError_t launch_attend_bwd_windows(const Prob &p, const float *q, const float *k,
-                                      const void *v, const float *gamma,
-                                      const int32_t *prefix_idx, const int32_t *idx,
-                                      const void *dout, float *dq, float *dk, void *dv,
-                                      float *dgamma, void *ws, int32_t *status, cudaStream_t st) {
-    if (!bwd_windows_path(p))
-        return launch_attend_bwd(p, q, k, v, gamma, idx, dout, dq, dk, dv, dgamma, ws, status, st);
-    BwdWinWs w = carve_bwd_win(p, ws, nullptr);
-    cudaError_t e = launch_bwd_query_tc(p, q, k, v, gamma, idx, dout, dq, w.rec, w.dgp, status,
-                                        st);
-    if (e != cudaSuccess) return e;
-    e = launch_win_build(p, prefix_idx, idx, w.wl, status, st);
-    if (e != cudaSuccess) return e;
-    KeyLists lists;
-    lists.rw = w.wl.rw;
-    lists.ord = w.wl.ord;
-    lists.T = p.T;
-    lists.n = (int)p.n;
-    e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, lists, true, dk, dv, st);
-    if (e != cudaSuccess) return e;
-    dgamma_slices<<<(unsigned)p.S, 1024, 0, st>>>(w.dgp, p.N, w.slice_sum);
-    dgamma_heads<<<(unsigned)((p.H + 127) / 128), 128, 0, st>>>(w.slice_sum, p.B, p.H, dgamma);
-    return cudaGetLastError();
 }
 
 }  // namespace zeta

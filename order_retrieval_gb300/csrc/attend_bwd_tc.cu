@@ -634,89 +634,20 @@ constexpr size_t kKeyBig = sizeof(KOwn) > kKeyWarps * kRingBytes ? sizeof(KOwn)
 
 // The window walk's rings and the own-chunk tiles share `big` (the walk ends in
 // every warp before the tiles are staged); a warp's G scratch lives in its own
-// rows of dvp until its dv rows are written there.  kcnt: a warp's per-key
-// entry counts (window ranges only).
+// rows of dvp until its dv rows are written there.
 struct __align__(16) KSmem {
     unsigned char big[kKeyBig];
     float dvp[T64][DV + 4];
     float dkp[T64][4];
-    uint32_t kcnt[kKeyWarps][16];
-};
-
-// Entries of a range word (lo << 16) | len; a word that would reach past its
-// chunk (not written by a valid prefix table) counts as empty, so every read
-// stays inside the chunk's ordered queries.
-__device__ __forceinline__ uint32_t win_len(uint32_t wv, int C) {
-    const uint32_t len = wv & 0xffffu;
-    return (wv >> 16) + len <= (uint32_t)C ? len : 0u;
-}
-
-// The queries of one warp's keys read off the window ranges (windows.cu), as
-// one flat run: key by key, each key's later chunks in order, each range in
-// the order of ord.  Word q of the warp (q < NR = keys * nr) is key q / nr,
-// chunk c1 + q % nr, packing (lo << 16) | len: the queries ord[chunk * C + lo
-// .. + len).  Ranges are taken 32 at a time (one per lane, with their
-// inclusive scan); at(t) returns the query at flat position t of each lane,
-// for positions that never decrease from call to call.
-struct WinCursor {
-    const uint32_t *w;
-    const int32_t *ord;
-    int NR, nr, c1, C;
-    int rb;                                   // first range of the current batch
-    uint32_t base;                            // flat position of its first entry
-    uint32_t incl, excl, obase, tot;          // lane l: range rb + l; tot: the batch
-    __device__ void load(int lane) {
-        const int q = rb + lane;
-        uint32_t len = 0, ob = 0;
-        if (q < NR) {
-            const uint32_t wv = __ldg(w + q);
-            len = win_len(wv, C);
-            const int kr = q / nr;
-            ob = (uint32_t)(c1 + (q - kr * nr)) * (uint32_t)C + (wv >> 16);
-        }
-        uint32_t s = len;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(kFull, s, o);
-            if (lane >= o) s += y;
-        }
-        incl = s;
-        excl = s - len;
-        obase = ob;
-        tot = __shfl_sync(kFull, s, 31);
-    }
-    __device__ uint32_t at(uint32_t t, uint32_t total, int lane) {
-        uint32_t res = 0xffffffffu;
-        bool done = t >= total;
-        while (true) {
-            const bool in = !done && t >= base && t - base < tot;
-            const uint32_t rel = in ? t - base : 0u;
-            int l = 0;                                // ranges of the batch ending at or before rel
-#pragma unroll
-            for (int st = 16; st > 0; st >>= 1)
-                if (__shfl_sync(kFull, incl, l + st - 1) <= rel) l += st;
-            const uint32_t e = __shfl_sync(kFull, excl, l);
-            const uint32_t o = __shfl_sync(kFull, obase, l);
-            if (in) {
-                res = (uint32_t)__ldg(ord + o + (rel - e));
-                done = true;
-            }
-            if (!__any_sync(kFull, !done)) break;
-            rb += 32;
-            base += tot;
-            if (rb >= NR) break;                      // no range left (not reached when
-            load(lane);                               // total is the sum of the lengths)
-        }
-        return res;
-    }
 };
 static_assert(32 * kGs <= 16 * (DV + 4), "G scratch fits in a warp's dvp rows");
 
-template <int DK, int WK, bool WIN>
+template <int DK, int WK>
 __global__ void __launch_bounds__(THREADS, 4)
 bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
            const float *__restrict__ gamma, const __nv_bfloat16 *__restrict__ dout,
-           const QRec *__restrict__ rec, KeyLists lists, float *__restrict__ dk,
+           const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q, uint32_t csr_mask,
+           const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
            __nv_bfloat16 *__restrict__ dv, int N, int H, int C, int tiles_per_chunk) {
     extern __shared__ __align__(16) unsigned char key_smem[];
     KSmem &sm = *reinterpret_cast<KSmem *>(key_smem);
@@ -761,52 +692,14 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     // 16-entry tile belongs to is skipped.  The dk terms are summed per key by a
     // segmented scan over the step (entries of one key are adjacent), in the
     // order of the list.
+    const uint32_t *lst = csr_q + seg * csr_stride;
+    const uint32_t *ob = off + seg * (int64_t)(N + 1);
     constexpr uint32_t kNone = 0xffffffffu;
     const int wj0 = j0 + warp * 16;
     const int nkw = max(0, min(16, jend - wj0));
     // lane r < nkw: start of key r's list; lane nkw: end of the last list;
     // other lanes: a bound that no list position reaches
-    uint32_t bnd;
-    WinCursor cur;
-    const uint32_t *lst = nullptr;
-    if constexpr (WIN) {
-        // the warp's range words are adjacent: key wj0's first, then the next keys'
-        const int64_t nm1 = lists.n - 1;
-        const int nr = (int)(nm1 - c);
-        const int NR = nkw * nr;
-        const uint32_t *wp = lists.rw + seg * lists.T +
-                             (int64_t)C * (c * nm1 - (int64_t)c * (c - 1) / 2) +
-                             (int64_t)(wj0 - cC) * nr;
-        uint32_t *kcount = sm.kcnt[warp];                // entries per key of the warp
-        if (lane < 16) kcount[lane] = 0u;
-        __syncwarp();
-        for (int q0 = 0; q0 < NR; q0 += 32) {
-            const int q = q0 + lane;
-            if (q < NR) atomicAdd(&kcount[q / nr], win_len(__ldg(wp + q), C));
-        }
-        __syncwarp();
-        const uint32_t tk = lane < nkw ? kcount[lane] : 0u;
-        uint32_t sc = tk;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(kFull, sc, o);
-            if (lane >= o) sc += y;
-        }
-        bnd = lane <= nkw ? sc - tk : kNone;
-        cur.w = wp;
-        cur.ord = lists.ord + seg * (int64_t)N;
-        cur.NR = NR;
-        cur.nr = nr;
-        cur.c1 = c + 1;
-        cur.C = C;
-        cur.rb = 0;
-        cur.base = 0;
-        cur.load(lane);
-    } else {
-        lst = lists.lst + seg * lists.stride;
-        const uint32_t *ob = lists.off + seg * (int64_t)(N + 1);
-        bnd = (nkw > 0 && lane <= nkw) ? ob[wj0 + lane] : kNone;
-    }
+    const uint32_t bnd = (nkw > 0 && lane <= nkw) ? ob[wj0 + lane] : kNone;
     const uint32_t bnd_hi = __shfl_sync(kFull, bnd, (lane + 1) & 31);   // lane r: end of key r's list
     const uint32_t P0 = __shfl_sync(kFull, bnd, 0);
     const uint32_t P1 = __shfl_sync(kFull, bnd, nkw);
@@ -840,10 +733,9 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     float dkacc[4] = {0.f, 0.f, 0.f, 0.f};                    // lane r: dk of key r
     const uint32_t ring = smem_u32(sm.big) + (uint32_t)warp * kRingBytes;
     float *gs = &sm.dvp[warp * 16][0];                        // G scratch: [32 entries][kGs]
-    auto list_at = [&](int n) -> uint32_t {              // called for n = 0, 1, 2, ...
+    auto list_at = [&](int n) -> uint32_t {
         const uint32_t pp = P0 + 32u * (uint32_t)n + (uint32_t)lane;
-        if constexpr (WIN) return n < nch ? cur.at(pp, P1, lane) : kNone;
-        else return (n < nch && pp < P1) ? (__ldg(lst + pp) & lists.mask) : kNone;
+        return (n < nch && pp < P1) ? (__ldg(lst + pp) & csr_mask) : kNone;
     };
     auto issue = [&](int n, uint32_t ie) {                    // dO rows of step n
         const uint32_t slot = ring + (uint32_t)(n & 1) * (kRingBytes / 2);
@@ -1222,51 +1114,39 @@ cudaError_t bwd_query_tc_dk(const Prob &p, dim3 grid, int tpc, const float *q, c
     }
 }
 
-template <int D, int WK, bool WIN>
+template <int D, int WK>
 cudaError_t bwd_key_tc_launch(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
                               const float *gamma, const void *dout, const void *rec,
-                              const KeyLists &lists, float *dk, void *dv, cudaStream_t st) {
+                              const uint32_t *csr_q, uint32_t csr_mask, const uint32_t *off,
+                              int64_t csr_stride, float *dk, void *dv, cudaStream_t st) {
     static PerDeviceOnce smem_once;          // run once per device, outside any capture
     const cudaError_t e = smem_once.run([] {
-        return cudaFuncSetAttribute(bwd_key_tc<D, WK, WIN>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(bwd_key_tc<D, WK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)sizeof(KSmem));
     });
     if (e != cudaSuccess) return e;
-    bwd_key_tc<D, WK, WIN><<<grid, THREADS, sizeof(KSmem), st>>>(
+    bwd_key_tc<D, WK><<<grid, THREADS, sizeof(KSmem), st>>>(
         k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout),
-        static_cast<const QRec *>(rec), lists, dk, static_cast<__nv_bfloat16 *>(dv), p.N, p.H,
-        p.C, tpc);
+        static_cast<const QRec *>(rec), csr_q, csr_mask, off, csr_stride, dk,
+        static_cast<__nv_bfloat16 *>(dv), p.N, p.H, p.C, tpc);
     return cudaGetLastError();
 }
 
-template <int WK, bool WIN>
+template <int WK>
 cudaError_t bwd_key_tc_dk(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
                           const float *gamma, const void *dout, const void *rec,
-                          const KeyLists &lists, float *dk, void *dv, cudaStream_t st) {
+                          const uint32_t *csr_q, uint32_t csr_mask, const uint32_t *off,
+                          int64_t csr_stride, float *dk, void *dv, cudaStream_t st) {
     switch (p.dK) {
-        case 1: return bwd_key_tc_launch<1, WK, WIN>(p, grid, tpc, k, v, gamma, dout, rec, lists,
-                                                     dk, dv, st);
-        case 2: return bwd_key_tc_launch<2, WK, WIN>(p, grid, tpc, k, v, gamma, dout, rec, lists,
-                                                     dk, dv, st);
-        case 3: return bwd_key_tc_launch<3, WK, WIN>(p, grid, tpc, k, v, gamma, dout, rec, lists,
-                                                     dk, dv, st);
-        default: return bwd_key_tc_launch<4, WK, WIN>(p, grid, tpc, k, v, gamma, dout, rec, lists,
-                                                      dk, dv, st);
+        case 1: return bwd_key_tc_launch<1, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+                                                csr_mask, off, csr_stride, dk, dv, st);
+        case 2: return bwd_key_tc_launch<2, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+                                                csr_mask, off, csr_stride, dk, dv, st);
+        case 3: return bwd_key_tc_launch<3, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+                                                csr_mask, off, csr_stride, dk, dv, st);
+        default: return bwd_key_tc_launch<4, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+                                                 csr_mask, off, csr_stride, dk, dv, st);
     }
-}
-
-template <bool WIN>
-cudaError_t bwd_key_tc_wk(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
-                          const float *gamma, const void *dout, const void *rec,
-                          const KeyLists &lists, float *dk, void *dv, cudaStream_t st) {
-    if (p.wk == kWSoftmax)
-        return bwd_key_tc_dk<kWSoftmax, WIN>(p, grid, tpc, k, v, gamma, dout, rec, lists, dk, dv,
-                                             st);
-    if (p.wk == kWInvEuclid)
-        return bwd_key_tc_dk<kWInvEuclid, WIN>(p, grid, tpc, k, v, gamma, dout, rec, lists, dk,
-                                               dv, st);
-    return bwd_key_tc_dk<kWCauchy, WIN>(p, grid, tpc, k, v, gamma, dout, rec, lists, dk, dv, st);
 }
 
 cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, const void *v,
@@ -1286,13 +1166,19 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
 }
 
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
-                              const void *dout, const void *rec, const KeyLists &lists,
-                              bool windows, float *dk, void *dv, cudaStream_t st) {
+                              const void *dout, const void *rec, const uint32_t *csr_q,
+                              uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
+                              float *dk, void *dv, cudaStream_t st) {
     const int tpc = (p.C + T64 - 1) / T64;
     const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
-    if (windows)
-        return bwd_key_tc_wk<true>(p, grid, tpc, k, v, gamma, dout, rec, lists, dk, dv, st);
-    return bwd_key_tc_wk<false>(p, grid, tpc, k, v, gamma, dout, rec, lists, dk, dv, st);
+    if (p.wk == kWSoftmax)
+        return bwd_key_tc_dk<kWSoftmax>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask,
+                                        off, csr_stride, dk, dv, st);
+    if (p.wk == kWInvEuclid)
+        return bwd_key_tc_dk<kWInvEuclid>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask,
+                                          off, csr_stride, dk, dv, st);
+    return bwd_key_tc_dk<kWCauchy>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
+                                   csr_stride, dk, dv, st);
 }
 
 }  // namespace zeta

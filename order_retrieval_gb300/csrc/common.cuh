@@ -162,53 +162,17 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
                                 const float *gamma, const int32_t *idx, const void *dout,
                                 float *dq, void *rec, float *dg_part, int32_t *status,
                                 cudaStream_t st);
-// Where the key kernel finds the queries that selected each key: the lists of
-// a sorted transpose of idx (lst masked with mask, key j's list starting at
-// off[j], slices stride apart), or the window ranges of windows.cu (range
-// words rw, T per slice; ordered queries ord, N per slice; n chunks).
-struct KeyLists {
-    const uint32_t *lst = nullptr;
-    uint32_t mask = 0;
-    const uint32_t *off = nullptr;
-    int64_t stride = 0;
-    const uint32_t *rw = nullptr;
-    const int32_t *ord = nullptr;
-    int64_t T = 0;
-    int n = 0;
-};
+// csr_q holds the queries of every key's list (masked with csr_mask).
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
-                              const void *dout, const void *rec, const KeyLists &lists,
-                              bool windows, float *dk, void *dv, cudaStream_t st);
-
-// The key side's lists read off contiguous windows (windows.cu): per slice the
-// inverse of every prefix permutation, the queries of each chunk ordered by
-// window start, and every (key, later chunk) pair's range of that order.
-constexpr int kWinMaxC = 4096;
-struct WinLists {
-    int32_t *inv;
-    int32_t *ord;
-    uint32_t *rw;
-};
-bool win_lists_supported(const Prob &p);
-size_t win_ws_bytes(const Prob &p);
-WinLists carve_win(const Prob &p, void *base);
-cudaError_t launch_win_build(const Prob &p, const int32_t *prefix_idx, const int32_t *idx,
-                             const WinLists &w, int32_t *status, cudaStream_t st);
+                              const void *dout, const void *rec, const uint32_t *csr_q,
+                              uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
+                              float *dk, void *dv, cudaStream_t st);
 
 size_t bwd_ws_bytes(const Prob &p);
 cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, const void *v,
                               const float *gamma, const int32_t *idx, const void *dout, float *dq,
                               float *dk, void *dv, float *dgamma, void *ws, int32_t *status,
                               cudaStream_t st);
-// The backward for idx rows that are windows of prefix_idx (the tensor-core
-// shapes with C <= kWinMaxC; other problems take launch_attend_bwd).
-bool bwd_windows_path(const Prob &p);
-size_t bwd_windows_ws_bytes(const Prob &p);
-cudaError_t launch_attend_bwd_windows(const Prob &p, const float *q, const float *k,
-                                      const void *v, const float *gamma,
-                                      const int32_t *prefix_idx, const int32_t *idx,
-                                      const void *dout, float *dq, float *dk, void *dv,
-                                      float *dgamma, void *ws, int32_t *status, cudaStream_t st);
 
 // Segmented stable LSD radix sort of (key, value) pairs, 8-bit digits.
 // Slices of `len` items each, laid out `stride` apart.

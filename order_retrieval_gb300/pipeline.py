@@ -55,12 +55,8 @@ class ZetaPlan:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.has_bwd = backward
         if backward:
-            # one curve: the rows are windows of the prefix table, and the key
-            # side reads its lists off them (zeta_attend_bwd_windows); the union
-            # of several curves takes the general call (a sorted transpose)
-            ws = (zb.zeta_bwd_windows_workspace_bytes(p) if curves == 1
-                  else zb.zeta_bwd_workspace_bytes(p))
-            self.bwd_ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+            self.bwd_ws = torch.empty(max(zb.zeta_bwd_workspace_bytes(p), 256),
+                                      dtype=torch.uint8, device=dev)
             self.dq = torch.empty(S * N * p.d_K, dtype=torch.float32, device=dev)
             self.dk = torch.empty(S * N * p.d_K, dtype=torch.float32, device=dev)
             self.dv = torch.empty(S * N * p.d_V, dtype=vdt, device=dev)
@@ -95,13 +91,8 @@ class ZetaPlan:
     def backward(self, q, k, v, gamma, dout, stream=None):
         """Gradients for the last forward.  Returns (dq, dk, dv, dgamma) views."""
         p = self.p
-        if self.curves == 1:
-            zb.zeta_attend_bwd_windows(p, q, k, v, gamma, self.prefix_idx, self.idx, dout,
-                                       self.dq, self.dk, self.dv, self.dgamma, self.bwd_ws,
-                                       self.status, stream)
-        else:
-            zb.zeta_attend_bwd(p, q, k, v, gamma, self.idx, dout, self.dq, self.dk, self.dv,
-                               self.dgamma, self.bwd_ws, self.status, stream)
+        zb.zeta_attend_bwd(p, q, k, v, gamma, self.idx, dout, self.dq, self.dk, self.dv,
+                           self.dgamma, self.bwd_ws, self.status, stream)
         return self.dq, self.dk, self.dv, self.dgamma
 
 

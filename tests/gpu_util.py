@@ -86,28 +86,6 @@ class Run:
                 self.plan.dk.view(self.S, self.N, w.d_K)[s].cpu().numpy().astype(np.float64),
                 host_vals(self.plan.dv.view(self.S, self.N, w.d_V)[s]))
 
-    def transpose_bwd(self):
-        """The general backward (zeta_attend_bwd, whose key side sorts a
-        transpose of idx) on this run's inputs and selection, into fresh
-        buffers; returns (dq, dk, dv, dgamma) as float64 numpy, [S, ...]."""
-        w, p = self.w, self.p
-        S, N = self.S, self.N
-        vt = zb.v_torch_dtype(p)
-        dq = torch.empty(S * N * w.d_K, dtype=torch.float32, device="cuda")
-        dk = torch.empty_like(dq)
-        dv = torch.empty(S * N * w.d_V, dtype=vt, device="cuda")
-        dg = torch.empty(w.H, dtype=torch.float32, device="cuda")
-        ws = torch.empty(max(zb.zeta_bwd_workspace_bytes(p), 256), dtype=torch.uint8,
-                         device="cuda")
-        st = torch.zeros(1, dtype=torch.int32, device="cuda")
-        zb.zeta_attend_bwd(p, self.q, self.k, self.v, self.gamma, self.plan.idx, self.dout, dq,
-                           dk, dv, dg, ws, st)
-        torch.cuda.synchronize()
-        assert int(st.item()) == 0
-        return (dq.cpu().numpy().astype(np.float64).reshape(S, N, w.d_K),
-                dk.cpu().numpy().astype(np.float64).reshape(S, N, w.d_K),
-                host_vals(dv).reshape(S, N, w.d_V), dg.cpu().numpy().astype(np.float64))
-
     def grads(self):
         w = self.w
         return (self.plan.dq.cpu().numpy().astype(np.float64).reshape(self.S, self.N, w.d_K),
