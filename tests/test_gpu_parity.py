@@ -273,6 +273,35 @@ def test_backward_beyond_float_slot_division():
     assert_close_bf16(run.grads()[3], _dgamma_ref(run), what="dgamma")
 
 
+def test_backward_train_one_batch_bf16():
+    """One batch of the training workload (H=8, N=65536, k=48, C=1024; about
+    1 GB on the device): slices 0 and 7 whole and the gamma gradient of every
+    head against the oracle."""
+    w = W.TRAIN.replace(name="train_bf16_b1_n65536", B=1)
+    run = Run(w, backward=True)
+    assert run.status() == 0
+    refs = {}
+
+    def one(s):
+        q, k, v, gamma, dout = slice_inputs(w, run.g, s)
+        ref = oracle.select(oracle.encode(q, w.bits)[None], oracle.encode(k, w.bits)[None],
+                            w.C, w.k)[0]
+        return ref, oracle.attend_bwd(q, k, v, gamma, ref, dout, w.C)
+
+    res = in_threads(one, range(run.S))
+    dev_idx = run.idx()
+    for s, (ref_idx, r) in enumerate(res):
+        assert np.array_equal(dev_idx[s], ref_idx)
+        refs[s] = r
+    for s in (0, 7):
+        dq, dk, dv = run.grads_slice(s)
+        assert_close_bf16(dq, refs[s][0], what="dq")
+        assert_close_bf16(dk, refs[s][1], what="dk")
+        assert_close_bf16(dv, refs[s][2], what="dv")
+    dg = run.plan.dgamma.cpu().numpy().astype(np.float64)
+    assert_close_bf16(dg, np.array([refs[s][3] for s in range(run.S)]), what="dgamma")
+
+
 def test_backward_beyond_16bit_sequence_bf16():
     """N = 131072 (> 2^16) takes the unpacked (key, query) transpose in the
     tensor-core backward; one slice against the oracle."""
