@@ -158,17 +158,45 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
             const int nr = max(0, min(16, iend - wq0));
             for (int r = 0; r < nr; ++r)
                 for (int t = lane; t < k; t += 32) sel.idx_out[(seg * N + wq0 + r) * (int64_t)k + t] = -1;
-        } else if (lane < nqw) {    // every lane's search runs over cC keys: same trip count
+        } else {
+            // Upper bound of each query's code in its prefix (the number of keys
+            // with code <= the query's), in two levels: the first code of every
+            // block of 2^fsh prefix entries (a fence) is staged in shared memory
+            // (the window partials' space, unused until the first query is done)
+            // and searched there; the query's block is then searched in global
+            // memory, where its probes after the first hit L1.  Same result as
+            // one binary search over the prefix, with far fewer dependent loads
+            // from L2 before the first gather.
             const K *pc = sel.pcodes + seg * sel.T + (int64_t)C * c * (c - 1) / 2;
-            const K x = sel.qcodes[seg * N + wq0 + lane];
-            int lo = 0, hi = cC;    // upper bound: keys with code <= the query's
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (pc[mid] <= x) lo = mid + 1; else hi = mid;
+            K *fence = reinterpret_cast<K *>(&sm.win[0][0]);
+            constexpr int kFenceMax = (int)(sizeof(sm.win) / sizeof(K));
+            int fsh = 6;
+            while ((cC >> fsh) >= kFenceMax) ++fsh;
+            const int nf = (cC + (1 << fsh) - 1) >> fsh;
+            for (int f = threadIdx.x; f < nf; f += THREADS) fence[f] = pc[(int64_t)f << fsh];
+            __syncthreads();
+            if (lane < nqw) {
+                const K x = sel.qcodes[seg * N + wq0 + lane];
+                int lo = 0, hi = nf;           // fences with code <= x
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (fence[mid] <= x) lo = mid + 1; else hi = mid;
+                }
+                int r = 0;
+                if (lo > 0) {                  // entry b0 (the fence) is <= x; later blocks are > x
+                    const int b0 = (lo - 1) << fsh;
+                    int a = b0 + 1, b = min(cC, b0 + (1 << fsh));
+                    while (a < b) {
+                        const int mid = (a + b) >> 1;
+                        if (pc[mid] <= x) a = mid + 1; else b = mid;
+                    }
+                    r = a;
+                }
+                int s0 = r - (k + 1) / 2;
+                s0 = s0 > cC - k ? cC - k : s0;
+                wstart = s0 < 0 ? 0 : s0;
             }
-            int s0 = lo - (k + 1) / 2;
-            s0 = s0 > cC - k ? cC - k : s0;
-            wstart = s0 < 0 ? 0 : s0;
+            __syncthreads();                   // fences read before any window partial is written
         }
     }
     auto load_idx = [&](int i, int t0, int (&j)[2]) {

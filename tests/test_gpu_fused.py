@@ -93,3 +93,16 @@ def test_efficiency_scale_full_slice(w):
     rng = np.random.default_rng(5)
     rows = np.sort(np.concatenate([rng.choice(w.N, 40, replace=False), [0, w.C, w.N - 1]]))
     _run(w, rows=rows, slices=(0,), full=(5,))
+
+
+@pytest.mark.parametrize("kw", [dict(N=262144, C=1024, bits=12), dict(N=524288, C=2048, bits=10)],
+                         ids=["n262144-u64", "n524288-u32"])
+def test_long_prefixes(kw):
+    """Prefixes long enough that the fused call's first-level table holds the
+    first code of every 128 or more entries (64-bit codes at N = 262,144,
+    32-bit codes at N = 524,288): every row equal to the two-call path, rows of
+    three chunks against the oracle."""
+    w = W.EFFICIENCY.replace(name="fused_long", H=1, k=64, **kw)
+    n = w.N // w.C
+    rows = np.concatenate([np.arange(c * w.C, c * w.C + 24) for c in (1, n // 2, n - 1)])
+    _run(w, rows=rows, slices=(0,))
