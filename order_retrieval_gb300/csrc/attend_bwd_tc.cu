@@ -617,11 +617,15 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
 
 // ============================================================== key side ===
 
-// Tiles of the own-chunk part.
+// Tiles of the own-chunk part.  A query tile's records are staged 48 bytes
+// apart (the 32-byte record and 16 bytes of padding): the four records a
+// quarter-warp reads at once then start in four different bank groups, where a
+// 32- or 64-byte stride puts two of them on the same banks.
+constexpr int kRecPad = 3;                        // float4 slots per staged record
 struct __align__(16) KOwn {
     __nv_bfloat16 v[T64 * DV];
     __nv_bfloat16 dO[2][T64 * DV];
-    QRec qr[2][T64];
+    float4 qr[2][T64][kRecPad];
 };
 constexpr int kKeyWarps = THREADS / 32;
 constexpr uint32_t kRingBytes = 2 * 32 * DV * 2;   // one warp's two slots of 32 dO rows
@@ -672,7 +676,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             const int r = threadIdx.x >> 1, h = threadIdx.x & 1;
             const int i = iq0 + r;
             const bool ok = i < cend;
-            cp_async16(smem_u32(reinterpret_cast<float4 *>(&own.qr[b][r]) + h),
+            cp_async16(smem_u32(&own.qr[b][r][h]),
                        reinterpret_cast<const float4 *>(rb_ + (ok ? i : iq0)) + h, ok ? 16 : 0);
         }
     };
@@ -939,7 +943,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     uint32_t va[4][4];
     auto qtile = [&](int t, int iq0, auto masked) {
         const uint32_t dbase = smem_u32(own.dO[t & 1]);
-        const QRec *qt_rec = own.qr[t & 1];
+        const float4 (*qt_rec)[kRecPad] = own.qr[t & 1];
         // per 16 queries: S^T = V . dO^T (16 keys x 16 queries), the element-wise
         // terms for key rows (a, b) packed, P^T into A fragments, then
         // dV += P^T . dO with the same dO fragments transposed in registers
@@ -967,7 +971,9 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int ql = nt * 8 + 2 * tig + e;
-                    const QRec qrc = qt_rec[ql];
+                    QRec qrc;
+                    qrc.q = qt_rec[ql][0];
+                    qrc.sg = qt_rec[ql][1];
                     const float qc[4] = {qrc.q.x, qrc.q.y, qrc.q.z, qrc.q.w};
                     const float2 inv_s = dup2(qrc.sg.x), ngbs = dup2(qrc.sg.w);
                     const float2 mq = dup2(qrc.sg.z);
