@@ -62,6 +62,12 @@ struct FusedSel {
     int64_t T;
 };
 
+// Column of window-partial dimension d: the eight lanes that store one query's
+// sums write dimensions {0, 1, 16, 17, 32, 33, 48, 49} + 2 cb at once, which
+// fall on four banks twice; flipping bit 1 in the upper half (d ^ 2 for
+// d >= 32) spreads them over eight.  Adjacent even/odd dimensions stay adjacent.
+__device__ __forceinline__ int wcol(int d) { return d ^ ((d >> 5) << 1); }
+
 struct __align__(16) FwdSmem {
     __nv_bfloat16 v[2][TK * DV];  // swizzled: 16-byte chunk c of row r at c ^ (r & 7)
     float4 kt[2][TK];
@@ -320,8 +326,8 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
             const int d0 = 16 * (g4 >> 1) + (g4 & 1);
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
-                sm.win[row][d0 + 2 * cb] = cacc[cb][0];
-                sm.win[row][d0 + 8 + 2 * cb] = cacc[cb][2];
+                sm.win[row][wcol(d0 + 2 * cb)] = cacc[cb][0];
+                sm.win[row][wcol(d0 + 8 + 2 * cb)] = cacc[cb][2];
             }
         }
         if (lane == 0) {
@@ -476,14 +482,14 @@ attend_fwd_tc(const float *__restrict__ q, const float *__restrict__ kx,
     for (int nt = 0; nt < 8; ++nt) {
         const int col = nt * 8 + 2 * tig;
         if (ra < iend) {
-            const float o0 = __fmaf_rn(sm.win[rowa][col], fa, acc[nt][0]) * ia;
-            const float o1 = __fmaf_rn(sm.win[rowa][col + 1], fa, acc[nt][1]) * ia;
+            const float o0 = __fmaf_rn(sm.win[rowa][wcol(col)], fa, acc[nt][0]) * ia;
+            const float o1 = __fmaf_rn(sm.win[rowa][wcol(col) + 1], fa, acc[nt][1]) * ia;
             *reinterpret_cast<__nv_bfloat162 *>(out + (seg * N + ra) * (int64_t)DV + col) =
                 __floats2bfloat162_rn(o0, o1);
         }
         if (rb < iend) {
-            const float o0 = __fmaf_rn(sm.win[rowb][col], fb, acc[nt][2]) * ib;
-            const float o1 = __fmaf_rn(sm.win[rowb][col + 1], fb, acc[nt][3]) * ib;
+            const float o0 = __fmaf_rn(sm.win[rowb][wcol(col)], fb, acc[nt][2]) * ib;
+            const float o1 = __fmaf_rn(sm.win[rowb][wcol(col) + 1], fb, acc[nt][3]) * ib;
             *reinterpret_cast<__nv_bfloat162 *>(out + (seg * N + rb) * (int64_t)DV + col) =
                 __floats2bfloat162_rn(o0, o1);
         }
