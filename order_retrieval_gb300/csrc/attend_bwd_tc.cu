@@ -44,9 +44,10 @@ constexpr int T64 = 64;           // rows per CTA tile (queries or keys)
 constexpr int DV = 64;
 constexpr int THREADS = 128;
 
-// Per-query record for the key side: q (padded to 4), then {1/s, gbar, m,
-// -gbar/s} (m: the softmax shift; 0 for the other weight kernels), so that
-// dL/dw_ij = g_ij / s - gbar / s is one fma.
+// Per-query record for the key side: q (padded to 4), then {1/s, -gbar/s, m,
+// gbar} (m: the softmax shift; 0 for the other weight kernels), so that
+// dL/dw_ij = g_ij / s - gbar / s is one fma and the two scalars it needs are
+// adjacent (one 8-byte load).
 struct __align__(16) QRec {
     float4 q;
     float4 sg;
@@ -609,7 +610,7 @@ bwd_query_tc(const float *__restrict__ q, const float *__restrict__ kx,
             const float *qq = tig == 0 ? qa : qbv;
             QRec rcd;
             rcd.q = make_float4(qq[0], qq[1], qq[2], qq[3]);
-            rcd.sg = make_float4(inv_s, gb, WK == kWSoftmax ? mfin : 0.f, -gb * inv_s);
+            rcd.sg = make_float4(inv_s, -gb * inv_s, WK == kWSoftmax ? mfin : 0.f, gb);
             rec[gi] = rcd;
         }
     }
@@ -803,7 +804,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             }
             const float w = weight_fast<WK>(d2, rq1.z, inv_g2);
             inv_s = rq1.x;
-            ngbs = rq1.w;
+            ngbs = rq1.y;
             a = w * inv_s;
             // Cauchy: 2 w^2 / gamma^2 with the constant applied to dk at the end
             s2 = WK == kWCauchy ? w * w : 2.f * neg_dw_dd2<WK>(w, inv_g2);
@@ -971,12 +972,19 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int ql = nt * 8 + 2 * tig + e;
-                    QRec qrc;
-                    qrc.q = qt_rec[ql][0];
-                    qrc.sg = qt_rec[ql][1];
-                    const float qc[4] = {qrc.q.x, qrc.q.y, qrc.q.z, qrc.q.w};
-                    const float2 inv_s = dup2(qrc.sg.x), ngbs = dup2(qrc.sg.w);
-                    const float2 mq = dup2(qrc.sg.z);
+                    const float4 qv = qt_rec[ql][0];
+                    const float qc[4] = {qv.x, qv.y, qv.z, qv.w};
+                    float2 sgv;                    // (1/s, -gbar/s)
+                    float mz = 0.f;                // softmax shift
+                    if constexpr (WK == kWSoftmax) {
+                        const float4 t4 = qt_rec[ql][1];
+                        sgv = make_float2(t4.x, t4.y);
+                        mz = t4.z;
+                    } else {
+                        sgv = *reinterpret_cast<const float2 *>(&qt_rec[ql][1]);
+                    }
+                    const float2 inv_s = dup2(sgv.x), ngbs = dup2(sgv.y);
+                    const float2 mq = dup2(mz);
                     float2 dqk[4];
                     float2 d2 = make_float2(0.f, 0.f);
 #pragma unroll
