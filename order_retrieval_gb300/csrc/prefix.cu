@@ -19,8 +19,13 @@
 //           each warp store writes a contiguous run of prefix c.
 // Reads are one pass over the sorted slice; writes are the table itself.
 //
-// Select.  One lane binary-searches one query (upper bound of its code in its
-// chunk's prefix), then the warp copies the 32 windows with coalesced loads.
+// Select.  One lane finds one query's upper bound (of its code in its chunk's
+// prefix), then the warp copies the 32 windows with coalesced loads.  When a
+// block's 256 queries lie in one chunk (C a multiple of 256), the search runs
+// in two levels: the first code of every block of 2^fsh prefix entries is
+// staged in shared memory and searched there, then the query's block in global
+// memory (its probes after the first hit L1); otherwise one binary search over
+// the prefix.  Both give the same upper bound.
 #include "common.cuh"
 
 namespace zeta {
@@ -179,14 +184,63 @@ prefix_scatter(const K *__restrict__ skey, const uint32_t *__restrict__ sidx, in
     }
 }
 
+constexpr int kSelThreads = 256;
+constexpr int kSelFence = 2048;                            // fences per block, at most
+
 template <typename K>
-__global__ void select_kernel(const K *__restrict__ qc, const K *__restrict__ pc,
-                              const int32_t *__restrict__ pidx, int32_t *__restrict__ out,
-                              int64_t S, int N, int C, int k, int64_t T) {
+__global__ void __launch_bounds__(kSelThreads)
+select_kernel(const K *__restrict__ qc, const K *__restrict__ pc,
+              const int32_t *__restrict__ pidx, int32_t *__restrict__ out, int64_t S, int N,
+              int C, int k, int64_t T, int fenced) {
+    __shared__ K fence[kSelFence];
     const int64_t wpr = (N + 31) / 32;                    // warps per slice
     const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-    if (gw >= S * wpr) return;                            // whole warp exits together
     const int lane = threadIdx.x & 31;
+    if (fenced) {
+        // all 256 queries of this block are in one chunk c (C % 256 == 0, N % 256 == 0)
+        const int64_t gb = blockIdx.x * (int64_t)(kSelThreads / 32);
+        const int64_t seg = gb / wpr;
+        const int c = (int)((gb % wpr) * 32 / C);
+        if (c >= 1) {
+            const int M = c * C;
+            const K *p = pc + seg * T + (int64_t)C * c * (c - 1) / 2;
+            int fsh = 6;
+            while ((M >> fsh) >= kSelFence) ++fsh;
+            const int nf = (M + (1 << fsh) - 1) >> fsh;
+            for (int f = threadIdx.x; f < nf; f += kSelThreads) fence[f] = p[(int64_t)f << fsh];
+            __syncthreads();
+            const int qb = (int)(gw % wpr) * 32;
+            const K x = qc[seg * N + qb + lane];
+            int lo = 0, hi = nf;                           // fences with code <= x
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (fence[mid] <= x) lo = mid + 1; else hi = mid;
+            }
+            int r = 0;
+            if (lo > 0) {                                  // entry b0 <= x; later blocks > x
+                const int b0 = (lo - 1) << fsh;
+                int a = b0 + 1, b = min(M, b0 + (1 << fsh));
+                while (a < b) {
+                    const int mid = (a + b) >> 1;
+                    if (p[mid] <= x) a = mid + 1; else b = mid;
+                }
+                r = a;
+            }
+            int start = r - (k + 1) / 2;
+            start = start < 0 ? 0 : start;
+            start = start > M - k ? M - k : start;
+            // the warp copies its 32 windows
+            const int32_t *pi = pidx + seg * T + (int64_t)C * c * (c - 1) / 2;
+            for (int qq = 0; qq < 32; ++qq) {
+                const int s = __shfl_sync(kFull, start, qq);
+                int32_t *o = out + (seg * N + qb + qq) * (int64_t)k;
+                for (int t = lane; t < k; t += 32) o[t] = pi[s + t];
+            }
+            return;
+        }
+        // chunk 0: falls through to the plain path (every row is -1)
+    }
+    if (gw >= S * wpr) return;                            // whole warp exits together
     const int64_t seg = gw / wpr;
     const int qb = (int)(gw % wpr) * 32;
     const int i = qb + lane;
@@ -277,16 +331,18 @@ cudaError_t launch_sort_chunks(const Prob &p, const void *key_codes, void *prefi
 cudaError_t launch_select(const Prob &p, const void *q_codes, const void *prefix_codes,
                           const int32_t *prefix_idx, int32_t *idx, cudaStream_t st) {
     const int64_t warps = p.S * ((p.N + 31) / 32);
-    const int threads = 256;
+    const int threads = kSelThreads;
     const int64_t blocks = (warps * 32 + threads - 1) / threads;
+    // every block's 256 queries in one chunk of one slice: the two-level search
+    const int fenced = (p.C % kSelThreads == 0 && p.N % kSelThreads == 0) ? 1 : 0;
     if (p.code64)
         select_kernel<uint64_t><<<(unsigned)blocks, threads, 0, st>>>(
             static_cast<const uint64_t *>(q_codes), static_cast<const uint64_t *>(prefix_codes),
-            prefix_idx, idx, p.S, p.N, p.C, p.k, p.T);
+            prefix_idx, idx, p.S, p.N, p.C, p.k, p.T, fenced);
     else
         select_kernel<uint32_t><<<(unsigned)blocks, threads, 0, st>>>(
             static_cast<const uint32_t *>(q_codes), static_cast<const uint32_t *>(prefix_codes),
-            prefix_idx, idx, p.S, p.N, p.C, p.k, p.T);
+            prefix_idx, idx, p.S, p.N, p.C, p.k, p.T, fenced);
     return cudaGetLastError();
 }
 
