@@ -40,8 +40,8 @@ sys.path.insert(0, ROOT)
 # digest of the kernel's sources at that time.  The line reports the figure only
 # while the sources still have that digest (else null: the kernel has changed).
 ATTEND_FWD_TRAFFIC = {
-    "bytes": 212_310_784 + 50_391_552,
-    "sources_sha256": "6828ece66bfa9f6f23cf1883b1bd13288b4259d3f447a9698a52bb67d50f8de9",
+    "bytes": 211_953_664 + 50_646_784,
+    "sources_sha256": "bd492b803d552fe9889ffe938dfab0cd66b819dbd78a93397cfe8d1501909236",
     "capture": "attend_fwd_tc, efficiency_bf16_n65536, ncu --metrics "
                "dram__bytes_read.sum,dram__bytes_write.sum",
 }
@@ -432,14 +432,18 @@ def run_ours(args, w, rank, world):
     # --- end to end through the C ABI with host buffers (pinned): every step
     # copies its inputs host -> device, runs the five calls, and copies its
     # results device -> host.  Serial: one stream, step after step.  Pipelined
-    # (the e2e figure): two device buffer sets; step n+1's inputs go up on a copy
-    # stream while step n computes, and step n's results come down on another
-    # while step n+1 computes.  Both time every copy of every step.
-    out_h = [torch.empty(plan.out.numel(), dtype=plan.out.dtype).pin_memory() for _ in range(2)]
-    dq_h = [torch.empty(plan.dq.numel(), dtype=torch.float32).pin_memory() for _ in range(2)]
-    dk_h = [torch.empty(plan.dk.numel(), dtype=torch.float32).pin_memory() for _ in range(2)]
-    dv_h = [torch.empty(plan.dv.numel(), dtype=plan.dv.dtype).pin_memory() for _ in range(2)]
-    dg_h = [torch.empty(plan.dgamma.numel(), dtype=torch.float32).pin_memory() for _ in range(2)]
+    # (the e2e figure): NSETS device buffer sets; step n+1's inputs go up on a
+    # copy stream while step n computes, and step n's results come down on
+    # another while step n+1 computes, a set being reused only after its
+    # previous results are down.  Both time every copy of every step.
+    NSETS = 3
+    out_h = [torch.empty(plan.out.numel(), dtype=plan.out.dtype).pin_memory()
+             for _ in range(NSETS)]
+    dq_h = [torch.empty(plan.dq.numel(), dtype=torch.float32).pin_memory() for _ in range(NSETS)]
+    dk_h = [torch.empty(plan.dk.numel(), dtype=torch.float32).pin_memory() for _ in range(NSETS)]
+    dv_h = [torch.empty(plan.dv.numel(), dtype=plan.dv.dtype).pin_memory() for _ in range(NSETS)]
+    dg_h = [torch.empty(plan.dgamma.numel(), dtype=torch.float32).pin_memory()
+            for _ in range(NSETS)]
     ins_h = (q_h, k_h, v_h, g_h, do_h)
     h2d = sum(x.numel() * x.element_size() for x in ins_h)
     d2h = sum(x[0].numel() * x[0].element_size() for x in (out_h, dq_h, dk_h, dv_h, dg_h))
@@ -469,28 +473,28 @@ def run_ours(args, w, rank, world):
             e2e_ms.append(a.elapsed_time(b))
     e2e_serial = tokens / (sum(e2e_ms) / len(e2e_ms) * 1e-3)
 
-    plan2 = ZetaPlan(p, dev)
-    dev_in = [(q, k, v, gamma, dout), tuple(torch.empty_like(t) for t in (q, k, v, gamma, dout))]
-    plans = [plan, plan2]
+    plans = [plan] + [ZetaPlan(p, dev) for _ in range(NSETS - 1)]
+    dev_in = [(q, k, v, gamma, dout)] + [tuple(torch.empty_like(t) for t in (q, k, v, gamma, dout))
+                                         for _ in range(NSETS - 1)]
     comp = torch.cuda.current_stream()
     cp_in, cp_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    comp_done = [ev(), ev()]
-    out_done = [ev(), ev()]
-    started = [False, False]
+    comp_done = [ev() for _ in range(NSETS)]
+    out_done = [ev() for _ in range(NSETS)]
+    in_ready = [ev() for _ in range(NSETS)]
+    started = [False] * NSETS
 
     def pipelined_steps(n):
         for it in range(n):
-            bi = it & 1
+            bi = it % NSETS
             with torch.cuda.stream(cp_in):
                 if started[bi]:
-                    cp_in.wait_event(comp_done[bi])       # step it-2 done with set bi
+                    cp_in.wait_event(comp_done[bi])       # the set's previous step computed
                 for src, dst in zip(ins_h, dev_in[bi]):
                     dst.copy_(src, non_blocking=True)
-                ready = ev()
-                ready.record(cp_in)
-            comp.wait_event(ready)
+                in_ready[bi].record(cp_in)
+            comp.wait_event(in_ready[bi])
             if started[bi]:
-                comp.wait_event(out_done[bi])             # results of step it-2 copied out
+                comp.wait_event(out_done[bi])             # and its results copied out
             qq, kk_, vv, gg, dd = dev_in[bi]
             plans[bi].forward(qq, kk_, vv, gg)
             plans[bi].backward(qq, kk_, vv, gg, dd)
@@ -515,7 +519,7 @@ def run_ours(args, w, rank, world):
     t_b.synchronize()
     torch.cuda.synchronize()
     e2e = tokens * args.steps / (t_a.elapsed_time(t_b) * 1e-3)
-    del plan2, dev_in
+    del plans, dev_in
 
     # --- efficiency workload: forward alone, and the attend-forward kernel roofline
     we = W.EFFICIENCY.replace(seed=W.EFFICIENCY.seed + 1000 * rank)
@@ -858,8 +862,8 @@ def run_ours(args, w, rank, world):
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "how": "pinned host buffers; per step H2D of q, k, v, gamma, dO, the five calls, "
-                       "D2H of out, dq, dk, dv, dgamma; two buffer sets, copies on side streams "
-                       "overlapping the neighbouring steps' compute",
+                       "D2H of out, dq, dk, dv, dgamma; three buffer sets, copies on side "
+                       "streams overlapping the neighbouring steps' compute",
                 "serial_value": e2e_serial},
         "gpu_launches": launches_per_step(w) * args.steps,
         "cpu_baseline": {"value": oracle_tokens_per_s(w, w.N, cpu_dt), "unit": "tokens/s",
