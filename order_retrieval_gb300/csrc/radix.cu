@@ -17,31 +17,55 @@
 namespace zeta {
 namespace {
 
+// Every source hands a thread the items p0, p0 + 32, ..., p0 + 32 (R - 1) of a
+// segment (a warp reads 32 consecutive items per load), all loads issued before
+// any is used; ok[r] is false past the segment's end and for skipped items.
+template <int R, typename Src, typename K>
+__device__ __forceinline__ void load_plain(const Src &s, int64_t seg, int64_t p0, int64_t len,
+                                           K (&key)[R], uint32_t (&val)[R], bool (&ok)[R]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t p = p0 + 32 * r;
+        ok[r] = p < len;
+        if (ok[r]) s.load1(seg, p, key[r], val[r]);
+    }
+}
+
 template <typename K>
 struct CodesSrc {          // first pass over Z codes: value = position
     static constexpr bool kHasVal = true;
+    static constexpr int kDownBlocks = 2;   // CTAs per SM the downsweep is built for
     const K *codes;
     int64_t N;
     __device__ int64_t len(int64_t) const { return N; }
-    __device__ bool load(int64_t seg, int64_t p, K &key, uint32_t &val, int32_t *) const {
+    __device__ void load1(int64_t seg, int64_t p, K &key, uint32_t &val) const {
         key = codes[seg * N + p];
         val = static_cast<uint32_t>(p);
-        return true;
+    }
+    template <int R>
+    __device__ void load_run(int64_t seg, int64_t p0, int64_t len, K (&key)[R], uint32_t (&val)[R],
+                             bool (&ok)[R], int32_t *) const {
+        load_plain(*this, seg, p0, len, key, val, ok);
     }
 };
 
 template <typename K>
 struct PairsSrc {          // later passes: ping-pong buffers
     static constexpr bool kHasVal = true;
+    static constexpr int kDownBlocks = 2;   // CTAs per SM the downsweep is built for
     const K *keys;
     const uint32_t *vals;
     int64_t stride;
     const uint32_t *seglen;
     __device__ int64_t len(int64_t seg) const { return seglen ? (int64_t)seglen[seg] : stride; }
-    __device__ bool load(int64_t seg, int64_t p, K &key, uint32_t &val, int32_t *) const {
+    __device__ void load1(int64_t seg, int64_t p, K &key, uint32_t &val) const {
         key = keys[seg * stride + p];
         val = vals[seg * stride + p];
-        return true;
+    }
+    template <int R>
+    __device__ void load_run(int64_t seg, int64_t p0, int64_t len, K (&key)[R], uint32_t (&val)[R],
+                             bool (&ok)[R], int32_t *) const {
+        load_plain(*this, seg, p0, len, key, val, ok);
     }
 };
 
@@ -56,6 +80,7 @@ struct SlotDiv {
     uint32_t k, C;
     float inv_k, inv_C;
     bool fast;                // N k <= 2^24
+    uint32_t a32, b32;        // 32 = a32 k + b32
     static __device__ __forceinline__ uint32_t quot(uint32_t n, uint32_t d, float inv_d) {
         uint32_t q = __float2uint_rz(__uint2float_rn(n) * inv_d);
         const int64_t r = (int64_t)n - (int64_t)q * d;
@@ -75,25 +100,56 @@ struct SlotDiv {
 };
 inline SlotDiv slot_div(int64_t N, int k, int C) {
     return SlotDiv{(uint32_t)k, (uint32_t)C, 1.0f / (float)k, 1.0f / (float)C,
-                   N * (int64_t)k <= (int64_t(1) << 24)};
+                   N * (int64_t)k <= (int64_t(1) << 24), 32u / (uint32_t)k, 32u % (uint32_t)k};
 }
+
+// Query and chunk start of the slots p0, p0 + 32, p0 + 64, ... of one thread:
+// one division for the first, then each step adds 32 = a32 k + b32 to the
+// remainder (one carry at most, as b32 < k) and moves the chunk start on by C
+// while the query has passed the chunk's end (at most 33 queries per step).
+struct SlotRun {
+    uint32_t i, rem, cC;
+    __device__ __forceinline__ SlotRun(const SlotDiv &dv, uint32_t p0) {
+        dv.split(p0, i, cC);
+        rem = p0 - i * dv.k;
+    }
+    __device__ __forceinline__ void next(const SlotDiv &dv) {
+        i += dv.a32;
+        rem += dv.b32;
+        if (rem >= dv.k) {
+            rem -= dv.k;
+            ++i;
+        }
+        while (i >= cC + dv.C) cC += dv.C;
+    }
+};
 
 struct IdxSrc {            // window indices: key = selected key, value = query
     static constexpr bool kHasVal = true;
+    static constexpr int kDownBlocks = 2;   // CTAs per SM the downsweep is built for
     const int32_t *idx;
     int64_t N;
     int k;
     SlotDiv dv;
     __device__ int64_t len(int64_t) const { return N * k; }
-    __device__ bool load(int64_t seg, int64_t p, uint32_t &key, uint32_t &val, int32_t *st) const {
-        const int32_t j = idx[seg * N * k + p];
-        if (j == -1) return false;
-        uint32_t i, cC;
-        dv.split(static_cast<uint32_t>(p), i, cC);                                 // N*k < 2^31
-        if (static_cast<uint32_t>(j) >= cC) { set_status(st, ZETA_ERR_BOUNDS); return false; }
-        key = static_cast<uint32_t>(j);
-        val = i;
-        return true;
+    template <int R>
+    __device__ void load_run(int64_t seg, int64_t p0, int64_t len, uint32_t (&key)[R],
+                             uint32_t (&val)[R], bool (&ok)[R], int32_t *st) const {
+        int32_t j[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) j[r] = p0 + 32 * r < len ? idx[seg * N * k + p0 + 32 * r] : -1;
+        SlotRun sr(dv, static_cast<uint32_t>(p0));                                 // N*k < 2^31
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (r > 0) sr.next(dv);
+            ok[r] = j[r] != -1;
+            if (ok[r] && static_cast<uint32_t>(j[r]) >= sr.cC) {
+                set_status(st, ZETA_ERR_BOUNDS);
+                ok[r] = false;
+            }
+            key[r] = static_cast<uint32_t>(j[r]);
+            val[r] = sr.i;
+        }
     }
 };
 
@@ -102,31 +158,46 @@ struct IdxSrc {            // window indices: key = selected key, value = query
 // no separate value array moves.
 struct PackedIdxSrc {
     static constexpr bool kHasVal = false;
+    static constexpr int kDownBlocks = 2;   // CTAs per SM the downsweep is built for
     const int32_t *idx;
     int64_t N;
     int k;
     SlotDiv dv;
     __device__ int64_t len(int64_t) const { return N * k; }
-    __device__ bool load(int64_t seg, int64_t p, uint32_t &key, uint32_t &, int32_t *st) const {
-        const int32_t j = idx[seg * N * k + p];
-        if (j == -1) return false;
-        uint32_t i, cC;
-        dv.split(static_cast<uint32_t>(p), i, cC);
-        if (static_cast<uint32_t>(j) >= cC) { set_status(st, ZETA_ERR_BOUNDS); return false; }
-        key = (static_cast<uint32_t>(j) << 16) | i;
-        return true;
+    template <int R>
+    __device__ void load_run(int64_t seg, int64_t p0, int64_t len, uint32_t (&key)[R],
+                             uint32_t (&)[R], bool (&ok)[R], int32_t *st) const {
+        int32_t j[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) j[r] = p0 + 32 * r < len ? idx[seg * N * k + p0 + 32 * r] : -1;
+        SlotRun sr(dv, static_cast<uint32_t>(p0));
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (r > 0) sr.next(dv);
+            ok[r] = j[r] != -1;
+            if (ok[r] && static_cast<uint32_t>(j[r]) >= sr.cC) {
+                set_status(st, ZETA_ERR_BOUNDS);
+                ok[r] = false;
+            }
+            key[r] = (static_cast<uint32_t>(j[r]) << 16) | sr.i;
+        }
     }
 };
 
 struct PackedSrc {         // later passes over packed words
     static constexpr bool kHasVal = false;
+    static constexpr int kDownBlocks = 3;   // CTAs per SM the downsweep is built for
     const uint32_t *keys;
     int64_t stride;
     const uint32_t *seglen;
     __device__ int64_t len(int64_t seg) const { return (int64_t)seglen[seg]; }
-    __device__ bool load(int64_t seg, int64_t p, uint32_t &key, uint32_t &, int32_t *) const {
+    __device__ void load1(int64_t seg, int64_t p, uint32_t &key, uint32_t &) const {
         key = keys[seg * stride + p];
-        return true;
+    }
+    template <int R>
+    __device__ void load_run(int64_t seg, int64_t p0, int64_t len, uint32_t (&key)[R],
+                             uint32_t (&val)[R], bool (&ok)[R], int32_t *) const {
+        load_plain(*this, seg, p0, len, key, val, ok);
     }
 };
 
@@ -139,15 +210,14 @@ radix_upsweep(Src src, int shift, uint32_t *__restrict__ hist, int64_t tiles, in
     __syncthreads();
     const int64_t len = src.len(seg);
     const int64_t base = tile * kRadixTile;
-    for (int r = 0; r < kRadixItems; ++r) {
-        int64_t p = base + r * kRadixThreads + threadIdx.x;
-        if (p < len) {
-            K key;
-            uint32_t val;
-            if (src.load(seg, p, key, val, status))
-                atomicAdd(&sh[(unsigned)(key >> shift) & 255u], 1u);
-        }
-    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    K key[kRadixItems];
+    uint32_t val[kRadixItems];
+    bool ok[kRadixItems];
+    src.load_run(seg, base + w * (32 * kRadixItems) + lane, len, key, val, ok, status);
+#pragma unroll
+    for (int r = 0; r < kRadixItems; ++r)
+        if (ok[r]) atomicAdd(&sh[(unsigned)(key[r] >> shift) & 255u], 1u);
     __syncthreads();
     if (threadIdx.x < 256) hist[(seg * tiles + tile) * 256 + threadIdx.x] = sh[threadIdx.x];
 }
@@ -211,7 +281,7 @@ constexpr size_t downsweep_smem() {
 }
 
 template <typename K, typename Src>
-__global__ void __launch_bounds__(kRadixThreads)
+__global__ void __launch_bounds__(kRadixThreads, Src::kDownBlocks)
 radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t tiles,
                 K *__restrict__ keys_out, uint32_t *__restrict__ vals_out, int64_t out_stride) {
     constexpr int W = kRadixThreads / 32;
@@ -234,15 +304,12 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
     const unsigned lt = lanemask_lt();
     K key[kRadixItems];
     uint32_t val[kRadixItems];
+    bool ok[kRadixItems];
     int dig[kRadixItems];
     uint32_t rank[kRadixItems];
+    src.load_run(seg, base + w * (32 * kRadixItems) + lane, len, key, val, ok, nullptr);
 #pragma unroll
-    for (int r = 0; r < kRadixItems; ++r) {     // all of the thread's loads in flight first
-        const int64_t p = base + w * (32 * kRadixItems) + r * 32 + lane;
-        bool ok = false;
-        if (p < len) ok = src.load(seg, p, key[r], val[r], nullptr);
-        dig[r] = ok ? (int)((unsigned)(key[r] >> shift) & 255u) : 256;
-    }
+    for (int r = 0; r < kRadixItems; ++r) dig[r] = ok[r] ? (int)((unsigned)(key[r] >> shift) & 255u) : 256;
 #pragma unroll
     for (int r = 0; r < kRadixItems; ++r) {
         // lanes with this lane's digit: eight ballots, one per digit bit (far
