@@ -300,6 +300,8 @@ struct BwdWs {
     double *slice_sum;
     RadixWs rw;
     uint32_t *off;
+    float *own_dv;       // key side's own-chunk sums (tcgen05 path), else null
+    float *own_dk;
 };
 
 BwdWs carve_bwd(const Prob &p, void *base, size_t *bytes) {
@@ -320,6 +322,11 @@ BwdWs carve_bwd(const Prob &p, void *base, size_t *bytes) {
     w.rw.hist = cv.take<uint32_t>(p.S * radix_tiles(L) * 256);
     w.rw.seglen = cv.take<uint32_t>(p.S);
     w.off = cv.take<uint32_t>(p.S * (p.N + 1));
+    w.own_dv = w.own_dk = nullptr;
+    if (attend_bwd_tc_supported(p) && bwd_own_tc05_supported(p)) {
+        w.own_dv = cv.take<float>(rows * 64);
+        w.own_dk = cv.take<float>(rows * 4);
+    }
     if (bytes) *bytes = cv.bytes();
     return w;
 }
@@ -397,6 +404,15 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
         cudaError_t e = launch_bwd_query_tc(p, q, k, v, gamma, idx, dout, dq, w.rec, w.dgp,
                                             status, st);
         if (e != cudaSuccess) return e;
+        if (w.own_dv) {
+            e = launch_bwd_key_own_tc05(p, k, v, gamma, dout, w.rec, w.own_dv, w.own_dk, status,
+                                        st);
+            if (e == cudaErrorNotSupported) {       // no tensor-map encoder: the key kernel
+                w.own_dv = w.own_dk = nullptr;      // computes its own-chunk block itself
+                e = cudaSuccess;
+            }
+            if (e != cudaSuccess) return e;
+        }
         int ob = 0;
         const bool packed = p.N <= 65536;
         e = packed ? radix_sort_idx_packed(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st)
@@ -407,7 +423,8 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
         csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(sorted, w.rw.seglen, L, p.N,
                                                               packed ? 16 : 0, w.off);
         e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, packed ? sorted : w.rw.vals[ob],
-                              packed ? 0xffffu : 0xffffffffu, w.off, L, dk, dv, st);
+                              packed ? 0xffffu : 0xffffffffu, w.off, L, dk, dv, w.own_dv,
+                              w.own_dk, st);
         if (e != cudaSuccess) return e;
         dgamma_reduce(p, w, dgamma, st);
         return cudaGetLastError();

@@ -35,6 +35,7 @@
 // and records the final m with 1/s and gbar for the key side.
 #include <type_traits>
 
+#include "bwd_rec.cuh"
 #include "mma.cuh"
 
 namespace zeta {
@@ -43,15 +44,6 @@ namespace {
 constexpr int T64 = 64;           // rows per CTA tile (queries or keys)
 constexpr int DV = 64;
 constexpr int THREADS = 128;
-
-// Per-query record for the key side: q (padded to 4), then {1/s, -gbar/s, m,
-// gbar} (m: the softmax shift; 0 for the other weight kernels), so that
-// dL/dw_ij = g_ij / s - gbar / s is one fma and the two scalars it needs are
-// adjacent (one 8-byte load).
-struct __align__(16) QRec {
-    float4 q;
-    float4 sg;
-};
 
 // Sums over the warp of 16 values per lane with 16 shuffles (recursive
 // halving); lane L returns the total of value (L >> 1).
@@ -653,7 +645,8 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
            const float *__restrict__ gamma, const __nv_bfloat16 *__restrict__ dout,
            const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q, uint32_t csr_mask,
            const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
-           __nv_bfloat16 *__restrict__ dv, int N, int H, int C, int tiles_per_chunk) {
+           __nv_bfloat16 *__restrict__ dv, const float *__restrict__ own_dv,
+           const float *__restrict__ own_dk, int N, int H, int C, int tiles_per_chunk) {
     extern __shared__ __align__(16) unsigned char key_smem[];
     KSmem &sm = *reinterpret_cast<KSmem *>(key_smem);
     KOwn &own = *reinterpret_cast<KOwn *>(sm.big);
@@ -909,9 +902,12 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             make_float4(dkacc[0], dkacc[1], dkacc[2], dkacc[3]);
     // every warp's walk is done before the rings become the own-chunk tiles
     __syncthreads();
-    stage_rows(own.v, vb, j0, jend);
-    load_qtile(0, j0);                // query tiles start at the key tile
-    cp_async_commit();
+    // (own_dv set: the own-chunk sums come from a separate kernel)
+    if (!own_dv) {
+        stage_rows(own.v, vb, j0, jend);
+        load_qtile(0, j0);            // query tiles start at the key tile
+        cp_async_commit();
+    }
 
     // ------------------------------------------------- own-chunk part ---
     const int g8 = lane >> 2, tig = lane & 3;
@@ -1024,7 +1020,7 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             }
         }
     };
-    for (int t = 0; t < nqt; ++t) {
+    for (int t = 0; t < (own_dv ? 0 : nqt); ++t) {
         const int iq0 = j0 + t * T64;
         if (t + 1 < nqt) load_qtile((t + 1) & 1, iq0 + T64);
         cp_async_commit();
@@ -1059,6 +1055,29 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
         dkl_b[d] += __shfl_xor_sync(kFull, dkl_b[d], 2);
     }
     const int rowa = warp * 16 + g8, rowb = rowa + 8;
+    if (own_dv) {                    // the separate kernel's own-chunk sums
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int col = nt * 8 + 2 * tig;
+            const float2 oa = ka < jend ? *reinterpret_cast<const float2 *>(
+                                              own_dv + (seg * N + ka) * (int64_t)DV + col)
+                                        : dup2(0.f);
+            const float2 ob = kbi < jend ? *reinterpret_cast<const float2 *>(
+                                               own_dv + (seg * N + kbi) * (int64_t)DV + col)
+                                         : dup2(0.f);
+            dva[nt][0] = oa.x;
+            dva[nt][1] = oa.y;
+            dva[nt][2] = ob.x;
+            dva[nt][3] = ob.y;
+        }
+        if (tig == 0) {
+#pragma unroll
+            for (int d = 0; d < DK; ++d) {
+                dkl_a[d] = ka < jend ? own_dk[(seg * N + ka) * 4 + d] : 0.f;
+                dkl_b[d] = kbi < jend ? own_dk[(seg * N + kbi) * 4 + d] : 0.f;
+            }
+        }
+    }
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
         const int col = nt * 8 + 2 * tig;
@@ -1132,7 +1151,8 @@ template <int D, int WK>
 cudaError_t bwd_key_tc_launch(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
                               const float *gamma, const void *dout, const void *rec,
                               const uint32_t *csr_q, uint32_t csr_mask, const uint32_t *off,
-                              int64_t csr_stride, float *dk, void *dv, cudaStream_t st) {
+                              int64_t csr_stride, float *dk, void *dv, const float *own_dv,
+                              const float *own_dk, cudaStream_t st) {
     static PerDeviceOnce smem_once;          // run once per device, outside any capture
     const cudaError_t e = smem_once.run([] {
         return cudaFuncSetAttribute(bwd_key_tc<D, WK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1142,7 +1162,7 @@ cudaError_t bwd_key_tc_launch(const Prob &p, dim3 grid, int tpc, const float *k,
     bwd_key_tc<D, WK><<<grid, THREADS, sizeof(KSmem), st>>>(
         k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout),
         static_cast<const QRec *>(rec), csr_q, csr_mask, off, csr_stride, dk,
-        static_cast<__nv_bfloat16 *>(dv), p.N, p.H, p.C, tpc);
+        static_cast<__nv_bfloat16 *>(dv), own_dv, own_dk, p.N, p.H, p.C, tpc);
     return cudaGetLastError();
 }
 
@@ -1150,16 +1170,21 @@ template <int WK>
 cudaError_t bwd_key_tc_dk(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
                           const float *gamma, const void *dout, const void *rec,
                           const uint32_t *csr_q, uint32_t csr_mask, const uint32_t *off,
-                          int64_t csr_stride, float *dk, void *dv, cudaStream_t st) {
+                          int64_t csr_stride, float *dk, void *dv, const float *own_dv,
+                          const float *own_dk, cudaStream_t st) {
     switch (p.dK) {
         case 1: return bwd_key_tc_launch<1, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
-                                                csr_mask, off, csr_stride, dk, dv, st);
+                                                csr_mask, off, csr_stride, dk, dv, own_dv, own_dk,
+                                                st);
         case 2: return bwd_key_tc_launch<2, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
-                                                csr_mask, off, csr_stride, dk, dv, st);
+                                                csr_mask, off, csr_stride, dk, dv, own_dv, own_dk,
+                                                st);
         case 3: return bwd_key_tc_launch<3, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
-                                                csr_mask, off, csr_stride, dk, dv, st);
+                                                csr_mask, off, csr_stride, dk, dv, own_dv, own_dk,
+                                                st);
         default: return bwd_key_tc_launch<4, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
-                                                 csr_mask, off, csr_stride, dk, dv, st);
+                                                 csr_mask, off, csr_stride, dk, dv, own_dv,
+                                                 own_dk, st);
     }
 }
 
@@ -1182,17 +1207,18 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
                               const void *dout, const void *rec, const uint32_t *csr_q,
                               uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
-                              float *dk, void *dv, cudaStream_t st) {
+                              float *dk, void *dv, const float *own_dv, const float *own_dk,
+                              cudaStream_t st) {
     const int tpc = (p.C + T64 - 1) / T64;
     const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
     if (p.wk == kWSoftmax)
         return bwd_key_tc_dk<kWSoftmax>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask,
-                                        off, csr_stride, dk, dv, st);
+                                        off, csr_stride, dk, dv, own_dv, own_dk, st);
     if (p.wk == kWInvEuclid)
         return bwd_key_tc_dk<kWInvEuclid>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask,
-                                          off, csr_stride, dk, dv, st);
+                                          off, csr_stride, dk, dv, own_dv, own_dk, st);
     return bwd_key_tc_dk<kWCauchy>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
-                                   csr_stride, dk, dv, st);
+                                   csr_stride, dk, dv, own_dv, own_dk, st);
 }
 
 }  // namespace zeta

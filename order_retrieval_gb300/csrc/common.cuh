@@ -163,10 +163,23 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
                                 float *dq, void *rec, float *dg_part, int32_t *status,
                                 cudaStream_t st);
 // csr_q holds the queries of every key's list (masked with csr_mask).
+// own_dv / own_dk: the own-chunk partial sums from launch_bwd_key_own_tc05, or
+// null for the key kernel to compute its own-chunk block itself.
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
                               const void *dout, const void *rec, const uint32_t *csr_q,
                               uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
-                              float *dk, void *dv, cudaStream_t st);
+                              float *dk, void *dv, const float *own_dv, const float *own_dk,
+                              cudaStream_t st);
+// The key side's own-chunk block on tcgen05 (C a multiple of 128, N of C;
+// cudaErrorNotSupported when the driver offers no tensor-map encoder or k, v
+// or dout is not 16-byte aligned):
+// per key, dv (64 floats) and dk (4 floats) into own_dv / own_dk, without the
+// Cauchy constant.
+bool bwd_own_tc05_supported(const Prob &p);
+cudaError_t launch_bwd_key_own_tc05(const Prob &p, const float *k, const void *v,
+                                    const float *gamma, const void *dout, const void *rec,
+                                    float *own_dv, float *own_dk, int32_t *status,
+                                    cudaStream_t st);
 
 size_t bwd_ws_bytes(const Prob &p);
 cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, const void *v,

@@ -33,9 +33,8 @@
 // abort flag that ends every role's loop; the producer then waits (bounded)
 // for its loads in flight and the MMA thread for its MMAs before the TMEM is
 // freed.
-#include <cudaTypedefs.h>
-
 #include "tc05.cuh"
+#include "tmap.cuh"
 #include "zorder.cuh"
 
 namespace zeta {
@@ -284,32 +283,6 @@ project_encode_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constan
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &qr) != cudaSuccess ||
-            qr != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
-
-// Row-major bf16 matrix [rows, cols] as a 2-D TMA map with a (64 x box_rows)
-// box and the 128-byte swizzle.
-bool bf16_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int box_rows) {
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1u, 1u};
-    return tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr),
-                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename CodeT, int DK>
 cudaError_t launch_proj(const Prob &p, int D, const CUtensorMap &xmap, const CUtensorMap &wmap,
                         const float *b1, const float *w2, const float *b2, float *q, float *k,
@@ -358,7 +331,7 @@ cudaError_t launch_project_tc(const Prob &p, int D, const void *x, const void *w
                               cudaStream_t st) {
     const int64_t M = (int64_t)p.B * p.N;
     CUtensorMap xmap, wmap;
-    if (!bf16_map(&xmap, x, M, D, BM) || !bf16_map(&wmap, w1, 2LL * p.H * FH, D, BN))
+    if (!bf16_map(&xmap, x, M, D, BK, BM) || !bf16_map(&wmap, w1, 2LL * p.H * FH, D, BK, BN))
         return cudaErrorInvalidValue;
     if (p.code64)
         return launch_proj_dk<uint64_t>(p, D, xmap, wmap, b1, w2, b2, q, k, q_codes, k_codes,
