@@ -69,7 +69,7 @@ constexpr uint32_t V_BYTES = OKR * ODV * 2;
 constexpr uint32_t D_BYTES = OQ * ODV * 2;
 constexpr uint32_t P_BLOCK = OKR * 64 * 2;     // one 64-query K block of P^T
 constexpr uint32_t P_BYTES = 2 * P_BLOCK;
-constexpr uint32_t TM_DV = 2 * OQ;              // TMEM columns: G^T x 2, then dV
+constexpr uint32_t TM_DV = 2 * OQ;              // TMEM columns: G^T x 2, then dV x 2
 constexpr uint32_t TM_COLS = 512;
 constexpr int kRecFields = 8;                   // q0..q3, 1/s, -gbar/s, m, unused
 
@@ -82,7 +82,7 @@ struct OwnHead {
     uint64_t d_full[OSTG], d_empty[OSTG];
     uint64_t g_full[2], g_empty[2];
     uint64_t p_full[2], p_empty[2];
-    uint64_t dv_full, dv_empty;
+    uint64_t dv_full[2], dv_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
@@ -168,8 +168,10 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
             mbar_init(&sh.d_full[s], 32);        // every producer lane (records), + TMA bytes
             mbar_init(&sh.d_empty[s], 1);
         }
-        mbar_init(&sh.dv_full, 1);
-        mbar_init(&sh.dv_empty, OEPI);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh.dv_full[b], 1);
+            mbar_init(&sh.dv_empty[b], OEPI);
+        }
         mbar_init(&sh.drain, 1);
         sh.abort = 0;
         fence_mbar_init();
@@ -255,21 +257,31 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
             const uint32_t sP = smem_u32(base + OFF_P);
             uint32_t T = 0, U = 0;
             bool issued = false, ok = true;
-            // GEMM2 of global tile Tt (tile tt of its unit): dV (+)= P^T . dO
-            auto gemm2 = [&](uint32_t Tt, int tt) -> bool {
-                const uint32_t b = Tt & 1u, s = Tt % OSTG;
-                if (tt == 0 && !own_wait(sh, &sh.dv_empty, (U & 1u) ^ 1u, status)) return false;
-                if (!own_wait(sh, &sh.p_full[b], (Tt >> 1) & 1u, status)) return false;
+            // One stream of tiles across the units: GEMM1 of a tile, then GEMM2
+            // of the tile before it (whatever unit that was), so that the first
+            // G^T of a unit is ready when the element-wise warps finish the last
+            // tile of the previous one.  A unit's dV goes to accumulator U & 1.
+            struct Pend {
+                uint32_t Tt, U;
+                int tt;
+                bool last, valid;
+            } pend = {0u, 0u, 0, false, false};
+            auto gemm2 = [&](const Pend &q) -> bool {      // dV (+)= P^T . dO of tile q
+                const uint32_t b = q.Tt & 1u, s = q.Tt % OSTG, a = q.U & 1u;
+                if (q.tt == 0 && !own_wait(sh, &sh.dv_empty[a], ((q.U >> 1) & 1u) ^ 1u, status))
+                    return false;
+                if (!own_wait(sh, &sh.p_full[b], (q.Tt >> 1) & 1u, status)) return false;
                 tc05_fence_after();
                 const uint32_t pa = sP + b * P_BYTES, db = sD + s * D_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < OQ / 16; ++kk) {
                     const uint64_t ad = sdesc_k128(pa + (uint32_t)(kk >> 2) * P_BLOCK) + 2u * (kk & 3);
                     const uint64_t bd = sdesc_k128(db) + 128u * kk;   // 16 rows = 2048 bytes
-                    umma_bf16(tmem + TM_DV, ad, bd, idesc2, (tt | kk) != 0);
+                    umma_bf16(tmem + TM_DV + a * ODV, ad, bd, idesc2, (q.tt | kk) != 0);
                 }
                 umma_commit(&sh.p_empty[b]);
                 umma_commit(&sh.d_empty[s]);
+                if (q.last) umma_commit(&sh.dv_full[a]);
                 return true;
             };
             for (int64_t pr = blockIdx.x; 2 * pr < units && ok; pr += gridDim.x) {
@@ -292,14 +304,14 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
                         issued = true;
                         umma_commit(&sh.g_full[b]);
                         if (t == ntile - 1) umma_commit(&sh.v_empty[vb]);
-                        if (t > 0 && !(ok = gemm2(Tt - 1, t - 1))) break;
+                        if (pend.valid && !(ok = gemm2(pend))) break;
+                        pend = {Tt, U, t, t == ntile - 1, true};
                     }
                     if (!ok) break;
-                    if (!(ok = gemm2(T + ntile - 1, ntile - 1))) break;
-                    umma_commit(&sh.dv_full);
                     T += ntile;
                 }
             }
+            if (ok && pend.valid) ok = gemm2(pend);
             if (issued && own_aborted(sh)) {
                 umma_commit(&sh.drain);
                 mbar_wait_bounded(&sh.drain, 0);
@@ -318,6 +330,45 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
         const uint32_t sR = smem_u32(base + OFF_R);                  // the stages' records
         uint32_t T = 0, U = 0;
         bool ok = true;
+        // The epilogue of a unit (its dV row from TMEM, the dk parts summed
+        // through shared memory) runs after the first tile of the next unit,
+        // by which time the unit's last GEMM2 has long completed.
+        bool pend = false;
+        uint32_t pU = 0;
+        int64_t pgj = 0;
+        auto epilogue = [&]() -> bool {
+            const uint32_t a = pU & 1u;
+            bool okw = own_wait(sh, &sh.dv_full[a], (pU >> 1) & 1u, status);
+            if (!__all_sync(kFull, okw)) return false;
+            tc05_fence_after();
+            constexpr int DVC = ODV / OPARTS;            // dV columns per warp
+            uint32_t dr[DVC];
+            if constexpr (DVC == 16)
+                tmem_ld16(tl + TM_DV + a * ODV + DVC * part, *reinterpret_cast<uint32_t(*)[16]>(dr));
+            else
+                tmem_ld32(tl + TM_DV + a * ODV + DVC * part, *reinterpret_cast<uint32_t(*)[32]>(dr));
+            tmem_ld_wait();
+            tc05_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.dv_empty[a]);
+            float4 *dst = reinterpret_cast<float4 *>(own_dv + pgj * ODV + DVC * part);
+#pragma unroll
+            for (int x = 0; x < DVC / 4; ++x)
+                dst[x] = make_float4(__uint_as_float(dr[4 * x]), __uint_as_float(dr[4 * x + 1]),
+                                     __uint_as_float(dr[4 * x + 2]), __uint_as_float(dr[4 * x + 3]));
+            asm volatile("bar.sync 1, %0;\n" ::"n"(32 * OEPI) : "memory");
+            if (part == 0) {
+                float4 s4 = red[row];
+#pragma unroll
+                for (int x = 1; x < OPARTS; ++x) {
+                    const float4 b2 = red[x * OKR + row];
+                    s4 = make_float4(s4.x + b2.x, s4.y + b2.y, s4.z + b2.z, s4.w + b2.w);
+                }
+                *reinterpret_cast<float4 *>(own_dk + pgj * 4) = s4;
+            }
+            asm volatile("bar.sync 1, %0;\n" ::"n"(32 * OEPI) : "memory");
+            return true;
+        };
         for (int64_t pr = blockIdx.x; 2 * pr < units && ok; pr += gridDim.x) {
             for (int64_t u = 2 * pr; u < 2 * pr + 2 && u < units && ok; ++u, ++U) {
                 if (__any_sync(kFull, own_aborted(sh))) { ok = false; break; }
@@ -408,12 +459,12 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
                                 auto masked) {
                     uint32_t gb[2][8];
                     tmem_ld8(ga, gb[0]);
-                    tmem_ld_wait();
+                    tmem_ld_wait_tied(gb[0]);
 #pragma unroll
                     for (int c4 = 0; c4 < OCH; ++c4) {
                         if (c4 + 1 < OCH) tmem_ld8(ga + 8u * (c4 + 1), gb[(c4 + 1) & 1]);
                         chunk(rsa, gb[c4 & 1], pb, c4, masked);
-                        if (c4 + 1 < OCH) tmem_ld_wait();
+                        if (c4 + 1 < OCH) tmem_ld_wait_tied(gb[(c4 + 1) & 1]);
                         if (c4 + 2 == OCH || OCH == 1) {     // every column of the buffer read
                             tc05_fence_before();
                             __syncwarp();
@@ -435,29 +486,16 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh.p_full[b]);
+                    if (t == 0 && pend) {
+                        if (!(ok = epilogue())) break;
+                        pend = false;
+                    }
                 }
                 if (!ok) break;
                 T += ntile;
-                // the unit's dV row (16 columns per warp) and dk (the four parts
-                // summed through shared memory)
-                bool okw = own_wait(sh, &sh.dv_full, U & 1u, status);
-                if (!__all_sync(kFull, okw)) { ok = false; break; }
-                tc05_fence_after();
-                constexpr int DVC = ODV / OPARTS;            // dV columns per warp
-                uint32_t dr[DVC];
-                if constexpr (DVC == 16)
-                    tmem_ld16(tl + TM_DV + DVC * part, *reinterpret_cast<uint32_t(*)[16]>(dr));
-                else
-                    tmem_ld32(tl + TM_DV + DVC * part, *reinterpret_cast<uint32_t(*)[32]>(dr));
-                tmem_ld_wait();
-                tc05_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.dv_empty);
-                float4 *dst = reinterpret_cast<float4 *>(own_dv + gj * ODV + DVC * part);
-#pragma unroll
-                for (int x = 0; x < DVC / 4; ++x)
-                    dst[x] = make_float4(__uint_as_float(dr[4 * x]), __uint_as_float(dr[4 * x + 1]),
-                                         __uint_as_float(dr[4 * x + 2]), __uint_as_float(dr[4 * x + 3]));
+                // this unit's dk part for the deferred epilogue (the previous
+                // unit's epilogue has read the buffer: it ran after this unit's
+                // first tile)
                 float dks[4];
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
@@ -466,19 +504,12 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
                     dks[x] = lo + hi;
                 }
                 red[part * OKR + row] = make_float4(dks[0], dks[1], dks[2], dks[3]);
-                asm volatile("bar.sync 1, %0;\n" ::"n"(32 * OEPI) : "memory");
-                if (part == 0) {
-                    float4 a = red[row];
-#pragma unroll
-                    for (int x = 1; x < OPARTS; ++x) {
-                        const float4 b2 = red[x * OKR + row];
-                        a = make_float4(a.x + b2.x, a.y + b2.y, a.z + b2.z, a.w + b2.w);
-                    }
-                    *reinterpret_cast<float4 *>(own_dk + gj * 4) = a;
-                }
-                asm volatile("bar.sync 1, %0;\n" ::"n"(32 * OEPI) : "memory");
+                pend = true;
+                pU = U;
+                pgj = gj;
             }
         }
+        if (ok && pend) ok = epilogue();
     }
     __syncwarp();
     tc05_fence_before();
