@@ -158,7 +158,7 @@ struct IdxSrc {            // window indices: key = selected key, value = query
 // no separate value array moves.
 struct PackedIdxSrc {
     static constexpr bool kHasVal = false;
-    static constexpr int kDownBlocks = 2;   // CTAs per SM the downsweep is built for
+    static constexpr int kDownBlocks = 3;   // CTAs per SM the downsweep is built for
     const int32_t *idx;
     int64_t N;
     int k;
