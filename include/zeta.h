@@ -325,7 +325,9 @@ zeta_status_t zeta_select_attend_fwd(const zeta_problem_t *p, const float *q, co
  *   dv           out: v_dtype [B, H, N, d_V]  (16-B aligned)
  *   dgamma       out: float [H]
  *   workspace    scratch of at least zeta_bwd_workspace_bytes, 256-B aligned
- *   dev_status   optional int32 device word (ZETA_ERR_BOUNDS as for the forward)
+ *   dev_status   optional int32 device word (ZETA_ERR_BOUNDS as for the forward;
+ *                ZETA_ERR_DEVICE_TIMEOUT if a bounded wait of the tensor-core
+ *                own-chunk kernel gave up)
  * Every output is overwritten.  Reductions run in a fixed order, so results
  * are bit-reproducible run to run.
  * Errors: ZETA_ERR_INVALID_ARG, ZETA_ERR_UNSUPPORTED, ZETA_ERR_WORKSPACE.
@@ -339,7 +341,8 @@ zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, const flo
 /*
  * zeta_check_bounded_wait -- diagnostic of the device-side failure detection.
  * The pages have no counterpart: every wait of the TMA-fed and tensor-core
- * kernels (zeta_project_encode) on an mbarrier polls a bounded number of times
+ * kernels (zeta_project_encode, the own-chunk block of zeta_attend_bwd) on an
+ * mbarrier polls a bounded number of times
  * and, when it gives up, records ZETA_ERR_DEVICE_TIMEOUT in the status word and
  * lets the kernel return.  This call runs that wait on one barrier, completed
  * beforehand when arrive != 0 and never completed otherwise, polling at most

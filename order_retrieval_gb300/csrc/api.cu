@@ -4,7 +4,12 @@
 // returns a status without touching the device (and works without a GPU).
 #include <climits>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
+
+zeta::CallRange::CallRange(const char *name) { nvtxRangePushA(name); }
+zeta::CallRange::~CallRange() { nvtxRangePop(); }
 
 using zeta::Prob;
 
@@ -85,6 +90,7 @@ ZETA_API const char *zeta_status_string(zeta_status_t s) {
 
 ZETA_API zeta_status_t zeta_encode(const zeta_problem_t *p, const float *x, void *codes,
                                    cudaStream_t stream) {
+    zeta::CallRange range_("zeta_encode");
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -96,6 +102,7 @@ ZETA_API zeta_status_t zeta_encode(const zeta_problem_t *p, const float *x, void
 ZETA_API zeta_status_t zeta_sort_chunks(const zeta_problem_t *p, const void *key_codes,
                                         void *prefix_codes, int32_t *prefix_idx, void *workspace,
                                         size_t ws_bytes, cudaStream_t stream) {
+    zeta::CallRange range_("zeta_sort_chunks");
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -111,6 +118,7 @@ ZETA_API zeta_status_t zeta_sort_chunks(const zeta_problem_t *p, const void *key
 ZETA_API zeta_status_t zeta_select_topk(const zeta_problem_t *p, const void *q_codes,
                                         const void *prefix_codes, const int32_t *prefix_idx,
                                         int32_t *idx, cudaStream_t stream) {
+    zeta::CallRange range_("zeta_select_topk");
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -123,6 +131,7 @@ ZETA_API zeta_status_t zeta_select_topk(const zeta_problem_t *p, const void *q_c
 ZETA_API zeta_status_t zeta_encode_curves(const zeta_problem_t *p, const float *x,
                                           int32_t curves, const int32_t *axes, void *codes,
                                           cudaStream_t stream) {
+    zeta::CallRange range_("zeta_encode_curves");
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -144,6 +153,7 @@ ZETA_API zeta_status_t zeta_select_topk_curves(const zeta_problem_t *p, int32_t 
                                                const void *q_codes, const void *prefix_codes,
                                                const int32_t *prefix_idx, int32_t *idx,
                                                cudaStream_t stream) {
+    zeta::CallRange range_("zeta_select_topk_curves");
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -162,6 +172,7 @@ ZETA_API zeta_status_t zeta_project_encode(const zeta_problem_t *p, const zeta_p
                                            const float *w2, const float *b2, float *q, float *k,
                                            void *q_codes, void *k_codes, int32_t *dev_status,
                                            cudaStream_t stream) {
+    zeta::CallRange range_("zeta_project_encode");
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -179,6 +190,7 @@ ZETA_API zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, 
                                        const void *v, const float *gamma, const int32_t *idx,
                                        void *out, float *rowsum, int32_t *dev_status,
                                        cudaStream_t stream) {
+    zeta::CallRange range_("zeta_attend_fwd");
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -195,6 +207,7 @@ ZETA_API zeta_status_t zeta_select_attend_fwd(const zeta_problem_t *p, const flo
                                               const int32_t *prefix_idx, int32_t *idx, void *out,
                                               float *rowsum, int32_t *dev_status,
                                               cudaStream_t stream) {
+    zeta::CallRange range_("zeta_select_attend_fwd");
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -213,6 +226,7 @@ ZETA_API zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, 
                                        const void *dout, float *dq, float *dk, void *dv,
                                        float *dgamma, void *workspace, size_t ws_bytes,
                                        int32_t *dev_status, cudaStream_t stream) {
+    zeta::CallRange range_("zeta_attend_bwd");
     Prob pr;
     zeta_status_t s = check_problem(p, &pr);
     if (s != ZETA_OK) return s;
@@ -232,6 +246,7 @@ ZETA_API zeta_status_t zeta_attend_bwd(const zeta_problem_t *p, const float *q, 
 
 ZETA_API zeta_status_t zeta_check_bounded_wait(uint32_t iterations, int32_t arrive,
                                                int32_t *dev_status, cudaStream_t stream) {
+    zeta::CallRange range_("zeta_check_bounded_wait");
     if (!dev_status || iterations == 0) return ZETA_ERR_INVALID_ARG;
     return from_cuda(zeta::launch_bounded_wait_check(iterations, arrive, dev_status, stream));
 }

@@ -49,6 +49,15 @@ struct PerDeviceOnce {
     }
 };
 
+// A named NVTX range for the duration of one C-ABI call (host side: the
+// checks and the launches it enqueues); a no-op when no tool is attached.
+struct CallRange {
+    explicit CallRange(const char *name);
+    ~CallRange();
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
+
 // Record the first device-side error in an optional status word.
 __device__ __forceinline__ void set_status(int32_t *st, int code) {
     if (st) atomicCAS(st, 0, code);

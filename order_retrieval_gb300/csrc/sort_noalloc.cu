@@ -46,6 +46,7 @@ zeta_status_t scratch_on_current_device(void **out) {
 ZETA_API zeta_status_t zeta_sort_chunks_noalloc(const zeta_problem_t *p, const void *key_codes,
                                                 void *prefix_codes, int32_t *prefix_idx,
                                                 cudaStream_t stream) {
+    zeta::CallRange range_("zeta_sort_chunks_noalloc");
     // Every check of zeta_sort_chunks first, with no workspace: that call
     // returns before launching anything, with ZETA_OK when there is nothing to
     // sort (an empty problem, or fewer than two chunks), its own error for an

@@ -380,13 +380,20 @@ TC = [
     dict(N=768, C=192, k=64, d_K=2, bits=12),
     dict(N=512, C=128, k=20, d_K=4, bits=6),
     dict(N=512, C=64, k=64, bits=1),        # heavy code ties
+    # the key side's own-chunk kernel (C a multiple of 128): an odd number of
+    # one-tile units, d_K = 2, and more heads than its gamma table (H = 65: the
+    # key kernel then computes the own-chunk block itself)
+    dict(B=1, H=1, N=384, C=128, k=16),
+    dict(N=512, C=128, k=20, d_K=2, bits=12),
+    dict(B=1, H=65, N=256, C=128, k=8),
 ]
 
 
 @pytest.mark.parametrize("kw", TC, ids=lambda kw: "-".join(f"{a}{b}" for a, b in kw.items()))
 def test_tensor_core_path(kw):
     """bf16 values with d_V = 64 run the tensor-core forward and backward;
-    ragged tiles, k up to C, d_K from 1 to 4."""
+    ragged tiles, k up to C, d_K from 1 to 4, the key side's own-chunk block
+    on tcgen05 and its fallback."""
     base = dict(name="tc", B=2, H=2, N=256, d_K=3, d_V=64, k=8, C=64, bits=10, v_dtype="bf16",
                 gamma=(0.3, 1.0), dist="uniform", v_dist="normal", seed=21)
     base.update(kw)
