@@ -149,8 +149,10 @@ bwd_query_generic(const float *__restrict__ q, const float *__restrict__ kx,
 
 // off[seg][j] = first position of key j in the sorted (key, query) list; the
 // key of a sorted word is word >> key_shift (0: plain keys, 16: packed words).
-// Four positions per thread and step, read with one 16-byte load where the
-// segment's words are 16-byte aligned.
+// A lane takes eight consecutive positions (two 16-byte loads where the
+// segment's words are 16-byte aligned); the key before its first position
+// comes from the previous lane, lane 0 reading it.  Warps stride over the
+// segment together, so every lane of a warp takes part in each shuffle.
 __global__ void csr_offsets(const uint32_t *__restrict__ skeys, const uint32_t *__restrict__ seglen,
                             int64_t stride, int N, int key_shift, uint32_t *__restrict__ off) {
     const int64_t seg = blockIdx.y;
@@ -158,27 +160,35 @@ __global__ void csr_offsets(const uint32_t *__restrict__ skeys, const uint32_t *
     const uint32_t *K = skeys + seg * stride;
     uint32_t *o = off + seg * (int64_t)(N + 1);
     const bool vec = (reinterpret_cast<uintptr_t>(K) & 15u) == 0;
-    for (int64_t p0 = 4 * (blockIdx.x * (int64_t)blockDim.x + threadIdx.x); p0 <= L;
-         p0 += 4 * (int64_t)gridDim.x * blockDim.x) {
-        // key[0]: key before p0 (-1 at the start); key[1 + e]: key at p0 + e (N at L)
-        int64_t key[5];
-        key[0] = p0 > 0 ? (int64_t)(K[p0 - 1] >> key_shift) : -1;
-        if (vec && p0 + 4 <= L) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(K + p0);
-            key[1] = (int64_t)(w.x >> key_shift);
-            key[2] = (int64_t)(w.y >> key_shift);
-            key[3] = (int64_t)(w.z >> key_shift);
-            key[4] = (int64_t)(w.w >> key_shift);
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t w0 = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (int64_t wb = 256 * w0; wb <= L; wb += 256 * warps) {
+        const int64_t p0 = wb + 8 * lane;
+        // key[1 + e]: key at p0 + e (N at and past L); key[0]: the key before p0
+        int key[9];
+        if (vec && p0 + 8 <= L) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(K + p0);
+            const uint4 b = *reinterpret_cast<const uint4 *>(K + p0 + 4);
+            key[1] = (int)(a.x >> key_shift);
+            key[2] = (int)(a.y >> key_shift);
+            key[3] = (int)(a.z >> key_shift);
+            key[4] = (int)(a.w >> key_shift);
+            key[5] = (int)(b.x >> key_shift);
+            key[6] = (int)(b.y >> key_shift);
+            key[7] = (int)(b.z >> key_shift);
+            key[8] = (int)(b.w >> key_shift);
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                key[1 + e] = p0 + e < L ? (int64_t)(K[p0 + e] >> key_shift) : (int64_t)N;
+            for (int e = 0; e < 8; ++e) key[1 + e] = p0 + e < L ? (int)(K[p0 + e] >> key_shift) : N;
         }
+        key[0] = __shfl_up_sync(kFull, key[8], 1);
+        if (lane == 0) key[0] = p0 > 0 ? (int)(K[p0 - 1] >> key_shift) : -1;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 8; ++e) {
             const int64_t p = p0 + e;
             if (p > L) break;
-            for (int64_t j = key[e] + 1; j <= key[e + 1]; ++j) o[j] = (uint32_t)p;
+            for (int j = key[e] + 1; j <= key[e + 1]; ++j) o[j] = (uint32_t)p;
         }
     }
 }
