@@ -229,12 +229,19 @@ select_kernel(const K *__restrict__ qc, const K *__restrict__ pc,
             int start = r - (k + 1) / 2;
             start = start < 0 ? 0 : start;
             start = start > M - k ? M - k : start;
-            // the warp copies its 32 windows
+            // the warp copies its 32 windows: their rows are 32 k consecutive
+            // words of idx, written in order; word f is entry f % k of query
+            // f / k, whose window start comes from that query's lane
             const int32_t *pi = pidx + seg * T + (int64_t)C * c * (c - 1) / 2;
-            for (int qq = 0; qq < 32; ++qq) {
+            int32_t *o = out + (seg * N + qb) * (int64_t)k;
+            int qq = 0, t = lane;
+            while (t >= k) { t -= k; ++qq; }
+#pragma unroll 4
+            for (int f = lane; f < 32 * k; f += 32) {
                 const int s = __shfl_sync(kFull, start, qq);
-                int32_t *o = out + (seg * N + qb + qq) * (int64_t)k;
-                for (int t = lane; t < k; t += 32) o[t] = pi[s + t];
+                o[f] = pi[s + t];
+                t += 32;
+                while (t >= k) { t -= k; ++qq; }
             }
             return;
         }
@@ -261,14 +268,22 @@ select_kernel(const K *__restrict__ qc, const K *__restrict__ pc,
             start = start > M - k ? M - k : start;
         }
     }
+    // the warp's windows as one run of last * k words (as in the fenced path;
+    // here the queries may lie in different chunks, and chunk 0's rows are -1)
     const int last = min(32, N - qb);
-    for (int qq = 0; qq < last; ++qq) {
-        const int s = __shfl_sync(kFull, start, qq);
-        const int i2 = qb + qq;
-        const int c2 = i2 / C;
-        int32_t *o = out + (seg * N + i2) * (int64_t)k;
-        const int32_t *src = pidx + seg * T + (int64_t)C * c2 * (c2 - 1) / 2 + s;
-        for (int t = lane; t < k; t += 32) o[t] = s < 0 ? -1 : src[t];
+    const int total = last * k;
+    int32_t *o = out + (seg * N + qb) * (int64_t)k;
+    int qq = 0, t = lane;
+    while (t >= k) { t -= k; ++qq; }
+    for (int f0 = 0; f0 < total; f0 += 32) {
+        const int s = __shfl_sync(kFull, start, qq & 31);
+        const int f = f0 + lane;
+        if (f < total) {
+            const int c2 = (qb + qq) / C;
+            o[f] = s < 0 ? -1 : pidx[seg * T + (int64_t)C * c2 * (c2 - 1) / 2 + s + t];
+        }
+        t += 32;
+        while (t >= k) { t -= k; ++qq; }
     }
 }
 
