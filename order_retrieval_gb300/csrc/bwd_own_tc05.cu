@@ -26,13 +26,17 @@
 //          GEMM1, where it is the K-major B)
 // The kernel is persistent and warp-specialised:
 //   warp 0     producer: the unit's value tile and each query tile's dO rows
-//              by TMA, the tile's query records transposed into shared memory
-//              (one array per field) by the warp's lanes;
+//              by TMA, the unit's key coordinates by bulk copy, the tile's
+//              query records transposed into shared memory (one array per
+//              field) by the warp's lanes;
 //   warp 1     MMA issuer (one thread) and owner of the TMEM allocation: two
-//              128-column G^T buffers and the 64-column dV accumulator; GEMM1
-//              of the next tile is issued before GEMM2 of the current one;
+//              128-column G^T buffers and two 64-column dV accumulators (the
+//              units alternate); one stream of tiles across units, GEMM1 of a
+//              tile issued before GEMM2 of the tile before it;
 //   warps 2-17 element-wise, four warps per TMEM lane quarter (a warp may
-//              only read the lane quarter of its index mod 4).
+//              only read the lane quarter of its index mod 4); a unit's
+//              epilogue (its dV rows from TMEM, the dk sums) runs after the
+//              next unit's first tile, when that unit's last GEMM2 is done.
 // The units of a chunk are handed out in pairs (key tiles p and n-1-p: the same
 // number of query tiles per pair) to neighbouring CTAs, so that the chunk's dO
 // rows are read from L2.  Output per key: dv (64 floats) and dk (4 floats, the
