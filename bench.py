@@ -476,7 +476,9 @@ def run_ours(args, w, rank, world):
     plans = [plan] + [ZetaPlan(p, dev) for _ in range(NSETS - 1)]
     dev_in = [(q, k, v, gamma, dout)] + [tuple(torch.empty_like(t) for t in (q, k, v, gamma, dout))
                                          for _ in range(NSETS - 1)]
-    comp = torch.cuda.current_stream()
+    # compute on a stream of its own: on the legacy default stream the steps'
+    # kernels would serialise with the copies on the other streams
+    comp = torch.cuda.Stream(dev)
     cp_in, cp_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     comp_done = [ev() for _ in range(NSETS)]
     out_done = [ev() for _ in range(NSETS)]
@@ -495,12 +497,13 @@ def run_ours(args, w, rank, world):
             comp.wait_event(in_ready[bi])
             if started[bi]:
                 comp.wait_event(out_done[bi])             # and its results copied out
-            qq, kk_, vv, gg, dd = dev_in[bi]
-            plans[bi].forward(qq, kk_, vv, gg)
-            plans[bi].backward(qq, kk_, vv, gg, dd)
-            if world > 1:
-                dist.all_reduce(plans[bi].dgamma)
-            comp_done[bi].record(comp)
+            with torch.cuda.stream(comp):
+                qq, kk_, vv, gg, dd = dev_in[bi]
+                plans[bi].forward(qq, kk_, vv, gg)
+                plans[bi].backward(qq, kk_, vv, gg, dd)
+                if world > 1:
+                    dist.all_reduce(plans[bi].dgamma)
+                comp_done[bi].record(comp)
             with torch.cuda.stream(cp_out):
                 cp_out.wait_event(comp_done[bi])
                 for src, dst in zip(outs(plans[bi]), hosts(bi)):
