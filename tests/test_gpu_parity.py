@@ -386,6 +386,8 @@ TC = [
     dict(B=1, H=1, N=384, C=128, k=16),
     dict(N=512, C=128, k=20, d_K=2, bits=12),
     dict(B=1, H=65, N=256, C=128, k=8),
+    dict(N=768, C=384, k=16),               # three key tiles per chunk (pairs span chunks)
+    dict(B=1, H=2, N=8192, C=4096, k=64),   # units of up to 32 query tiles
 ]
 
 
