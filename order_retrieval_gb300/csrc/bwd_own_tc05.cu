@@ -40,8 +40,10 @@
 // The units of a chunk are handed out in pairs (key tiles p and n-1-p: the same
 // number of query tiles per pair) to neighbouring CTAs, so that the chunk's dO
 // rows are read from L2.  Output per key: dv (64 floats) and dk (4 floats, the
-// four quarters' sums added through shared memory), partial sums that the key
-// walk's epilogue adds to its own.
+// four query parts' sums added through shared memory, handed over by
+// mbarriers), partial sums that the key walk's epilogue adds to its own.  No
+// wait is on a hardware barrier among the element-wise warps, so that a warp
+// that gives up cannot leave the others blocked.
 // Hand-offs are mbarriers; every wait is bounded; a wait that gives up records
 // ZETA_ERR_DEVICE_TIMEOUT and raises an abort flag that ends every role's loop,
 // after which the producer waits (bounded) for its copies in flight and the MMA
@@ -87,6 +89,7 @@ struct OwnHead {
     uint64_t g_full[2], g_empty[2];
     uint64_t p_full[2], p_empty[2];
     uint64_t dv_full[2], dv_empty[2];
+    uint64_t red_full[2], red_free[2];    // a unit's dk parts written / read
     uint64_t drain;
     uint32_t tmem_base;
     int32_t abort;
@@ -96,8 +99,8 @@ constexpr uint32_t OFF_V = 0;
 constexpr uint32_t OFF_D = OFF_V + 2 * V_BYTES;
 constexpr uint32_t OFF_P = OFF_D + OSTG * D_BYTES;
 constexpr uint32_t OFF_R = OFF_P + 2 * P_BYTES;
-constexpr uint32_t OFF_K = OFF_R + OSTG * sizeof(OwnRecs);     // dk partials [parts][128] float4
-constexpr uint32_t OFF_KC = OFF_K + OPARTS * OKR * 16;          // key coordinates [2][128 * 4]
+constexpr uint32_t OFF_K = OFF_R + OSTG * sizeof(OwnRecs);     // dk parts [2][parts][128] float4
+constexpr uint32_t OFF_KC = OFF_K + 2 * OPARTS * OKR * 16;      // key coordinates [2][128 * 4]
 constexpr int kMaxHeads = 64;                                   // gammas staged in shared memory
 constexpr uint32_t OFF_G = OFF_KC + 2 * OKR * 16;
 constexpr uint32_t OFF_H = OFF_G + kMaxHeads * 4;
@@ -175,6 +178,8 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sh.dv_full[b], 1);
             mbar_init(&sh.dv_empty[b], OEPI);
+            mbar_init(&sh.red_full[b], OEPI);    // every element-wise warp's parts
+            mbar_init(&sh.red_free[b], 4);       // read by the four part-0 warps
         }
         mbar_init(&sh.drain, 1);
         sh.abort = 0;
@@ -330,7 +335,7 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
         // this thread's row of P^T in the K block of its queries
         const uint32_t sP = smem_u32(base + OFF_P) + (uint32_t)(row >> 3) * 1024u +
                             (uint32_t)(row & 7) * 128u;
-        float4 *red = reinterpret_cast<float4 *>(base + OFF_K);     // [part][row]
+        float4 *red = reinterpret_cast<float4 *>(base + OFF_K);     // [buffer][part][row]
         const uint32_t sR = smem_u32(base + OFF_R);                  // the stages' records
         uint32_t T = 0, U = 0;
         bool ok = true;
@@ -360,17 +365,20 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
             for (int x = 0; x < DVC / 4; ++x)
                 dst[x] = make_float4(__uint_as_float(dr[4 * x]), __uint_as_float(dr[4 * x + 1]),
                                      __uint_as_float(dr[4 * x + 2]), __uint_as_float(dr[4 * x + 3]));
-            asm volatile("bar.sync 1, %0;\n" ::"n"(32 * OEPI) : "memory");
-            if (part == 0) {
-                float4 s4 = red[row];
+            if (part == 0) {                             // the unit's dk: its parts summed
+                okw = own_wait(sh, &sh.red_full[a], (pU >> 1) & 1u, status);
+                if (!__all_sync(kFull, okw)) return false;
+                const float4 *rb = red + a * (OPARTS * OKR);
+                float4 s4 = rb[row];
 #pragma unroll
                 for (int x = 1; x < OPARTS; ++x) {
-                    const float4 b2 = red[x * OKR + row];
+                    const float4 b2 = rb[x * OKR + row];
                     s4 = make_float4(s4.x + b2.x, s4.y + b2.y, s4.z + b2.z, s4.w + b2.w);
                 }
                 *reinterpret_cast<float4 *>(own_dk + pgj * 4) = s4;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.red_free[a]);
             }
-            asm volatile("bar.sync 1, %0;\n" ::"n"(32 * OEPI) : "memory");
             return true;
         };
         for (int64_t pr = blockIdx.x; 2 * pr < units && ok; pr += gridDim.x) {
@@ -497,9 +505,8 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
                 }
                 if (!ok) break;
                 T += ntile;
-                // this unit's dk part for the deferred epilogue (the previous
-                // unit's epilogue has read the buffer: it ran after this unit's
-                // first tile)
+                // this unit's dk part for the deferred epilogue, into buffer
+                // U & 1 once the unit two back has been read from it
                 float dks[4];
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
@@ -507,7 +514,14 @@ bwd_key_own_tc05(const __grid_constant__ CUtensorMap vmap, const __grid_constant
                     f2_unpack(dk2[x], lo, hi);
                     dks[x] = lo + hi;
                 }
-                red[part * OKR + row] = make_float4(dks[0], dks[1], dks[2], dks[3]);
+                {
+                    const uint32_t a = U & 1u;
+                    bool okw = own_wait(sh, &sh.red_free[a], ((U >> 1) & 1u) ^ 1u, status);
+                    if (!__all_sync(kFull, okw)) { ok = false; break; }
+                    red[(a * OPARTS + part) * OKR + row] = make_float4(dks[0], dks[1], dks[2], dks[3]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh.red_full[a]);
+                }
                 pend = true;
                 pU = U;
                 pgj = gj;
