@@ -433,8 +433,8 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
         csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(sorted, w.rw.seglen, L, p.N,
                                                               packed ? 16 : 0, w.off);
         e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, packed ? sorted : w.rw.vals[ob],
-                              packed ? 0xffffu : 0xffffffffu, w.off, L, dk, dv, w.own_dv,
-                              w.own_dk, st);
+                              packed ? nullptr : sorted, packed ? 0xffffu : 0xffffffffu, w.off, L,
+                              dk, dv, w.own_dv, w.own_dk, st);
         if (e != cudaSuccess) return e;
         dgamma_reduce(p, w, dgamma, st);
         return cudaGetLastError();

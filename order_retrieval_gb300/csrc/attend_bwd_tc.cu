@@ -643,7 +643,8 @@ template <int DK, int WK>
 __global__ void __launch_bounds__(THREADS, 4)
 bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
            const float *__restrict__ gamma, const __nv_bfloat16 *__restrict__ dout,
-           const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q, uint32_t csr_mask,
+           const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q,
+           const uint32_t *__restrict__ csr_k, uint32_t csr_mask,
            const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
            __nv_bfloat16 *__restrict__ dv, const float *__restrict__ own_dv,
            const float *__restrict__ own_dk, int N, int H, int C, int tiles_per_chunk) {
@@ -676,31 +677,30 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     };
     // ---------------------------------------------------- window part ---
     // The queries that selected this warp's 16 keys are one contiguous run of
-    // the transposed lists (the lists of consecutive keys are adjacent), walked
-    // 32 entries at a time whatever key each entry belongs to.  Lane e owns
-    // entry e of a step: its key (the last key whose list starts at or before
-    // it), its query's record, w, a = w / s and the dk term.  The step's 32 dO
-    // rows are copied into a two-slot ring of swizzled 128-byte rows in shared
-    // memory (cp.async) one step ahead, the list positions two steps ahead.
+    // the transposed lists, walked 32 entries at a time whatever key each entry
+    // belongs to (the run need not be ordered by key).  Lane e owns entry e of a
+    // step: its key (from the list word, or the key array of the unpacked
+    // lists), its query's record, w, a = w / s and the dk term.  The step's 32
+    // dO rows are copied into a two-slot ring of swizzled 128-byte rows in
+    // shared memory (cp.async) one step ahead, the list entries two steps ahead.
     // With the 16 keys' v rows as the columns of B, G = dO_rows . V_keys^T on
     // the tensor cores gives every entry's g in the column of its key (read
     // back through a small scratch tile), and dV_keys += dO^T A, A holding a in
     // the column of the entry's key, accumulates all 16 keys' dv in the mma
     // registers over the whole walk.  A key half (8 columns) that no entry of a
-    // 16-entry tile belongs to is skipped.  The dk terms are summed per key by a
-    // segmented scan over the step (entries of one key are adjacent), in the
-    // order of the list.
+    // 16-entry tile belongs to is skipped.  dk is summed per key on the tensor
+    // cores too: dk_keys += OneHot^T X, X holding each entry's dk term split
+    // into a bf16 high part and a bf16 remainder (8 columns: d_K <= 4 dims x 2),
+    // staged as one 16-byte row per entry and read back by a transposing
+    // ldmatrix; the two parts are added at the end.
     const uint32_t *lst = csr_q + seg * csr_stride;
+    const uint32_t *klst = csr_k ? csr_k + seg * csr_stride : nullptr;
     const uint32_t *ob = off + seg * (int64_t)(N + 1);
     constexpr uint32_t kNone = 0xffffffffu;
     const int wj0 = j0 + warp * 16;
     const int nkw = max(0, min(16, jend - wj0));
-    // lane r < nkw: start of key r's list; lane nkw: end of the last list;
-    // other lanes: a bound that no list position reaches
-    const uint32_t bnd = (nkw > 0 && lane <= nkw) ? ob[wj0 + lane] : kNone;
-    const uint32_t bnd_hi = __shfl_sync(kFull, bnd, (lane + 1) & 31);   // lane r: end of key r's list
-    const uint32_t P0 = __shfl_sync(kFull, bnd, 0);
-    const uint32_t P1 = __shfl_sync(kFull, bnd, nkw);
+    const uint32_t P0 = nkw > 0 ? ob[wj0] : 0u;
+    const uint32_t P1 = nkw > 0 ? ob[wj0 + nkw] : 0u;
     const int nch = nkw > 0 ? (int)((P1 - P0 + 31) >> 5) : 0;
     const int g4 = lane >> 2, s4 = lane & 3;
     float kc[4] = {0.f, 0.f, 0.f, 0.f};                       // lane r: key r's coordinates
@@ -728,12 +728,20 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
         for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int e = 0; e < 4; ++e) cdv[c][h][e] = 0.f;
-    float dkacc[4] = {0.f, 0.f, 0.f, 0.f};                    // lane r: dk of key r
+    float cdk[4] = {0.f, 0.f, 0.f, 0.f};   // dk: keys g (+8) x columns 2t, 2t+1 (hi 0-3, lo 4-7)
     const uint32_t ring = smem_u32(sm.big) + (uint32_t)warp * kRingBytes;
     float *gs = &sm.dvp[warp * 16][0];                        // G scratch: [32 entries][kGs]
-    auto list_at = [&](int n) -> uint32_t {
+    const uint32_t gsa = smem_u32(gs);                        // ... then the dk rows [32][8] bf16
+    // entry n*32 + lane of the run: its query (kNone past the end) and its key
+    auto list_at = [&](int n, uint32_t &ie, int &kr) {
         const uint32_t pp = P0 + 32u * (uint32_t)n + (uint32_t)lane;
-        return (n < nch && pp < P1) ? (__ldg(lst + pp) & csr_mask) : kNone;
+        ie = kNone;
+        kr = 0;
+        if (n < nch && pp < P1) {
+            const uint32_t wd = __ldg(lst + pp);
+            ie = wd & csr_mask;
+            kr = (int)(klst ? __ldg(klst + pp) : (wd >> 16)) - wj0;
+        }
     };
     auto issue = [&](int n, uint32_t ie) {                    // dO rows of step n
         const uint32_t slot = ring + (uint32_t)(n & 1) * (kRingBytes / 2);
@@ -757,31 +765,30 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             r1 = r0;
         }
     };
-    uint32_t ie_cur = list_at(0);
+    uint32_t ie_cur, ie_nxt;
+    int kr_cur, kr_nxt;
+    list_at(0, ie_cur, kr_cur);
     float4 rn0, rn1;
     if (nch > 0) issue(0, ie_cur);
     record(ie_cur, rn0, rn1);
-    uint32_t ie_nxt = list_at(1);
+    list_at(1, ie_nxt, kr_nxt);
     for (int n = 0; n < nch; ++n) {
         const float4 rq0 = rn0, rq1 = rn1;
         const uint32_t ie = ie_cur;
+        const int kr = kr_cur;
         if (n + 1 < nch) {
             issue(n + 1, ie_nxt);
             record(ie_nxt, rn0, rn1);
         }
         ie_cur = ie_nxt;
-        ie_nxt = list_at(n + 2);
+        kr_cur = kr_nxt;
+        list_at(n + 2, ie_nxt, kr_nxt);
         if (n + 1 < nch) cp_async_wait<1>();
         else cp_async_wait<0>();
         __syncwarp();
         const uint32_t slot = ring + (uint32_t)(n & 1) * (kRingBytes / 2);
         const uint32_t base = P0 + 32u * (uint32_t)n;
-        const uint32_t pos = base + (uint32_t)lane;
         const bool valid = ie != kNone;
-        int kr = 0;
-#pragma unroll
-        for (int st = 8; st > 0; st >>= 1)
-            if (__shfl_sync(kFull, bnd, kr + st) <= pos) kr += st;
         float kj[4];
 #pragma unroll
         for (int d = 0; d < DK; ++d) kj[d] = __shfl_sync(kFull, kc[d], kr);
@@ -802,19 +809,18 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             // Cauchy: 2 w^2 / gamma^2 with the constant applied to dk at the end
             s2 = WK == kWCauchy ? w * w : 2.f * neg_dw_dd2<WK>(w, inv_g2);
         }
-        // keys met by each 16-entry tile (the step's entries are in key order)
+        // key halves met by each 16-entry tile
         const int last = min(31, (int)(P1 - base) - 1);
-        const int kr0 = __shfl_sync(kFull, kr, 0);
-        const int kr15 = __shfl_sync(kFull, kr, min(15, last));
-        const int kr16 = __shfl_sync(kFull, kr, 16);
-        const int kr31 = __shfl_sync(kFull, kr, last);
+        const unsigned blo = __ballot_sync(kFull, valid && kr < 8);
+        const unsigned bhi = __ballot_sync(kFull, valid && kr >= 8);
         const uint32_t pk = ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) << 16) |
                             (uint32_t)kr;
+        uint32_t ev[2][4];                                    // pk of entries 2t, 2t+1, 2t+8, 2t+9
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
             if (mt == 1 && last < 16) break;
-            const int klo = mt ? kr16 : kr0, khi = mt ? kr31 : kr15;
-            const bool half[2] = {klo < 8, khi >= 8};
+            const bool half[2] = {((blo >> (16 * mt)) & 0xffffu) != 0u,
+                                  ((bhi >> (16 * mt)) & 0xffffu) != 0u};
             uint32_t af[4][4];
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -833,10 +839,10 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                     make_float2(cg[2], cg[3]);
             }
             // dV_keys += dO^T A: entries 2t, 2t+1 (+8) of the tile in the rows of B
-            const uint32_t e0 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4);
-            const uint32_t e1 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 1);
-            const uint32_t e2 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 8);
-            const uint32_t e3 = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 9);
+            ev[mt][0] = __shfl_sync(kFull, pk, 16 * mt + 2 * s4);
+            ev[mt][1] = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 1);
+            ev[mt][2] = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 8);
+            ev[mt][3] = __shfl_sync(kFull, pk, 16 * mt + 2 * s4 + 9);
             // A of dim block c: the 8x8 blocks of the G fragments transposed in
             // registers (entries 0-7 | 8-15 x dims 0-7 | 8-15 of the block)
             uint32_t at[4][4];
@@ -852,8 +858,8 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
                 if (!half[h]) continue;
                 const uint32_t key = (uint32_t)(8 * h + g4);
                 auto pick = [key](uint32_t e) { return (e & 0xffffu) == key ? (e >> 16) : 0u; };
-                const uint32_t b0 = pick(e0) | (pick(e1) << 16);
-                const uint32_t b1 = pick(e2) | (pick(e3) << 16);
+                const uint32_t b0 = pick(ev[mt][0]) | (pick(ev[mt][1]) << 16);
+                const uint32_t b1 = pick(ev[mt][2]) | (pick(ev[mt][3]) << 16);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) mma16816(cdv[c][h], at[c], b0, b1);
             }
@@ -861,27 +867,37 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
         __syncwarp();
         const float gown = valid ? gs[lane * kGs + (kr ^ gs_swz(lane))] : 0.f;
         const float coef = valid ? __fmaf_rn(gown, inv_s, ngbs) * s2 : 0.f;
-        float x[4];
+        // this entry's dk term as a bf16 high part and remainder, one 16-byte row
+        uint32_t xw[4];
 #pragma unroll
-        for (int d = 0; d < DK; ++d) x[d] = coef * dqk[d];
-        // segmented inclusive scan: a lane adds only entries of its own key
-        const uint32_t kst = __shfl_sync(kFull, bnd, kr);
-        const int first = kst > base ? (int)(kst - base) : 0;
+        for (int hp = 0; hp < 2; ++hp) {
+            float x[2], r[2];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-            for (int d = 0; d < DK; ++d) {
-                const float y = __shfl_up_sync(kFull, x[d], o);
-                if (lane - o >= first) x[d] += y;
+            for (int e = 0; e < 2; ++e) {
+                const int d = 2 * hp + e;
+                x[e] = d < DK ? coef * dqk[d] : 0.f;
+                r[e] = x[e] - __bfloat162float(__float2bfloat16_rn(x[e]));
             }
+            xw[hp] = pack_bf16(x[0], x[1]);
+            xw[2 + hp] = pack_bf16(r[0], r[1]);
         }
-        // lane r < nkw takes key r's run of this step from the run's last entry
-        const bool has = lane < nkw && bnd_hi > base && bnd < base + 32u && bnd < bnd_hi;
-        const int tail = has ? (int)(min(bnd_hi, base + 32u) - 1u - base) : 0;
+        __syncwarp();                            // G scratch read before the rows overwrite it
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(gsa + 16u * lane),
+                     "r"(xw[0]), "r"(xw[1]), "r"(xw[2]), "r"(xw[3])
+                     : "memory");
+        __syncwarp();
+        uint32_t bx[4];                          // B fragments: tile 0 entries 0-7 | 8-15, tile 1 ..
+        ldsm_x4_trans(bx, gsa + 16u * lane);
 #pragma unroll
-        for (int d = 0; d < DK; ++d) {
-            const float y = __shfl_sync(kFull, x[d], tail);
-            if (has) dkacc[d] += y;
+        for (int mt = 0; mt < 2; ++mt) {
+            if (mt == 1 && last < 16) break;
+            auto one = [](uint32_t e, int key) { return (int)(e & 0xffffu) == key ? 0x3F80u : 0u; };
+            uint32_t ao[4];
+            ao[0] = one(ev[mt][0], g4) | (one(ev[mt][1], g4) << 16);
+            ao[1] = one(ev[mt][0], g4 + 8) | (one(ev[mt][1], g4 + 8) << 16);
+            ao[2] = one(ev[mt][2], g4) | (one(ev[mt][3], g4) << 16);
+            ao[3] = one(ev[mt][2], g4 + 8) | (one(ev[mt][3], g4 + 8) << 16);
+            mma16816(cdk, ao, bx[2 * mt], bx[2 * mt + 1]);
         }
         __syncwarp();
     }
@@ -897,9 +913,14 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
             sm.dvp[row][col + 8] = cdv[c][h][2];
             sm.dvp[row + 1][col + 8] = cdv[c][h][3];
         }
-    if (lane < 16)
-        *reinterpret_cast<float4 *>(sm.dkp[warp * 16 + lane]) =
-            make_float4(dkacc[0], dkacc[1], dkacc[2], dkacc[3]);
+    // dk: the high parts (columns 0-3) and remainders (4-7) added; lane (g, t)
+    // for t < 2 holds dims 2t, 2t+1 of keys g and g + 8
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cdk[e] += __shfl_xor_sync(kFull, cdk[e], 2);
+    if (s4 < 2) {
+        *reinterpret_cast<float2 *>(&sm.dkp[warp * 16 + g4][2 * s4]) = make_float2(cdk[0], cdk[1]);
+        *reinterpret_cast<float2 *>(&sm.dkp[warp * 16 + g4 + 8][2 * s4]) = make_float2(cdk[2], cdk[3]);
+    }
     // every warp's walk is done before the rings become the own-chunk tiles
     __syncthreads();
     // (own_dv set: the own-chunk sums come from a separate kernel)
@@ -1150,7 +1171,8 @@ cudaError_t bwd_query_tc_dk(const Prob &p, dim3 grid, int tpc, const float *q, c
 template <int D, int WK>
 cudaError_t bwd_key_tc_launch(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
                               const float *gamma, const void *dout, const void *rec,
-                              const uint32_t *csr_q, uint32_t csr_mask, const uint32_t *off,
+                              const uint32_t *csr_q, const uint32_t *csr_k, uint32_t csr_mask,
+                              const uint32_t *off,
                               int64_t csr_stride, float *dk, void *dv, const float *own_dv,
                               const float *own_dk, cudaStream_t st) {
     static PerDeviceOnce smem_once;          // run once per device, outside any capture
@@ -1161,7 +1183,7 @@ cudaError_t bwd_key_tc_launch(const Prob &p, dim3 grid, int tpc, const float *k,
     if (e != cudaSuccess) return e;
     bwd_key_tc<D, WK><<<grid, THREADS, sizeof(KSmem), st>>>(
         k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout),
-        static_cast<const QRec *>(rec), csr_q, csr_mask, off, csr_stride, dk,
+        static_cast<const QRec *>(rec), csr_q, csr_k, csr_mask, off, csr_stride, dk,
         static_cast<__nv_bfloat16 *>(dv), own_dv, own_dk, p.N, p.H, p.C, tpc);
     return cudaGetLastError();
 }
@@ -1169,20 +1191,21 @@ cudaError_t bwd_key_tc_launch(const Prob &p, dim3 grid, int tpc, const float *k,
 template <int WK>
 cudaError_t bwd_key_tc_dk(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
                           const float *gamma, const void *dout, const void *rec,
-                          const uint32_t *csr_q, uint32_t csr_mask, const uint32_t *off,
+                          const uint32_t *csr_q, const uint32_t *csr_k, uint32_t csr_mask,
+                          const uint32_t *off,
                           int64_t csr_stride, float *dk, void *dv, const float *own_dv,
                           const float *own_dk, cudaStream_t st) {
     switch (p.dK) {
-        case 1: return bwd_key_tc_launch<1, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+        case 1: return bwd_key_tc_launch<1, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
                                                 csr_mask, off, csr_stride, dk, dv, own_dv, own_dk,
                                                 st);
-        case 2: return bwd_key_tc_launch<2, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+        case 2: return bwd_key_tc_launch<2, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
                                                 csr_mask, off, csr_stride, dk, dv, own_dv, own_dk,
                                                 st);
-        case 3: return bwd_key_tc_launch<3, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+        case 3: return bwd_key_tc_launch<3, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
                                                 csr_mask, off, csr_stride, dk, dv, own_dv, own_dk,
                                                 st);
-        default: return bwd_key_tc_launch<4, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q,
+        default: return bwd_key_tc_launch<4, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
                                                  csr_mask, off, csr_stride, dk, dv, own_dv,
                                                  own_dk, st);
     }
@@ -1206,18 +1229,19 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
 
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
                               const void *dout, const void *rec, const uint32_t *csr_q,
-                              uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
+                              const uint32_t *csr_k, uint32_t csr_mask, const uint32_t *off,
+                              int64_t csr_stride,
                               float *dk, void *dv, const float *own_dv, const float *own_dk,
                               cudaStream_t st) {
     const int tpc = (p.C + T64 - 1) / T64;
     const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
     if (p.wk == kWSoftmax)
-        return bwd_key_tc_dk<kWSoftmax>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask,
+        return bwd_key_tc_dk<kWSoftmax>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k, csr_mask,
                                         off, csr_stride, dk, dv, own_dv, own_dk, st);
     if (p.wk == kWInvEuclid)
-        return bwd_key_tc_dk<kWInvEuclid>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask,
+        return bwd_key_tc_dk<kWInvEuclid>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k, csr_mask,
                                           off, csr_stride, dk, dv, own_dv, own_dk, st);
-    return bwd_key_tc_dk<kWCauchy>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_mask, off,
+    return bwd_key_tc_dk<kWCauchy>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k, csr_mask, off,
                                    csr_stride, dk, dv, own_dv, own_dk, st);
 }
 

@@ -172,11 +172,15 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
                                 float *dq, void *rec, float *dg_part, int32_t *status,
                                 cudaStream_t st);
 // csr_q holds the queries of every key's list (masked with csr_mask).
+// csr_q: the sorted list words (packed (key << 16) | query, csr_k null) or the
+// queries of the sorted (key, query) pairs with csr_k their keys; csr_mask
+// takes the query out of a word.
 // own_dv / own_dk: the own-chunk partial sums from launch_bwd_key_own_tc05, or
 // null for the key kernel to compute its own-chunk block itself.
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
                               const void *dout, const void *rec, const uint32_t *csr_q,
-                              uint32_t csr_mask, const uint32_t *off, int64_t csr_stride,
+                              const uint32_t *csr_k, uint32_t csr_mask, const uint32_t *off,
+                              int64_t csr_stride,
                               float *dk, void *dv, const float *own_dv, const float *own_dk,
                               cudaStream_t st);
 // The key side's own-chunk block on tcgen05 (C a multiple of 128, N of C;
