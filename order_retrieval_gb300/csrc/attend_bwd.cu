@@ -424,17 +424,23 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
             if (e != cudaSuccess) return e;
         }
         int ob = 0;
+        // the key walk needs a warp's 16 keys contiguous, not ordered by key;
+        // it skips the key half (8 keys) that none of 16 consecutive entries
+        // belongs to.  With packed words and chunks a multiple of 8 long, a
+        // sort by key / 8 keeps both.
         const bool packed = p.N <= 65536;
-        e = packed ? radix_sort_idx_packed(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st)
+        const bool groups = packed && p.C % 8 == 0;
+        e = packed ? radix_sort_idx_packed(idx, p.S, p.N, p.k, p.C, groups, w.rw, &ob, status, st)
                    : radix_sort_idx(idx, p.S, p.N, p.k, p.C, w.rw, &ob, status, st);
         if (e != cudaSuccess) return e;
         const int64_t L = p.N * (int64_t)p.k;
         const uint32_t *sorted = static_cast<const uint32_t *>(w.rw.keys[ob]);
-        csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(sorted, w.rw.seglen, L, p.N,
-                                                              packed ? 16 : 0, w.off);
+        const int kgs = groups ? 3 : 0;
+        csr_offsets<<<dim3(64, (unsigned)p.S), 256, 0, st>>>(sorted, w.rw.seglen, L, p.N >> kgs,
+                                                              packed ? 16 + kgs : 0, w.off);
         e = launch_bwd_key_tc(p, k, v, gamma, dout, w.rec, packed ? sorted : w.rw.vals[ob],
-                              packed ? nullptr : sorted, packed ? 0xffffu : 0xffffffffu, w.off, L,
-                              dk, dv, w.own_dv, w.own_dk, st);
+                              packed ? nullptr : sorted, packed ? 0xffffu : 0xffffffffu, kgs,
+                              w.off, L, dk, dv, w.own_dv, w.own_dk, st);
         if (e != cudaSuccess) return e;
         dgamma_reduce(p, w, dgamma, st);
         return cudaGetLastError();

@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(THREADS, 4)
 bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
            const float *__restrict__ gamma, const __nv_bfloat16 *__restrict__ dout,
            const QRec *__restrict__ rec, const uint32_t *__restrict__ csr_q,
-           const uint32_t *__restrict__ csr_k, uint32_t csr_mask,
+           const uint32_t *__restrict__ csr_k, uint32_t csr_mask, int kgs,
            const uint32_t *__restrict__ off, int64_t csr_stride, float *__restrict__ dk,
            __nv_bfloat16 *__restrict__ dv, const float *__restrict__ own_dv,
            const float *__restrict__ own_dk, int N, int H, int C, int tiles_per_chunk) {
@@ -695,12 +695,14 @@ bwd_key_tc(const float *__restrict__ kx, const __nv_bfloat16 *__restrict__ v,
     // ldmatrix; the two parts are added at the end.
     const uint32_t *lst = csr_q + seg * csr_stride;
     const uint32_t *klst = csr_k ? csr_k + seg * csr_stride : nullptr;
-    const uint32_t *ob = off + seg * (int64_t)(N + 1);
+    // list offsets per key (kgs = 0) or per 8-key group (kgs = 3: a warp's 16
+    // keys are then two groups)
+    const uint32_t *ob = off + seg * (int64_t)((N >> kgs) + 1);
     constexpr uint32_t kNone = 0xffffffffu;
     const int wj0 = j0 + warp * 16;
     const int nkw = max(0, min(16, jend - wj0));
-    const uint32_t P0 = nkw > 0 ? ob[wj0] : 0u;
-    const uint32_t P1 = nkw > 0 ? ob[wj0 + nkw] : 0u;
+    const uint32_t P0 = nkw > 0 ? ob[wj0 >> kgs] : 0u;
+    const uint32_t P1 = nkw > 0 ? ob[(wj0 + nkw) >> kgs] : 0u;
     const int nch = nkw > 0 ? (int)((P1 - P0 + 31) >> 5) : 0;
     const int g4 = lane >> 2, s4 = lane & 3;
     float kc[4] = {0.f, 0.f, 0.f, 0.f};                       // lane r: key r's coordinates
@@ -1172,7 +1174,7 @@ template <int D, int WK>
 cudaError_t bwd_key_tc_launch(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
                               const float *gamma, const void *dout, const void *rec,
                               const uint32_t *csr_q, const uint32_t *csr_k, uint32_t csr_mask,
-                              const uint32_t *off,
+                              int kgs, const uint32_t *off,
                               int64_t csr_stride, float *dk, void *dv, const float *own_dv,
                               const float *own_dk, cudaStream_t st) {
     static PerDeviceOnce smem_once;          // run once per device, outside any capture
@@ -1183,7 +1185,7 @@ cudaError_t bwd_key_tc_launch(const Prob &p, dim3 grid, int tpc, const float *k,
     if (e != cudaSuccess) return e;
     bwd_key_tc<D, WK><<<grid, THREADS, sizeof(KSmem), st>>>(
         k, static_cast<const __nv_bfloat16 *>(v), gamma, static_cast<const __nv_bfloat16 *>(dout),
-        static_cast<const QRec *>(rec), csr_q, csr_k, csr_mask, off, csr_stride, dk,
+        static_cast<const QRec *>(rec), csr_q, csr_k, csr_mask, kgs, off, csr_stride, dk,
         static_cast<__nv_bfloat16 *>(dv), own_dv, own_dk, p.N, p.H, p.C, tpc);
     return cudaGetLastError();
 }
@@ -1192,21 +1194,20 @@ template <int WK>
 cudaError_t bwd_key_tc_dk(const Prob &p, dim3 grid, int tpc, const float *k, const void *v,
                           const float *gamma, const void *dout, const void *rec,
                           const uint32_t *csr_q, const uint32_t *csr_k, uint32_t csr_mask,
-                          const uint32_t *off,
-                          int64_t csr_stride, float *dk, void *dv, const float *own_dv,
-                          const float *own_dk, cudaStream_t st) {
+                          int kgs, const uint32_t *off, int64_t csr_stride, float *dk, void *dv,
+                          const float *own_dv, const float *own_dk, cudaStream_t st) {
     switch (p.dK) {
         case 1: return bwd_key_tc_launch<1, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
-                                                csr_mask, off, csr_stride, dk, dv, own_dv, own_dk,
-                                                st);
+                                                csr_mask, kgs, off, csr_stride, dk, dv, own_dv,
+                                                own_dk, st);
         case 2: return bwd_key_tc_launch<2, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
-                                                csr_mask, off, csr_stride, dk, dv, own_dv, own_dk,
-                                                st);
+                                                csr_mask, kgs, off, csr_stride, dk, dv, own_dv,
+                                                own_dk, st);
         case 3: return bwd_key_tc_launch<3, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
-                                                csr_mask, off, csr_stride, dk, dv, own_dv, own_dk,
-                                                st);
+                                                csr_mask, kgs, off, csr_stride, dk, dv, own_dv,
+                                                own_dk, st);
         default: return bwd_key_tc_launch<4, WK>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
-                                                 csr_mask, off, csr_stride, dk, dv, own_dv,
+                                                 csr_mask, kgs, off, csr_stride, dk, dv, own_dv,
                                                  own_dk, st);
     }
 }
@@ -1229,19 +1230,22 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
 
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
                               const void *dout, const void *rec, const uint32_t *csr_q,
-                              const uint32_t *csr_k, uint32_t csr_mask, const uint32_t *off,
-                              int64_t csr_stride,
+                              const uint32_t *csr_k, uint32_t csr_mask, int kgs,
+                              const uint32_t *off, int64_t csr_stride,
                               float *dk, void *dv, const float *own_dv, const float *own_dk,
                               cudaStream_t st) {
     const int tpc = (p.C + T64 - 1) / T64;
     const dim3 grid((unsigned)(p.n * tpc), (unsigned)p.S);
     if (p.wk == kWSoftmax)
-        return bwd_key_tc_dk<kWSoftmax>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k, csr_mask,
+        return bwd_key_tc_dk<kWSoftmax>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
+                                        csr_mask, kgs,
                                         off, csr_stride, dk, dv, own_dv, own_dk, st);
     if (p.wk == kWInvEuclid)
-        return bwd_key_tc_dk<kWInvEuclid>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k, csr_mask,
+        return bwd_key_tc_dk<kWInvEuclid>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k,
+                                          csr_mask, kgs,
                                           off, csr_stride, dk, dv, own_dv, own_dk, st);
-    return bwd_key_tc_dk<kWCauchy>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k, csr_mask, off,
+    return bwd_key_tc_dk<kWCauchy>(p, grid, tpc, k, v, gamma, dout, rec, csr_q, csr_k, csr_mask,
+                                   kgs, off,
                                    csr_stride, dk, dv, own_dv, own_dk, st);
 }
 

@@ -174,13 +174,15 @@ cudaError_t launch_bwd_query_tc(const Prob &p, const float *q, const float *k, c
 // csr_q holds the queries of every key's list (masked with csr_mask).
 // csr_q: the sorted list words (packed (key << 16) | query, csr_k null) or the
 // queries of the sorted (key, query) pairs with csr_k their keys; csr_mask
-// takes the query out of a word.
+// takes the query out of a word.  off: per segment, the first list position of
+// each key (kgs = 0, N + 1 entries) or of each 8-key group (kgs = 3, N / 8 + 1
+// entries; C a multiple of 8).
 // own_dv / own_dk: the own-chunk partial sums from launch_bwd_key_own_tc05, or
 // null for the key kernel to compute its own-chunk block itself.
 cudaError_t launch_bwd_key_tc(const Prob &p, const float *k, const void *v, const float *gamma,
                               const void *dout, const void *rec, const uint32_t *csr_q,
-                              const uint32_t *csr_k, uint32_t csr_mask, const uint32_t *off,
-                              int64_t csr_stride,
+                              const uint32_t *csr_k, uint32_t csr_mask, int kgs,
+                              const uint32_t *off, int64_t csr_stride,
                               float *dk, void *dv, const float *own_dv, const float *own_dk,
                               cudaStream_t st);
 // The key side's own-chunk block on tcgen05 (C a multiple of 128, N of C;
@@ -229,9 +231,11 @@ cudaError_t radix_sort_idx(const int32_t *idx, int64_t S, int64_t N, int k, int 
 
 // The same transpose for N <= 65536 with each entry packed as (key << 16) |
 // query in one 32-bit word (keys only, no value array); sorted words land in
-// ws.keys[*out_buf].
+// ws.keys[*out_buf].  groups: ordered by key / 16 only (the entries of a
+// 16-key group contiguous, in query order, their keys mixed).
 cudaError_t radix_sort_idx_packed(const int32_t *idx, int64_t S, int64_t N, int k, int C,
-                                  RadixWs &ws, int *out_buf, int32_t *status, cudaStream_t st);
+                                  bool groups, RadixWs &ws, int *out_buf, int32_t *status,
+                                  cudaStream_t st);
 
 // Carve aligned sub-buffers out of a workspace.
 struct Carver {

@@ -1,4 +1,5 @@
-// radix.cu -- segmented, stable LSD radix sort of (key, value) pairs.
+// radix.cu -- segmented, stable LSD radix sort of (key, value) pairs (8-bit
+// digits; the transpose of idx can take a 5-bit digit for its first pass).
 //
 // The pages sort the Z-order codes with a radix sort (OpenReview discussion of
 // "ZETA: Leveraging Z-order Curves for Efficient Top-k Attention", reply A3
@@ -201,9 +202,10 @@ struct PackedSrc {         // later passes over packed words
     }
 };
 
-template <typename K, typename Src>
+template <typename K, typename Src, int DB>
 __global__ void __launch_bounds__(kRadixThreads)
 radix_upsweep(Src src, int shift, uint32_t *__restrict__ hist, int64_t tiles, int32_t *status) {
+    constexpr unsigned kMask = (1u << DB) - 1u;
     __shared__ uint32_t sh[256];
     const int64_t seg = blockIdx.y, tile = blockIdx.x;
     if (threadIdx.x < 256) sh[threadIdx.x] = 0;
@@ -217,7 +219,7 @@ radix_upsweep(Src src, int shift, uint32_t *__restrict__ hist, int64_t tiles, in
     src.load_run(seg, base + w * (32 * kRadixItems) + lane, len, key, val, ok, status);
 #pragma unroll
     for (int r = 0; r < kRadixItems; ++r)
-        if (ok[r]) atomicAdd(&sh[(unsigned)(key[r] >> shift) & 255u], 1u);
+        if (ok[r]) atomicAdd(&sh[(unsigned)(key[r] >> shift) & kMask], 1u);
     __syncthreads();
     if (threadIdx.x < 256) hist[(seg * tiles + tile) * 256 + threadIdx.x] = sh[threadIdx.x];
 }
@@ -280,10 +282,11 @@ constexpr size_t downsweep_smem() {
     return sizeof(K) * kRadixTile + sizeof(uint32_t) * kRadixTile;
 }
 
-template <typename K, typename Src>
+template <typename K, typename Src, int DB>
 __global__ void __launch_bounds__(kRadixThreads, Src::kDownBlocks)
 radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t tiles,
                 K *__restrict__ keys_out, uint32_t *__restrict__ vals_out, int64_t out_stride) {
+    constexpr unsigned kMask = (1u << DB) - 1u;
     constexpr int W = kRadixThreads / 32;
     __shared__ uint32_t soff[256];          // global start of each digit's run of this tile
     __shared__ uint32_t tds[256];           // tile-local start of each digit
@@ -309,17 +312,18 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
     uint32_t rank[kRadixItems];
     src.load_run(seg, base + w * (32 * kRadixItems) + lane, len, key, val, ok, nullptr);
 #pragma unroll
-    for (int r = 0; r < kRadixItems; ++r) dig[r] = ok[r] ? (int)((unsigned)(key[r] >> shift) & 255u) : 256;
+    for (int r = 0; r < kRadixItems; ++r)
+        dig[r] = ok[r] ? (int)((unsigned)(key[r] >> shift) & kMask) : 256;
 #pragma unroll
     for (int r = 0; r < kRadixItems; ++r) {
-        // lanes with this lane's digit: eight ballots, one per digit bit (far
+        // lanes with this lane's digit: one ballot per digit bit (far
         // cheaper here than a warp match); the lowest lane of each group bumps
         // the warp's counter for that digit and hands the old count to its group
         // (a warp's atomics on one counter take effect in program order, so
         // items keep their order)
         unsigned peers = __ballot_sync(kFull, dig[r] < 256);
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
+        for (int b = 0; b < DB; ++b) {
             const unsigned bal = __ballot_sync(kFull, (dig[r] >> b) & 1);
             peers &= ((dig[r] >> b) & 1) ? bal : ~bal;
         }
@@ -369,28 +373,28 @@ radix_downsweep(Src src, int shift, const uint32_t *__restrict__ hist, int64_t t
     // write each digit's run of the tile contiguously
     for (uint32_t t = threadIdx.x; t < nvalid; t += kRadixThreads) {
         const K kk = skey[t];
-        const int d = (int)((unsigned)(kk >> shift) & 255u);
+        const int d = (int)((unsigned)(kk >> shift) & kMask);
         const int64_t dst = (int64_t)soff[d] + (t - tds[d]);
         keys_out[seg * out_stride + dst] = kk;
         if constexpr (Src::kHasVal) vals_out[seg * out_stride + dst] = sval[t];
     }
 }
 
-template <typename K, typename Src>
+template <typename K, typename Src, int DB = 8>
 cudaError_t run_pass(const Src &src, int shift, int64_t S, int64_t maxlen, RadixWs &ws, int nxt,
                      int64_t out_stride, uint32_t *seglen_out, int32_t *status, cudaStream_t st) {
     const int64_t tiles = radix_tiles(maxlen);
     dim3 grid((unsigned)tiles, (unsigned)S);
-    radix_upsweep<K, Src><<<grid, kRadixThreads, 0, st>>>(src, shift, ws.hist, tiles, status);
+    radix_upsweep<K, Src, DB><<<grid, kRadixThreads, 0, st>>>(src, shift, ws.hist, tiles, status);
     radix_scan<<<(unsigned)S, 1024, 0, st>>>(ws.hist, tiles, seglen_out);
     static PerDeviceOnce smem_once;          // run once per device, outside any capture
     cudaError_t e = smem_once.run([] {
-        return cudaFuncSetAttribute(radix_downsweep<K, Src>,
+        return cudaFuncSetAttribute(radix_downsweep<K, Src, DB>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)downsweep_smem<K>());
     });
     if (e != cudaSuccess) return e;
-    radix_downsweep<K, Src><<<grid, kRadixThreads, downsweep_smem<K>(), st>>>(
+    radix_downsweep<K, Src, DB><<<grid, kRadixThreads, downsweep_smem<K>(), st>>>(
         src, shift, ws.hist, tiles, static_cast<K *>(ws.keys[nxt]), ws.vals[nxt], out_stride);
     return cudaGetLastError();
 }
@@ -449,10 +453,16 @@ cudaError_t radix_sort_idx(const int32_t *idx, int64_t S, int64_t N, int k, int 
 }
 
 cudaError_t radix_sort_idx_packed(const int32_t *idx, int64_t S, int64_t N, int k, int C,
-                                  RadixWs &ws, int *out_buf, int32_t *status, cudaStream_t st) {
+                                  bool groups, RadixWs &ws, int *out_buf, int32_t *status,
+                                  cudaStream_t st) {
     const int64_t L = N * (int64_t)k;
-    cudaError_t e = run_pass<uint32_t>(PackedIdxSrc{idx, N, k, slot_div(N, k, C)}, 16, S, L, ws, 0, L, ws.seglen,
-                                       status, st);
+    // by key: bits 16-23 then 24-31 of the words; by 8-key group: bits 19-23
+    // (a 5-bit digit) then 24-31
+    cudaError_t e = groups
+        ? run_pass<uint32_t, PackedIdxSrc, 5>(PackedIdxSrc{idx, N, k, slot_div(N, k, C)}, 19, S, L,
+                                               ws, 0, L, ws.seglen, status, st)
+        : run_pass<uint32_t>(PackedIdxSrc{idx, N, k, slot_div(N, k, C)}, 16, S, L, ws, 0, L,
+                             ws.seglen, status, st);
     if (e != cudaSuccess) return e;
     e = run_pass<uint32_t>(PackedSrc{static_cast<const uint32_t *>(ws.keys[0]), L, ws.seglen}, 24,
                            S, L, ws, 1, L, nullptr, nullptr, st);

@@ -374,6 +374,7 @@ def test_edge_shapes(kw, vd):
 
 TC = [
     dict(N=200, C=40, k=7),                 # chunks shorter than a query tile
+    dict(N=300, C=60, k=12),                # C not a multiple of 8: transpose sorted by key
     dict(N=480, C=96, k=33),                # one full tile plus a ragged one, k > 32
     dict(N=256, C=256, k=16),               # a single chunk: all local, four tiles
     dict(N=1024, C=128, k=128, d_K=1, bits=20),
@@ -395,7 +396,8 @@ TC = [
 def test_tensor_core_path(kw):
     """bf16 values with d_V = 64 run the tensor-core forward and backward;
     ragged tiles, k up to C, d_K from 1 to 4, the key side's own-chunk block
-    on tcgen05 and its fallback."""
+    on tcgen05 and its fallback, and the backward's transpose sorted by 8-key
+    group (C a multiple of 8) or by key."""
     base = dict(name="tc", B=2, H=2, N=256, d_K=3, d_V=64, k=8, C=64, bits=10, v_dtype="bf16",
                 gamma=(0.3, 1.0), dist="uniform", v_dist="normal", seed=21)
     base.update(kw)
