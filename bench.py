@@ -40,8 +40,8 @@ sys.path.insert(0, ROOT)
 # digest of the kernel's sources at that time.  The line reports the figure only
 # while the sources still have that digest (else null: the kernel has changed).
 ATTEND_FWD_TRAFFIC = {
-    "bytes": 211_861_504 + 50_557_952,
-    "sources_sha256": "4e4d73435e9e3b5bc6994bec20fdc4909d6ff8c506a9f88040815602d7a98a66",
+    "bytes": 211_924_736 + 50_113_280,
+    "sources_sha256": "037f32ff7eca627abd7ff16bfacea685f5e8dd124acbc86be79b11d99fe8d887",
     "capture": "attend_fwd_tc, efficiency_bf16_n65536, ncu --metrics "
                "dram__bytes_read.sum,dram__bytes_write.sum",
 }
@@ -511,14 +511,14 @@ def run_ours(args, w, rank, world):
                 out_done[bi].record(cp_out)
             started[bi] = True
 
-    # three timed trials of K steps each, the median reported: the host copies
+    # five timed trials of K steps each, the median reported: the host copies
     # share the machine's host memory and links with other jobs, which moves
-    # single trials by up to 15 %
+    # single trials by up to 20 %
     pipelined_steps(warm)
     torch.cuda.synchronize()
     barrier()
     e2e_trials = []
-    for _ in range(3):
+    for _ in range(5):
         t_a = ev()
         t_a.record(cp_in)
         pipelined_steps(args.steps)
@@ -877,7 +877,7 @@ def run_ours(args, w, rank, world):
                 "how": "pinned host buffers; per step H2D of q, k, v, gamma, dO, the five calls, "
                        "D2H of out, dq, dk, dv, dgamma; three buffer sets, copies on side "
                        "streams overlapping the neighbouring steps' compute on a third; median "
-                       "of three trials of K steps",
+                       "of five trials of K steps",
                 "trials": e2e_trials,
                 "serial_value": e2e_serial},
         "gpu_launches": launches_per_step(w) * args.steps,
