@@ -20,14 +20,18 @@
 //                  32-byte record {q_i, 1/s_i, gbar_i} for the key side.
 // Key side, one CTA per 64 keys of a chunk:
 //   window part  - the queries that selected key j (a transpose of idx sorted
-//                  by query): a warp walks the lists of its 16 keys as one run,
-//                  32 entries per step, the step's dO rows staged in a ring one
-//                  step ahead; G = dO_rows . V_keys^T and dV_keys += dO^T A on
-//                  the tensor cores, dk_j += dL/dw_ij (-2 dw/d(d^2)) (q_i - k_j)
-//                  summed per key by a segmented scan.
+//                  by key, or by 8-key group): a warp walks the lists of its 16
+//                  keys as one run, 32 entries per step, the step's dO rows
+//                  staged in a ring one step ahead; G = dO_rows . V_keys^T and
+//                  dV_keys += dO^T A on the tensor cores, and dk_j += dL/dw_ij
+//                  (-2 dw/d(d^2)) (q_i - k_j) summed per key on the tensor
+//                  cores as well (one-hot keys times the entries' terms).
 //   own chunk    - S^T = V . dO^T on tensor cores, the element-wise terms, then
 //                  dV += P^T . dO with P^T re-packed from the accumulator
-//                  fragments (their layout is the A-fragment layout).
+//                  fragments (their layout is the A-fragment layout).  Where
+//                  it applies (C a multiple of 128, H <= 64, aligned inputs)
+//                  the separate tcgen05 kernel of bwd_own_tc05.cu does this
+//                  part and the walk adds its sums.
 // Other weight kernels (flags; reply A3 "Justification for Euclidean Distance
 // Claim") swap in their w, dw/d(d^2) and dw/dgamma.  The softmax keeps a running
 // shift m per query on the query side (the sums are moved onto a lower shift
@@ -129,10 +133,6 @@ __host__ __device__ inline size_t q_smem_bytes(int k) {
 // sc = exp(dm / gamma^2) and subtracts dm 2/gamma^3 w from each e.
 struct QAcc {
     float x[12];
-    __device__ void zero() {
-#pragma unroll
-        for (int y = 0; y < 12; ++y) x[y] = 0.f;
-    }
     __device__ void rebase(float dm, float sc, float k2) {
         x[2] -= dm * k2 * x[1];
         x[3] -= dm * k2 * x[0];
