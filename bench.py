@@ -435,7 +435,8 @@ def run_ours(args, w, rank, world):
     # (the e2e figure): NSETS device buffer sets; step n+1's inputs go up on a
     # copy stream while step n computes, and step n's results come down on
     # another while step n+1 computes, a set being reused only after its
-    # previous results are down.  Both time every copy of every step.
+    # previous results are down; each set's five calls are replayed as one
+    # CUDA graph.  Both time every copy of every step.
     NSETS = 3
     out_h = [torch.empty(plan.out.numel(), dtype=plan.out.dtype).pin_memory()
              for _ in range(NSETS)]
@@ -474,8 +475,21 @@ def run_ours(args, w, rank, world):
     e2e_serial = tokens / (sum(e2e_ms) / len(e2e_ms) * 1e-3)
 
     plans = [plan] + [ZetaPlan(p, dev) for _ in range(NSETS - 1)]
-    dev_in = [(q, k, v, gamma, dout)] + [tuple(torch.empty_like(t) for t in (q, k, v, gamma, dout))
+    dev_in = [(q, k, v, gamma, dout)] + [tuple(t.clone() for t in (q, k, v, gamma, dout))
                                          for _ in range(NSETS - 1)]
+    # each set's five calls as one CUDA graph, as in the timed step (one eager
+    # pass of every set first)
+    for bi in range(1, NSETS):
+        plans[bi].forward(*dev_in[bi][:4])
+        plans[bi].backward(*dev_in[bi])
+    torch.cuda.synchronize()
+    comp_graphs = []
+    for bi in range(NSETS):
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_):
+            plans[bi].forward(*dev_in[bi][:4])
+            plans[bi].backward(*dev_in[bi])
+        comp_graphs.append(g_)
     # compute on a stream of its own: on the legacy default stream the steps'
     # kernels would serialise with the copies on the other streams
     comp = torch.cuda.Stream(dev)
@@ -485,12 +499,17 @@ def run_ours(args, w, rank, world):
     in_ready = [ev() for _ in range(NSETS)]
     started = [False] * NSETS
 
-    def pipelined_steps(n):
+    def pipelined_steps(n, stages=None):
+        # stages: if given, gets per step the start events of its H2D copies,
+        # compute and D2H copies (their ends are in_ready, comp_done, out_done)
         for it in range(n):
             bi = it % NSETS
+            st3 = [ev(), ev(), ev()] if stages is not None else None
             with torch.cuda.stream(cp_in):
                 if started[bi]:
                     cp_in.wait_event(comp_done[bi])       # the set's previous step computed
+                if st3:
+                    st3[0].record(cp_in)
                 for src, dst in zip(ins_h, dev_in[bi]):
                     dst.copy_(src, non_blocking=True)
                 in_ready[bi].record(cp_in)
@@ -498,18 +517,28 @@ def run_ours(args, w, rank, world):
             if started[bi]:
                 comp.wait_event(out_done[bi])             # and its results copied out
             with torch.cuda.stream(comp):
-                qq, kk_, vv, gg, dd = dev_in[bi]
-                plans[bi].forward(qq, kk_, vv, gg)
-                plans[bi].backward(qq, kk_, vv, gg, dd)
+                if st3:
+                    st3[1].record(comp)
+                comp_graphs[bi].replay()
                 if world > 1:
                     dist.all_reduce(plans[bi].dgamma)
                 comp_done[bi].record(comp)
             with torch.cuda.stream(cp_out):
                 cp_out.wait_event(comp_done[bi])
+                if st3:
+                    st3[2].record(cp_out)
                 for src, dst in zip(outs(plans[bi]), hosts(bi)):
                     dst.copy_(src, non_blocking=True)
                 out_done[bi].record(cp_out)
             started[bi] = True
+            if st3:
+                # the end events are reused by later steps: time them now, on
+                # copies of this step's ends
+                ends = [ev(), ev(), ev()]
+                ends[0].record(cp_in)
+                ends[1].record(comp)
+                ends[2].record(cp_out)
+                stages.append((st3, ends))
 
     # five timed trials of K steps each, the median reported: the host copies
     # share the machine's host memory and links with other jobs, which moves
@@ -517,22 +546,28 @@ def run_ours(args, w, rank, world):
     pipelined_steps(warm)
     torch.cuda.synchronize()
     barrier()
-    e2e_trials = []
+    e2e_trials, e2e_host_ms, e2e_stage_ms = [], [], []
     for _ in range(5):
         t_a = ev()
         t_a.record(cp_in)
-        pipelined_steps(args.steps)
+        h0 = time.perf_counter()
+        stages = []
+        pipelined_steps(args.steps, stages)
         t_b = ev()
         t_b.record(cp_out)
+        e2e_host_ms.append((time.perf_counter() - h0) * 1e3)     # host enqueue of the trial
         t_b.synchronize()
         torch.cuda.synchronize()
+        # mean H2D, compute and D2H time per step of the trial
+        e2e_stage_ms.append([statistics.mean(st[i].elapsed_time(en[i]) for st, en in stages)
+                             for i in range(3)])
         tt = torch.tensor([t_a.elapsed_time(t_b)], dtype=torch.float64, device=dev)
         if world > 1:
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_trials.append(tokens * args.steps / (float(tt.item()) * 1e-3))
         barrier()
     e2e = statistics.median(e2e_trials)
-    del plans, dev_in
+    del comp_graphs, plans, dev_in
 
     # --- efficiency workload: forward alone, and the attend-forward kernel roofline
     we = W.EFFICIENCY.replace(seed=W.EFFICIENCY.seed + 1000 * rank)
@@ -874,11 +909,14 @@ def run_ours(args, w, rank, world):
             "unit": "GB/s"},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "how": "pinned host buffers; per step H2D of q, k, v, gamma, dO, the five calls, "
-                       "D2H of out, dq, dk, dv, dgamma; three buffer sets, copies on side "
+                "how": "pinned host buffers; per step H2D of q, k, v, gamma, dO, the five calls "
+                       "(one CUDA graph per buffer set), D2H of out, dq, dk, dv, dgamma; three "
+                       "buffer sets, copies on side "
                        "streams overlapping the neighbouring steps' compute on a third; median "
                        "of five trials of K steps",
                 "trials": e2e_trials,
+                "trial_host_enqueue_ms": e2e_host_ms,
+                "trial_step_h2d_compute_d2h_ms": e2e_stage_ms,
                 "serial_value": e2e_serial},
         "gpu_launches": launches_per_step(w) * args.steps,
         "cpu_baseline": {"value": oracle_tokens_per_s(w, w.N, cpu_dt), "unit": "tokens/s",
