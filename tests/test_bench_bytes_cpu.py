@@ -14,8 +14,8 @@ Per query-head (bf16 values, d_V = 64, d_K = 3, 4-byte indices and floats):
   dO row on the key side (2 * 128 B), coordinates twice (2 * 12 B) and four
   index words (idx read twice, the transpose written and read: 16 B) = 296 B;
   per query dO (128 B), q and dq (24 B) and 16 B of scalars handed to the key
-  side = 168 B; per key
-  its own-chunk k, v and dO rows (3 * 140 B) and dk, dv (140 B) = 560 B.
+  side = 168 B; per key its own-chunk k, v and dO rows (3 * 140 B) and dk, dv
+  (140 B) = 560 B.
   48 * 296 + 168 + 560 = 14,936 B.
 """
 import os
