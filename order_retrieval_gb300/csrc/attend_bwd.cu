@@ -427,7 +427,8 @@ cudaError_t launch_attend_bwd(const Prob &p, const float *q, const float *k, con
         // the key walk needs a warp's 16 keys contiguous, not ordered by key;
         // it skips the key half (8 keys) that none of 16 consecutive entries
         // belongs to.  With packed words and chunks a multiple of 8 long, a
-        // sort by key / 8 keeps both.
+        // sort by key / 8 keeps both (N, a multiple of C, is then one of 8 too,
+        // so every group is whole).
         const bool packed = p.N <= 65536;
         const bool groups = packed && p.C % 8 == 0;
         e = packed ? radix_sort_idx_packed(idx, p.S, p.N, p.k, p.C, groups, w.rw, &ob, status, st)
