@@ -265,7 +265,10 @@ zeta_status_t zeta_project_encode(const zeta_problem_t *p, const zeta_proj_t *pj
  * selects, see zeta_weight_t) and s_i = sum_j w_ij:
  * out_i = sum_j w_ij v_j / s_i, rowsum_i = s_i.
  *   q, k    in : float [B, H, N, d_K]
- *   v       in : v_dtype [B, H, N, d_V]  (16-B aligned)
+ *   v       in : v_dtype [B, H, N, d_V]  (16-B aligned; the tensor-core kernel
+ *                (bf16, d_V = 64, d_K <= 4) reads value rows 32 bytes at a time
+ *                and runs only where v is 32-B aligned, the general kernel
+ *                otherwise)
  *   gamma   in : float [H]
  *   idx     in : int32 [B, H, N, k]; entries must be -1 or in [0, cC)
  *   out     out: v_dtype [B, H, N, d_V]  (16-B aligned)
@@ -284,10 +287,11 @@ zeta_status_t zeta_attend_fwd(const zeta_problem_t *p, const float *q, const flo
  * Passage: as for those two calls (OpenReview reply A3 "Chunking ... & Where
  * efficiency is coming from": binary search of the insertion position; the
  * attended set and weights of zeta_attend_fwd).
- * On the tensor-core shapes (bf16 values, d_V = 64, d_K <= 4) one kernel finds
- * each query's window by binary search in its sorted prefix, reads the window
- * as a contiguous run of prefix_idx, attends, and writes the run to idx for
- * zeta_attend_bwd; other shapes run the two calls one after the other.
+ * On the tensor-core shapes (bf16 values, d_V = 64, d_K <= 4, v 32-B aligned)
+ * one kernel finds each query's window by binary search in its sorted prefix,
+ * reads the window as a contiguous run of prefix_idx, attends, and writes the
+ * run to idx for zeta_attend_bwd; otherwise the two calls run one after the
+ * other.
  * Results are those of zeta_select_topk followed by zeta_attend_fwd.
  *   q, k, v, gamma   in : as for zeta_attend_fwd
  *   q_codes          in : codes of the queries [B, H, N]

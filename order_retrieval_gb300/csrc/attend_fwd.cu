@@ -158,7 +158,8 @@ cudaError_t fwd_generic_dispatch(const Prob &p, const float *q, const float *k, 
 cudaError_t launch_attend_fwd(const Prob &p, const float *q, const float *k, const void *v,
                               const float *gamma, const int32_t *idx, void *out, float *rowsum,
                               int32_t *status, cudaStream_t st) {
-    if (attend_fwd_tc_supported(p))
+    // the tensor-core kernel reads value rows 32 bytes at a time
+    if (attend_fwd_tc_supported(p) && (reinterpret_cast<uintptr_t>(v) & 31u) == 0)
         return launch_attend_fwd_tc(p, q, k, v, gamma, idx, out, rowsum, status, st);
     if (p.vdt == ZETA_BF16)
         return fwd_generic_dispatch<__nv_bfloat16>(p, q, k, v, gamma, idx, out, rowsum, status,

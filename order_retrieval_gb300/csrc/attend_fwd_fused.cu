@@ -50,7 +50,8 @@ cudaError_t launch_select_attend_fwd(const Prob &p, const float *q, const float 
                                      const void *prefix_codes, const int32_t *prefix_idx,
                                      int32_t *idx, void *out, float *rowsum, int32_t *status,
                                      cudaStream_t st) {
-    if (!attend_fwd_tc_supported(p)) {
+    // the fused kernel is the tensor-core forward: value rows read 32 bytes at a time
+    if (!attend_fwd_tc_supported(p) || (reinterpret_cast<uintptr_t>(v) & 31u) != 0) {
         cudaError_t e = launch_select(p, q_codes, prefix_codes, prefix_idx, idx, st);
         if (e != cudaSuccess) return e;
         return launch_attend_fwd(p, q, k, v, gamma, idx, out, rowsum, status, st);

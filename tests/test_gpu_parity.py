@@ -15,7 +15,7 @@ from order_retrieval_gb300 import binding as zb
 from order_retrieval_gb300 import workloads as W
 
 from gpu_util import (Run, assert_close_bf16, assert_close_f32, codes_np, dev_vals,
-                      in_threads, slice_inputs)
+                      host_vals, in_threads, slice_inputs)
 
 pytestmark = [
     pytest.mark.gpu,
@@ -408,6 +408,35 @@ def test_tensor_core_path(kw):
         _check_forward_slice(run, s, bf16=True)
         _check_backward_slice(run, s, bf16=True)
     assert_close_bf16(run.grads()[3], _dgamma_ref(run), what="dgamma")
+
+
+def test_values_not_32_byte_aligned():
+    """v at a 16-byte but not 32-byte boundary: the tensor-core forward reads
+    value rows 32 bytes at a time, so the two-call and the fused forward both
+    take the general kernel; their results match the oracle."""
+    w = W.Workload(name="tc", B=1, H=2, N=512, d_K=3, d_V=64, k=16, C=128, bits=10,
+                   v_dtype="bf16", gamma=(0.3, 1.0), dist="uniform", v_dist="normal", seed=23)
+    run = Run(w)
+    pl = run.plan
+    buf = torch.empty(run.v.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    v16 = buf[8:]
+    v16.copy_(run.v)
+    assert v16.data_ptr() % 32 == 16
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, rowsum = torch.empty_like(pl.out), torch.empty_like(pl.rowsum)
+    zb.zeta_attend_fwd(run.p, run.q, run.k, v16, run.gamma, pl.idx, out, rowsum, status)
+    idx2 = torch.empty_like(pl.idx)
+    out2, rowsum2 = torch.empty_like(pl.out), torch.empty_like(pl.rowsum)
+    zb.zeta_select_attend_fwd(run.p, run.q, run.k, v16, run.gamma, pl.q_codes, pl.prefix_codes,
+                              pl.prefix_idx, idx2, out2, rowsum2, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for o, rs, ix in ((out, rowsum, pl.idx), (out2, rowsum2, idx2)):
+        o_h = host_vals(o).reshape(run.S, run.N, w.d_V)
+        rs_h = rs.cpu().numpy().astype(np.float64).reshape(run.S, run.N)
+        ix_h = ix.cpu().numpy().reshape(run.S, run.N, w.k)
+        for s in range(run.S):
+            _check_forward_host(w, run.g, s, ix_h[s], o_h[s], rs_h[s], bf16=True)
 
 
 def test_empty_problem_is_a_no_op():
