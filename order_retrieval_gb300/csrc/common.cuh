@@ -231,8 +231,8 @@ cudaError_t radix_sort_idx(const int32_t *idx, int64_t S, int64_t N, int k, int 
 
 // The same transpose for N <= 65536 with each entry packed as (key << 16) |
 // query in one 32-bit word (keys only, no value array); sorted words land in
-// ws.keys[*out_buf].  groups: ordered by key / 16 only (the entries of a
-// 16-key group contiguous, in query order, their keys mixed).
+// ws.keys[*out_buf].  groups: ordered by key / 8 only (the entries of an
+// 8-key group contiguous, in query order, their keys mixed).
 cudaError_t radix_sort_idx_packed(const int32_t *idx, int64_t S, int64_t N, int k, int C,
                                   bool groups, RadixWs &ws, int *out_buf, int32_t *status,
                                   cudaStream_t st);

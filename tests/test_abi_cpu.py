@@ -101,6 +101,8 @@ def test_null_pointers_and_workspace(L):
     bws = zb.zeta_bwd_workspace_bytes(p)
     args = [fake] * 10
     assert L.zeta_attend_bwd(P, *args, None, bws, None, None) == 3
+    assert L.zeta_attend_bwd(P, *args, ctypes.c_void_p(0x10000), bws - 1, None, None) == 3
+    assert L.zeta_attend_bwd(P, *args, ctypes.c_void_p(0x10010), bws, None, None) == 3
     # Unaligned value pointers are refused.
     odd = ctypes.c_void_p(0x1002)
     assert L.zeta_attend_fwd(P, fake, fake, odd, fake, fake, fake, fake, None, None) == 1
